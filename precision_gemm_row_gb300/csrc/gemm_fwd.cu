@@ -1,0 +1,381 @@
+// Forward FP4 GEMM of the quantized linear layer on sm_103a tensor cores.
+//
+// The page "首个 FP4 精度的大模型训练框架来了" (czzqal.com), GeMM passage,
+// describes a custom FP4 GEMM kernel that stages FP4 A and B through FP16 in
+// shared memory and emulates the FP4 tile multiply on FP8 tensor cores (no FP4
+// hardware existed then).  sm_103a multiplies E2M1 natively, so this kernel
+// instead feeds the packed codes by TMA straight into 128-byte-swizzled shared
+// memory and runs tcgen05.mma kind::mxf4 with every UE8M0 block scale equal to
+// 1.0, accumulating exactly in fp32 in tensor memory (every product is a
+// multiple of 1/4 of magnitude <= 36, so sums stay exact for K <= 16384).
+//
+// The epilogue applies the per-row and per-column scales (they factor out of
+// the K-sum: A is quantized per token and W per channel, granularity passage)
+// and adds the sparse compensation dA*W (outlier passage), then stores Y.
+//
+// Structure: persistent CTAs (one per SM), 192 threads:
+//   warp 0  TMA producer (one elected lane issues),
+//   warp 1  TMEM allocator and MMA issuer (one lane issues, commits to mbarriers),
+//   warps 2-5 epilogue, warp w reading TMEM lanes 32*(w%4) .. +31 (one output row per thread).
+// Every mbarrier wait is bounded; on expiry the CTA records FP4_FLAG_TIMEOUT,
+// drains its TMA loads and MMAs, frees TMEM and exits.
+#include "common.cuh"
+
+namespace fp4 {
+namespace {
+
+constexpr int kBM = 128;          // rows of A per tile (TMEM lanes)
+constexpr int kBKBytes = 128;     // bytes of K per stage = 256 E2M1 values (one swizzle row)
+constexpr int kMmaKBytes = 32;    // 64 E2M1 values per MMA
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+
+template <int BN, int NACC>
+struct FwdCfg {
+  static constexpr int kAStage = kBM * kBKBytes;
+  static constexpr int kBStage = BN * kBKBytes;
+  static constexpr int kStageBytes = kAStage + kBStage;
+  static constexpr int kStages = (196 * 1024) / kStageBytes;
+  // scale-factor columns (all bytes 0x7F = 2^0) after the accumulators
+  static constexpr uint32_t kSfaCol = ((NACC * BN + 15) / 16) * 16;
+  static constexpr uint32_t kSfbCol = kSfaCol + 16;
+  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * NACC + 1) + 16;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static_assert(kSfbCol + 16 <= kTmemCols, "accumulators and scale factors exceed TMEM");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "invalid N tile");
+  static_assert(kStages >= 2, "too few pipeline stages");
+};
+
+// Instruction descriptor, kind::mxf4: A and B E2M1 (format 1), both K-major,
+// UE8M0 scale type, M = 128, N = BN, dense K = 64, scale-factor ids 0.
+template <int BN>
+__host__ __device__ constexpr uint32_t idesc_mxf4() {
+  return (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (1u << 23) | (uint32_t(kBM >> 4) << 24);
+}
+
+struct FwdParams {
+  const float* s_a;
+  const float* s_w;
+  const int32_t* rp;
+  const int32_t* ci;
+  const float* cv;
+  const uint16_t* W;
+  int64_t ldw;
+  void* Y;
+  int64_t ldy;
+  int y_type;
+  int M, N, K;
+  uint32_t* status;
+  uint64_t wait_ns;
+};
+
+template <int BN, int NACC>
+__global__ void __launch_bounds__(kThreads, 1)
+    fp4_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const FwdParams p) {
+  using C = FwdCfg<BN, NACC>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::kStages * C::kAStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 2 * NACC + 1);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * C::kStages;
+  const uint32_t accf0 = empty0 + 8 * C::kStages;
+  const uint32_t acce0 = accf0 + 8 * NACC;
+  const uint32_t done_bar = acce0 + 8 * NACC;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < NACC; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, 4);
+    }
+    mbar_init(done_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= 2) {  // unit block scales: every scale byte = 0x7F (2^0)
+    const uint32_t lb = uint32_t((warp & 3) * 32) << 16;
+    tmem_st8_fill(tmem + lb + C::kSfaCol, 0x7F7F7F7Fu);
+    tmem_st8_fill(tmem + lb + C::kSfaCol + 8, 0x7F7F7F7Fu);
+    tmem_st8_fill(tmem + lb + C::kSfbCol, 0x7F7F7F7Fu);
+    tmem_st8_fill(tmem + lb + C::kSfbCol + 8, 0x7F7F7F7Fu);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const int num_m = (p.M + kBM - 1) / kBM;
+  const int num_n = (p.N + BN - 1) / BN;
+  const int tiles = num_m * num_n;
+  const int kblocks = (p.K / 2 + kBKBytes - 1) / kBKBytes;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      const int mb = tile % num_m, nb = tile / num_m;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_arrive_expect_tx(fb, C::kStageBytes);
+          tma_load_2d(smem_u32(sA + stage * C::kAStage), &tmA, fb, kb * kBKBytes, mb * kBM);
+          tma_load_2d(smem_u32(sB + stage * C::kBStage), &tmB, fb, kb * kBKBytes, nb * BN);
+        }
+        __syncwarp();
+        ++issued;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    // wait for the last load armed on every stage before the CTA may exit
+    for (int s = 0; s < C::kStages; ++s) {
+      const uint32_t n_s = issued / C::kStages + (uint32_t(s) < issued % C::kStages ? 1u : 0u);
+      if (n_s > 0 && !mbar_wait(full0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
+        atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    constexpr uint32_t idesc = idesc_mxf4<BN>();
+    const uint32_t sfa = tmem + C::kSfaCol, sfb = tmem + C::kSfbCol;
+    const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + uint32_t(acc * BN);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = a_base + stage * C::kAStage, b0 = b_base + stage * C::kBStage;
+#pragma unroll
+          for (int k = 0; k < kBKBytes / kMmaKBytes; ++k) {
+            const uint64_t ad = smem_desc_sw128(a0 + k * kMmaKBytes, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b0 + k * kMmaKBytes, 16, 1024);
+            mma_mxf4(d_tmem, ad, bd, idesc, sfa, sfb, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty0 + 8 * stage);
+        }
+        __syncwarp();
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(accf0 + 8 * acc);
+      __syncwarp();
+      if (++acc == NACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    // every MMA issued by this thread must finish before TMEM is released
+    if (lane == 0) tc_commit(done_bar);
+    __syncwarp();
+    if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+  } else {
+    // ------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int r_local = q * 32 + lane;
+    const uint32_t lane_base = uint32_t(q * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    const bool raw = (p.y_type == FP4_OUT_RAW_ACC_FP32);
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+      const int mb = tile % num_m, nb = tile / num_m;
+      if (!mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int row = mb * kBM + r_local;
+      const bool row_ok = row < p.M;
+      float inv_sa = 1.0f;
+      int e0 = 0, e1 = 0;
+      if (row_ok && !raw) {
+        inv_sa = 1.0f / __ldg(p.s_a + row);
+        if (p.rp) {
+          e0 = __ldg(p.rp + row);
+          e1 = __ldg(p.rp + row + 1);
+        }
+      }
+      for (int c = 0; c < BN; c += 16) {
+        const int col0 = nb * BN + c;
+        if (col0 >= p.N) break;  // same for the whole warp
+        const int nvalid = (p.N - col0) >= 16 ? 16 : (p.N - col0);  // 8 or 16 (N % 8 == 0)
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_base + uint32_t(acc * BN + c), r);
+        tmem_wait_ld();
+        float y[16];
+        if (raw) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) y[t] = __uint_as_float(r[t]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float sw = t < nvalid ? __ldg(p.s_w + col0 + t) : 1.0f;
+            y[t] = __uint_as_float(r[t]) * inv_sa * (1.0f / sw);
+          }
+          for (int e = e0; e < e1; ++e) {
+            const int k = __ldg(p.ci + e);
+            const float v = __ldg(p.cv + e);
+            const uint4* wr = reinterpret_cast<const uint4*>(p.W + int64_t(k) * p.ldw + col0);
+            uint4 w0 = __ldg(wr);
+            uint4 w1 = nvalid > 8 ? __ldg(wr + 1) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+              y[t] = fmaf(v, bf16_bits_to_float((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu), y[t]);
+          }
+        }
+        if (row_ok) {
+          if (p.y_type == FP4_OUT_BF16) {
+            uint32_t packed[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * t], y[2 * t + 1]);
+              packed[t] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.Y) + int64_t(row) * p.ldy + col0);
+            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            if (nvalid > 8) dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + int64_t(row) * p.ldy + col0);
+            dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+            dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+            if (nvalid > 8) {
+              dst[2] = make_float4(y[8], y[9], y[10], y[11]);
+              dst[3] = make_float4(y[12], y[13], y[14], y[15]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+      if (++acc == NACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+constexpr int kFwdBN = 256;
+constexpr int kFwdAcc = 1;
+
+}  // namespace
+}  // namespace fp4
+
+FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_bytes, const float* s_a,
+                                  const uint8_t* w_codes_t, int64_t ldw_codes_bytes, const float* s_w, int64_t M,
+                                  int64_t N, int64_t K, const int32_t* dA_row_ptr, const int32_t* dA_col,
+                                  const float* dA_val, const void* W, int64_t ldw, void* Y, int y_type, int64_t ldy,
+                                  fp4_stream_t stream) {
+  using namespace fp4;
+  using C = FwdCfg<kFwdBN, kFwdAcc>;
+  if (!a_codes || !w_codes_t || !Y) return FP4_ERR_INVALID_ARG;
+  if (y_type != FP4_OUT_BF16 && y_type != FP4_OUT_FP32 && y_type != FP4_OUT_RAW_ACC_FP32) return FP4_ERR_INVALID_ARG;
+  const bool raw = (y_type == FP4_OUT_RAW_ACC_FP32);
+  if (!raw && (!s_a || !s_w)) return FP4_ERR_INVALID_ARG;
+  const int ncsr = (dA_row_ptr != nullptr) + (dA_col != nullptr) + (dA_val != nullptr);
+  if (ncsr != 0 && ncsr != 3) return FP4_ERR_INVALID_ARG;
+  const bool comp = (ncsr == 3) && !raw;
+  if (comp && !W) return FP4_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || N % 8 != 0 || M >= (int64_t(1) << 31) ||
+      N >= (int64_t(1) << 31) || K > 16384)
+    return FP4_ERR_SHAPE;
+  if (lda_codes_bytes < K / 2 || ldw_codes_bytes < K / 2 || ldy < N || (comp && ldw < N)) return FP4_ERR_SHAPE;
+  if (lda_codes_bytes % 16 || ldw_codes_bytes % 16 || !aligned16(a_codes) || !aligned16(w_codes_t) || !aligned16(Y) ||
+      ldy % 8 || (comp && (!aligned16(W) || ldw % 8)))
+    return FP4_ERR_ALIGNMENT;
+  int sms = 0;
+  fp4_status st = check_device(&sms);
+  if (st != FP4_OK) return st;
+
+  CUtensorMap tmA, tmB;
+  st = encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, uint64_t(K / 2), uint64_t(M),
+                      uint64_t(lda_codes_bytes), kBKBytes, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != FP4_OK) return st;
+  st = encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_codes_t, uint64_t(K / 2), uint64_t(N),
+                      uint64_t(ldw_codes_bytes), kBKBytes, kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != FP4_OK) return st;
+
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto kern = fp4_fwd_kernel<kFwdBN, kFwdAcc>;
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+      return FP4_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  FwdParams p;
+  p.s_a = s_a;
+  p.s_w = s_w;
+  p.rp = comp ? dA_row_ptr : nullptr;
+  p.ci = comp ? dA_col : nullptr;
+  p.cv = comp ? dA_val : nullptr;
+  p.W = static_cast<const uint16_t*>(W);
+  p.ldw = ldw;
+  p.Y = Y;
+  p.ldy = ldy;
+  p.y_type = y_type;
+  p.M = int(M);
+  p.N = int(N);
+  p.K = int(K);
+  p.status = status_word();
+  p.wait_ns = kWaitLimitNs;
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kFwdBN - 1) / kFwdBN);
+  const int grid = int(tiles < sms ? tiles : sms);
+  kern<<<grid, kThreads, C::kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmB, p);
+  return launch_status();
+}

@@ -1,0 +1,326 @@
+// Weight gradient of the quantized linear layer with the differentiable
+// gradient estimator (DGE), on sm_103a tensor cores.
+//
+// The page "首个 FP4 精度的大模型训练框架来了" (czzqal.com), DGE passage: the
+// derivative of the hard quantizer is almost everywhere 0, so the forward pass
+// keeps hard quantization while the backward pass refits the quantizer with a
+// continuous differentiable function and uses its derivative as a correction
+// of the weight gradient (also the abstract of "Optimizing Large Language Model
+// Training Using FP4 Quantization").  The function is not printed on the pages;
+// the one used is a per-interval power function:
+//   x = |fl32(W s_W)|, [lo, lo + delta] the E2M1 interval holding x,
+//   u = 2 (x - lo) / delta - 1,  f'(x) = min(clip, (1/k) |u|^(1/k - 1)),  f' = 1/k for x >= 6.
+//
+// G = A^T dY is a BF16 GEMM with both operands stored with the reduction
+// (token) dimension strided, i.e. MN-major: TMA loads [64 tokens x 64
+// features] boxes with 128-byte swizzle and tcgen05.mma kind::f16 reads them
+// through MN-major descriptors, so no transpose copy is ever made.  The fp32
+// accumulator is double-buffered in TMEM (2 x 256 columns) so the DGE epilogue
+// of one tile overlaps the main loop of the next.  Same warp roles and bounded
+// waits as the forward kernel.
+#include "common.cuh"
+
+namespace fp4 {
+namespace {
+
+constexpr int kBM = 128;      // rows of dW (input features) per tile
+constexpr int kBN = 256;      // columns of dW (output features) per tile
+constexpr int kBT = 64;       // tokens per stage
+constexpr int kMmaT = 16;     // tokens per MMA (BF16 K = 16)
+constexpr int kThreads = 192;
+constexpr int kNAcc = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBox = 64;                          // features per TMA box (128 bytes of BF16)
+constexpr int kBoxBytes = kBox * kBT * 2;         // 8 KB
+constexpr int kAStage = (kBM / kBox) * kBoxBytes; // 16 KB
+constexpr int kBStage = (kBN / kBox) * kBoxBytes; // 32 KB
+constexpr int kStageBytes = kAStage + kBStage;
+constexpr int kStages = 4;
+constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNAcc + 1) + 16;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B BF16, both
+// MN-major, N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
+                            (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+
+struct WgradParams {
+  const uint16_t* W;
+  int64_t ldw;
+  const float* s_w;
+  float* dW;
+  int64_t lddw;
+  int M, N, K;
+  float inv_k, expo, clip;
+  uint32_t* status;
+  uint64_t wait_ns;
+};
+
+// DGE factor f'(x) for the scaled weight magnitude x.
+__device__ __forceinline__ float dge_factor(float x, float inv_k, float expo, float clip) {
+  if (!(x < 6.0f)) return inv_k;
+  float lo, delta;
+  if (x < 2.0f) {
+    delta = 0.5f;
+    lo = floorf(x * 2.0f) * 0.5f;
+  } else if (x < 4.0f) {
+    delta = 1.0f;
+    lo = floorf(x);
+  } else {
+    delta = 2.0f;
+    lo = 4.0f;
+  }
+  const float u = fabsf(2.0f * (x - lo) / delta - 1.0f);
+  return fminf(clip, inv_k * powf(u, expo));  // u = 0 gives +inf, clipped
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    wgrad_dge_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
+                     const WgradParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kAStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2 * kNAcc + 1);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kStages;
+  const uint32_t accf0 = empty0 + 8 * kStages;
+  const uint32_t acce0 = accf0 + 8 * kNAcc;
+  const uint32_t done_bar = acce0 + 8 * kNAcc;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmG);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < kNAcc; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, 4);
+    }
+    mbar_init(done_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int num_r = (p.K + kBM - 1) / kBM;
+  const int num_n = (p.N + kBN - 1) / kBN;
+  const int tiles = num_r * num_n;
+  const int tblocks = (p.M + kBT - 1) / kBT;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      const int rb = tile % num_r, nb = tile / num_r;
+      for (int tb = 0; tb < tblocks; ++tb) {
+        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          const uint32_t a_dst = smem_u32(sA + stage * kAStage);
+          const uint32_t b_dst = smem_u32(sB + stage * kBStage);
+#pragma unroll
+          for (int h = 0; h < kBM / kBox; ++h) tma_load_2d(a_dst + h * kBoxBytes, &tmA, fb, rb * kBM + h * kBox, tb * kBT);
+#pragma unroll
+          for (int h = 0; h < kBN / kBox; ++h) tma_load_2d(b_dst + h * kBoxBytes, &tmG, fb, nb * kBN + h * kBox, tb * kBT);
+        }
+        __syncwarp();
+        ++issued;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    for (int s = 0; s < kStages; ++s) {
+      const uint32_t n_s = issued / kStages + (uint32_t(s) < issued % kStages ? 1u : 0u);
+      if (n_s > 0 && !mbar_wait(full0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
+        atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + uint32_t(acc * kBN);
+      for (int tb = 0; tb < tblocks; ++tb) {
+        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = a_base + stage * kAStage, b0 = b_base + stage * kBStage;
+#pragma unroll
+          for (int k = 0; k < kBT / kMmaT; ++k) {
+            // MN-major, 128-byte swizzle: 64-feature atoms kBoxBytes apart (LBO),
+            // 8-token groups 1024 bytes apart (SBO); 16 tokens = 2048 bytes per MMA.
+            const uint64_t ad = smem_desc_sw128(a0 + k * (kMmaT * 128), kBoxBytes, 1024);
+            const uint64_t bd = smem_desc_sw128(b0 + k * (kMmaT * 128), kBoxBytes, 1024);
+            mma_f16(d_tmem, ad, bd, kIdesc, (tb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty0 + 8 * stage);
+        }
+        __syncwarp();
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(accf0 + 8 * acc);
+      __syncwarp();
+      if (++acc == kNAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    if (lane == 0) tc_commit(done_bar);
+    __syncwarp();
+    if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+  } else {
+    // ------------------------------------------------ DGE epilogue
+    const int q = warp & 3;
+    const int r_local = q * 32 + lane;
+    const uint32_t lane_base = uint32_t(q * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+      const int rb = tile % num_r, nb = tile / num_r;
+      if (!mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int row = rb * kBM + r_local;
+      const bool row_ok = row < p.K;
+      for (int c = 0; c < kBN; c += 16) {
+        const int col0 = nb * kBN + c;
+        if (col0 >= p.N) break;
+        const int nvalid = (p.N - col0) >= 16 ? 16 : (p.N - col0);
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_base + uint32_t(acc * kBN + c), r);
+        tmem_wait_ld();
+        if (row_ok) {
+          const uint4* wr = reinterpret_cast<const uint4*>(p.W + int64_t(row) * p.ldw + col0);
+          const uint4 w0 = __ldg(wr);
+          const uint4 w1 = nvalid > 8 ? __ldg(wr + 1) : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          float o[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float sw = t < nvalid ? __ldg(p.s_w + col0 + t) : 1.0f;
+            const float w = bf16_bits_to_float((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu);
+            const float x = fabsf(__fmul_rn(w, sw));
+            o[t] = __uint_as_float(r[t]) * dge_factor(x, p.inv_k, p.expo, p.clip);
+          }
+          float4* dst = reinterpret_cast<float4*>(p.dW + int64_t(row) * p.lddw + col0);
+          dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+          dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+          if (nvalid > 8) {
+            dst[2] = make_float4(o[8], o[9], o[10], o[11]);
+            dst[3] = make_float4(o[12], o[13], o[14], o[15]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+      if (++acc == kNAcc) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+}  // namespace fp4
+
+FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* dY, int64_t lddy, const void* W,
+                                        int64_t ldw, const float* s_w, int64_t M, int64_t N, int64_t K, float dge_k,
+                                        float dge_clip, float* dW, int64_t lddw, fp4_stream_t stream) {
+  using namespace fp4;
+  if (!A || !dY || !W || !s_w || !dW) return FP4_ERR_INVALID_ARG;
+  if (!(dge_k > 0.0f) || !(dge_clip > 0.0f) || !isfinite(dge_k)) return FP4_ERR_INVALID_ARG;
+  if (M < 1 || N < 8 || K < 8 || N % 8 || K % 8 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
+      K >= (int64_t(1) << 31))
+    return FP4_ERR_SHAPE;
+  if (lda < K || lddy < N || ldw < N || lddw < N) return FP4_ERR_SHAPE;
+  if (lda % 8 || lddy % 8 || ldw % 8 || lddw % 4 || !aligned16(A) || !aligned16(dY) || !aligned16(W) ||
+      !aligned16(dW) || (reinterpret_cast<uintptr_t>(s_w) & 3u))
+    return FP4_ERR_ALIGNMENT;
+  int sms = 0;
+  fp4_status st = check_device(&sms);
+  if (st != FP4_OK) return st;
+  CUtensorMap tmA, tmG;
+  st = encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, uint64_t(K), uint64_t(M), uint64_t(lda) * 2, kBox,
+                      kBT, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != FP4_OK) return st;
+  st = encode_tmap_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, uint64_t(N), uint64_t(M), uint64_t(lddy) * 2, kBox,
+                      kBT, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != FP4_OK) return st;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(wgrad_dge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+        cudaSuccess)
+      return FP4_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  WgradParams p;
+  p.W = static_cast<const uint16_t*>(W);
+  p.ldw = ldw;
+  p.s_w = s_w;
+  p.dW = dW;
+  p.lddw = lddw;
+  p.M = int(M);
+  p.N = int(N);
+  p.K = int(K);
+  p.inv_k = 1.0f / dge_k;
+  p.expo = 1.0f / dge_k - 1.0f;
+  p.clip = dge_clip;
+  p.status = status_word();
+  p.wait_ns = kWaitLimitNs;
+  const int64_t tiles = ((K + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const int grid = int(tiles < sms ? tiles : sms);
+  wgrad_dge_kernel<<<grid, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmG, p);
+  return launch_status();
+}

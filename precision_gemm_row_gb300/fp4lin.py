@@ -1,0 +1,248 @@
+"""Python binding of libfp4lin.so (ctypes), argument marshalling only.
+
+Every function has the name of the C entry point it calls and takes torch CUDA
+tensors.  Outputs that are not passed in are allocated with torch (PyTorch is
+used for device memory and streams only); every step of the computation runs
+in the library's CUDA kernels.  There is no fallback: if the library is not
+built, importing this module raises ImportError, and a non-zero status from the
+library raises FP4Error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp4lin.so")
+
+FP4_OUT_BF16, FP4_OUT_FP32, FP4_OUT_RAW_ACC_FP32 = 0, 1, 2
+_OUT_TYPES = {"bf16": FP4_OUT_BF16, "fp32": FP4_OUT_FP32, "raw": FP4_OUT_RAW_ACC_FP32}
+FLAG_TIMEOUT, FLAG_CAPACITY, FLAG_INTERNAL = 0x1, 0x2, 0x4
+
+# exported symbols, in the order include/fp4lin.h declares them
+EXPORTS = (
+    "fp4_status_string", "fp4_abi_version", "fp4_quantize_rows", "fp4_quantize_cols_workspace",
+    "fp4_quantize_cols", "outlier_max_nnz", "outlier_clamp_quantile_workspace", "outlier_clamp_quantile",
+    "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_device_status", "fp4_selftest_bounded_wait",
+)
+
+
+class FP4Error(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} ({status})")
+        self.status = status
+        self.status_name = msg
+
+
+_c_i64, _c_sz, _c_vp, _c_int, _c_f, _c_d, _c_u32 = (ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int,
+                                                    ctypes.c_float, ctypes.c_double, ctypes.c_uint32)
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built: run precision_gemm_row_gb300.build.build() (needs nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    sig = {
+        "fp4_status_string": (ctypes.c_char_p, [_c_int]),
+        "fp4_abi_version": (_c_int, []),
+        "fp4_quantize_rows": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp]),
+        "fp4_quantize_cols_workspace": (_c_sz, [_c_i64]),
+        "fp4_quantize_cols": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]),
+        "outlier_max_nnz": (_c_i64, [_c_i64, _c_i64, _c_d]),
+        "outlier_clamp_quantile_workspace": (_c_sz, [_c_i64, _c_i64, _c_i64]),
+        "outlier_clamp_quantile": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_d, _c_vp, _c_vp, _c_vp, _c_vp,
+                                            _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_sz, _c_vp]),
+        "fp4_linear_fwd": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp,
+                                    _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_i64, _c_vp]),
+        "fp4_linear_wgrad_dge": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64,
+                                          _c_i64, _c_f, _c_f, _c_vp, _c_i64, _c_vp]),
+        "fp4_device_status": (_c_int, [_c_vp, ctypes.POINTER(_c_u32)]),
+        "fp4_selftest_bounded_wait": (_c_int, [_c_u32, _c_vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = load_library()
+
+
+def status_string(status: int) -> str:
+    return _lib.fp4_status_string(status).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise FP4Error(fn, status, status_string(status))
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _rowmajor(t: torch.Tensor, name: str, dtype: torch.dtype) -> int:
+    if not t.is_cuda or t.dtype != dtype or t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D row-major CUDA {dtype} tensor (got {t.dtype}, {tuple(t.shape)}, "
+                         f"strides {t.stride()}, device {t.device})")
+    return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), t.shape[1])
+
+
+def abi_version() -> int:
+    return _lib.fp4_abi_version()
+
+
+# ---------------------------------------------------------------- quantizers
+
+def fp4_quantize_rows(A: torch.Tensor, clamp_t: Optional[torch.Tensor] = None, codes: Optional[torch.Tensor] = None,
+                      scales: Optional[torch.Tensor] = None, stream=None):
+    """Row-wise E2M1 quantization of A (M x K, BF16); returns (codes M x K/2 uint8, scales M fp32)."""
+    lda = _rowmajor(A, "A", torch.bfloat16)
+    M, K = A.shape
+    if codes is None:
+        codes = torch.empty((M, K // 2), dtype=torch.uint8, device=A.device)
+    if scales is None:
+        scales = torch.empty((M,), dtype=torch.float32, device=A.device)
+    ldc = _rowmajor(codes, "codes", torch.uint8)
+    _check("fp4_quantize_rows", _lib.fp4_quantize_rows(_p(A), M, K, lda, _p(clamp_t), _p(codes), ldc, _p(scales),
+                                                       _s(stream)))
+    return codes, scales
+
+
+def fp4_quantize_cols_workspace(N: int) -> int:
+    return int(_lib.fp4_quantize_cols_workspace(N))
+
+
+def fp4_quantize_cols(W: torch.Tensor, codes_t: Optional[torch.Tensor] = None, scales: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None):
+    """Column-wise E2M1 quantization of W (K x N, BF16); returns (codes_t N x K/2 uint8, scales N fp32)."""
+    ldw = _rowmajor(W, "W", torch.bfloat16)
+    K, N = W.shape
+    if codes_t is None:
+        codes_t = torch.empty((N, K // 2), dtype=torch.uint8, device=W.device)
+    if scales is None:
+        scales = torch.empty((N,), dtype=torch.float32, device=W.device)
+    ws_bytes = fp4_quantize_cols_workspace(N)
+    if workspace is None:
+        workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=W.device)
+    ldc = _rowmajor(codes_t, "codes_t", torch.uint8)
+    _check("fp4_quantize_cols", _lib.fp4_quantize_cols(_p(W), K, N, ldw, _p(codes_t), ldc, _p(scales), _p(workspace),
+                                                       workspace.numel() * workspace.element_size(), _s(stream)))
+    return codes_t, scales
+
+
+# ---------------------------------------------------------------- outlier clamp
+
+def outlier_max_nnz(M: int, K: int, q: float) -> int:
+    return int(_lib.outlier_max_nnz(M, K, float(q)))
+
+
+def outlier_clamp_quantile_workspace(M: int, K: int, nnz_capacity: int) -> int:
+    return int(_lib.outlier_clamp_quantile_workspace(M, K, nnz_capacity))
+
+
+def outlier_clamp_quantile(A: torch.Tensor, q: float, want_clamped: bool = False,
+                           out: Optional[Dict[str, torch.Tensor]] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """Quantile threshold t of |A|, CSR of dA = A - A_clamped (and A_clamped on request).
+
+    Returns a dict with t (1 fp32), row_ptr (M+1 int32), col_idx / vals (capacity-sized;
+    the first nnz entries are valid), nnz (1 int64) and, if asked, A_clamped."""
+    lda = _rowmajor(A, "A", torch.bfloat16)
+    M, K = A.shape
+    cap = outlier_max_nnz(M, K, q)
+    dev = A.device
+    o = dict(out) if out is not None else {}
+    o.setdefault("t", torch.empty((1,), dtype=torch.float32, device=dev))
+    o.setdefault("row_ptr", torch.empty((M + 1,), dtype=torch.int32, device=dev))
+    o.setdefault("col_idx", torch.empty((max(cap, 1),), dtype=torch.int32, device=dev))
+    o.setdefault("vals", torch.empty((max(cap, 1),), dtype=torch.float32, device=dev))
+    o.setdefault("nnz", torch.empty((1,), dtype=torch.int64, device=dev))
+    ws_bytes = outlier_clamp_quantile_workspace(M, K, cap)
+    o.setdefault("workspace", torch.empty((ws_bytes,), dtype=torch.uint8, device=dev))
+    if want_clamped:
+        o.setdefault("A_clamped", torch.empty_like(A))
+    ac = o.get("A_clamped") if want_clamped else None
+    ldac = _rowmajor(ac, "A_clamped", torch.bfloat16) if ac is not None else 0
+    ws = o["workspace"]
+    _check("outlier_clamp_quantile", _lib.outlier_clamp_quantile(
+        _p(A), M, K, lda, float(q), _p(o["t"]), _p(o["row_ptr"]), _p(o["col_idx"]), _p(o["vals"]),
+        o["col_idx"].numel(), _p(o["nnz"]), _p(ac), ldac, _p(ws), ws.numel(), _s(stream)))
+    return o
+
+
+# ---------------------------------------------------------------- GEMMs
+
+def fp4_linear_fwd(a_codes: torch.Tensor, s_a: Optional[torch.Tensor], w_codes_t: torch.Tensor,
+                   s_w: Optional[torch.Tensor], K: int, csr: Optional[Dict[str, torch.Tensor]] = None,
+                   W: Optional[torch.Tensor] = None, out_type: str = "bf16", Y: Optional[torch.Tensor] = None,
+                   stream=None) -> torch.Tensor:
+    """Y = (qA qW^T) / (s_A s_W^T) [+ dA W]; out_type 'bf16', 'fp32' or 'raw' (unscaled accumulator)."""
+    lda_c = _rowmajor(a_codes, "a_codes", torch.uint8)
+    ldw_c = _rowmajor(w_codes_t, "w_codes_t", torch.uint8)
+    M, N = a_codes.shape[0], w_codes_t.shape[0]
+    yt = _OUT_TYPES[out_type]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16 if yt == FP4_OUT_BF16 else torch.float32, device=a_codes.device)
+    ldy = _rowmajor(Y, "Y", torch.bfloat16 if yt == FP4_OUT_BF16 else torch.float32)
+    rp = ci = cv = None
+    ldw = 0
+    if csr is not None:
+        rp, ci, cv = csr["row_ptr"], csr["col_idx"], csr["vals"]
+        ldw = _rowmajor(W, "W", torch.bfloat16)
+    _check("fp4_linear_fwd", _lib.fp4_linear_fwd(
+        _p(a_codes), lda_c, _p(s_a), _p(w_codes_t), ldw_c, _p(s_w), M, N, K, _p(rp), _p(ci), _p(cv), _p(W), ldw,
+        _p(Y), yt, ldy, _s(stream)))
+    return Y
+
+
+def fp4_linear_wgrad_dge(A: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, s_w: torch.Tensor,
+                         dge_k: float = 5.0, dge_clip: float = 3.0, dW: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """dW = (A^T dY) * f'(|W s_W|), fp32 (K x N)."""
+    lda = _rowmajor(A, "A", torch.bfloat16)
+    lddy = _rowmajor(dY, "dY", torch.bfloat16)
+    ldw = _rowmajor(W, "W", torch.bfloat16)
+    M, K = A.shape
+    N = dY.shape[1]
+    if dW is None:
+        dW = torch.empty((K, N), dtype=torch.float32, device=A.device)
+    lddw = _rowmajor(dW, "dW", torch.float32)
+    _check("fp4_linear_wgrad_dge", _lib.fp4_linear_wgrad_dge(
+        _p(A), lda, _p(dY), lddy, _p(W), ldw, _p(s_w), M, N, K, float(dge_k), float(dge_clip), _p(dW), lddw,
+        _s(stream)))
+    return dW
+
+
+# ---------------------------------------------------------------- status
+
+def fp4_device_status(stream=None):
+    """Synchronizes the stream; returns (status name, flags) and clears the device flags."""
+    flags = ctypes.c_uint32(0)
+    st = _lib.fp4_device_status(_s(stream), ctypes.byref(flags))
+    return status_string(st), int(flags.value)
+
+
+def fp4_selftest_bounded_wait(timeout_us: int, stream=None) -> None:
+    _check("fp4_selftest_bounded_wait", _lib.fp4_selftest_bounded_wait(int(timeout_us), _s(stream)))
+
+
+# ---------------------------------------------------------------- one layer
+
+def linear_forward(A: torch.Tensor, W: torch.Tensor, q: float, out_type: str = "bf16", stream=None):
+    """The whole forward of the quantized linear layer: quantile clamp + CSR,
+    row quantization of A_clamped (fused clamp), column quantization of W,
+    FP4 GEMM with scales and compensation.  Returns (Y, intermediates)."""
+    o = outlier_clamp_quantile(A, q, stream=stream)
+    a_codes, s_a = fp4_quantize_rows(A, clamp_t=o["t"], stream=stream)
+    w_codes_t, s_w = fp4_quantize_cols(W, stream=stream)
+    Y = fp4_linear_fwd(a_codes, s_a, w_codes_t, s_w, A.shape[1], csr=o, W=W, out_type=out_type, stream=stream)
+    return Y, dict(outlier=o, a_codes=a_codes, s_a=s_a, w_codes_t=w_codes_t, s_w=s_w)

@@ -1,0 +1,37 @@
+"""Helpers shared by the GPU parity tests: host <-> device transfer of BF16 bit
+patterns and the comparison rules (bit-exact, BF16 ulp distance, relative
+Frobenius error)."""
+import numpy as np
+import torch
+
+BF16_ULP_TOL = 1          # final BF16 outputs: within 1 BF16 ulp
+FROB_TOL = 1e-5           # compensated fp32 outputs and DGE weight gradients
+
+
+def dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bf16_ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    """Distance in BF16 ulps between two BF16 bit patterns (+0 and -0 coincide)."""
+    def key(b):
+        b = np.asarray(b, dtype=np.uint16).astype(np.int64)
+        mag = b & 0x7FFF
+        return np.where(b & 0x8000, -mag, mag)
+    return np.abs(key(a_bits) - key(b_bits))
+
+
+def rel_frobenius(got: np.ndarray, ref: np.ndarray) -> float:
+    ref = np.asarray(ref, dtype=np.float64)
+    num = np.linalg.norm(np.asarray(got, dtype=np.float64) - ref)
+    den = np.linalg.norm(ref)
+    return float(num / den) if den > 0 else float(num)
+
+
+def assert_no_device_flags(fp4lin):
+    name, flags = fp4lin.fp4_device_status()
+    assert flags == 0 and name == "FP4_OK", (name, flags)

@@ -1,0 +1,249 @@
+"""GPU parity of every kernel against the CPU oracle, element by element, on
+seeded inputs at sizes the oracle finishes in seconds: several tiles, ragged
+tails in M, N and K, and the degenerate cases (zero rows, negative zeros, ties,
+q = 1, all-equal magnitudes).  All calls go through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import fp4_linear as orc
+from precision_gemm_row_gb300 import workloads as wl
+from tests.gpu_common import (BF16_ULP_TOL, FROB_TOL, assert_no_device_flags, bf16_ulp_distance, dev_bf16,
+                              host_bits, rel_frobenius)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fp4():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from precision_gemm_row_gb300 import build
+    build.build()
+    from precision_gemm_row_gb300 import fp4lin
+    return fp4lin
+
+
+def _normal_bits(seed, shape, std=1.0):
+    rng = np.random.default_rng(seed)
+    return wl.f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * np.float32(std))
+
+
+def _t3_bits(seed, shape, scale=1.0):
+    rng = np.random.default_rng(seed)
+    return wl.f32_to_bf16_bits(rng.standard_t(3, size=shape).astype(np.float32) * np.float32(scale))
+
+
+# ---------------------------------------------------------------- bounded waits
+
+def test_bounded_wait_times_out_and_context_survives(fp4):
+    fp4.fp4_selftest_bounded_wait(2000)          # 2 ms wait on an mbarrier nobody completes
+    name, flags = fp4.fp4_device_status()
+    assert name == "FP4_ERR_TIMEOUT" and flags & fp4.FLAG_TIMEOUT
+    assert fp4.fp4_device_status() == ("FP4_OK", 0)   # flags were cleared
+    x = torch.ones(1024, device="cuda")
+    assert float(x.sum()) == 1024.0                    # context still usable
+
+
+# ---------------------------------------------------------------- row / column quantization
+
+@pytest.mark.parametrize("M,K", [(256, 512), (37, 96), (5, 4096), (3, 13824), (130, 11008), (1, 32)])
+def test_quantize_rows_bit_exact(fp4, M, K):
+    A_bits = _normal_bits(M * 7 + K, (M, K))
+    A_bits[0, :] = 0                      # zero row -> scale 1, all codes 0
+    if M > 2:
+        A_bits[2, ::3] = 0x8000           # negative zeros keep their sign
+        A_bits[1, 5] = wl.f32_to_bf16_bits(np.array([60.0], np.float32))[0]
+    codes, s = fp4.fp4_quantize_rows(dev_bf16(A_bits))
+    ref_codes, ref_s = orc.quantize_rows(orc.bf16_to_f32(A_bits))
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
+    assert_no_device_flags(fp4)
+
+
+def test_quantize_rows_with_fused_clamp_bit_exact(fp4):
+    A_bits = _t3_bits(1, (96, 640), 2.0)
+    t, _, _ = orc.quantile_threshold(A_bits, 0.97)
+    A_c, _, _, _ = orc.clamp_and_compensation(A_bits, t)
+    ref_codes, ref_s = orc.quantize_rows(A_c)
+    t_dev = torch.tensor([float(t)], dtype=torch.float32, device="cuda")
+    codes, s = fp4.fp4_quantize_rows(dev_bf16(A_bits), clamp_t=t_dev)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
+
+
+def test_quantize_rows_strided_input(fp4):
+    A_bits = _normal_bits(3, (20, 200))
+    big = dev_bf16(A_bits)
+    view = big[:, :160]                   # lda = 200 > K = 160
+    codes = torch.full((20, 96), 0xAB, dtype=torch.uint8, device="cuda")   # ldc 96 > K/2, padding kept
+    fp4.fp4_quantize_rows(view, codes=codes)
+    ref_codes, _ = orc.quantize_rows(orc.bf16_to_f32(A_bits[:, :160]))
+    got = codes.cpu().numpy()
+    assert np.array_equal(got[:, :80], ref_codes)
+    assert np.all(got[:, 80:] == 0xAB)
+
+
+@pytest.mark.parametrize("K,N", [(512, 512), (96, 40), (2048, 264), (64, 8)])
+def test_quantize_cols_bit_exact(fp4, K, N):
+    W_bits = _normal_bits(K + N, (K, N), 0.02)
+    W_bits[:, 1] = 0                      # zero column
+    codes_t, s = fp4.fp4_quantize_cols(dev_bf16(W_bits))
+    ref_codes, ref_s = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(codes_t.cpu().numpy(), ref_codes)
+
+
+# ---------------------------------------------------------------- quantile, clamp, CSR
+
+def _check_outlier(fp4, A_bits, q, want_clamped=True):
+    o = fp4.outlier_clamp_quantile(dev_bf16(A_bits), q, want_clamped=want_clamped)
+    torch.cuda.synchronize()
+    t, t_bits, k = orc.quantile_threshold(A_bits, q)
+    A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
+    assert o["t"].cpu().numpy().view(np.uint32)[0] == np.float32(t).view(np.uint32)
+    nnz = int(o["nnz"].item())
+    assert nnz == rp[-1]
+    assert np.array_equal(o["row_ptr"].cpu().numpy(), rp)
+    assert np.array_equal(o["col_idx"][:nnz].cpu().numpy(), ci)
+    assert np.array_equal(o["vals"][:nnz].cpu().numpy().view(np.uint32), cv.view(np.uint32))
+    if want_clamped:
+        assert np.array_equal(host_bits(o["A_clamped"]), (A_c.view(np.uint32) >> 16).astype(np.uint16))
+    assert_no_device_flags(fp4)
+    return o
+
+
+@pytest.mark.parametrize("q", [0.99, 0.9, 0.5, 0.999, 1.0, 1e-7])
+def test_outlier_clamp_c1_shape(fp4, q):
+    lin = wl.WORKLOADS["c1_single_linear_256x512x512"].linears[0]
+    A_bits = wl.WORKLOADS["c1_single_linear_256x512x512"].activation(lin)
+    _check_outlier(fp4, A_bits, q)
+
+
+@pytest.mark.parametrize("shape,q", [((300, 136), 0.97), ((1, 8), 0.5), ((7, 1000), 0.999), ((2048, 64), 0.99)])
+def test_outlier_clamp_ragged_and_heavy_tails(fp4, shape, q):
+    _check_outlier(fp4, _t3_bits(shape[0] + shape[1], shape, 3.0), q)
+
+
+def test_outlier_clamp_heavy_ties_and_zeros(fp4):
+    rng = np.random.default_rng(5)
+    vals = wl.f32_to_bf16_bits(np.array([0.5, -0.5, 1.0, -2.0, 2.0, 3.0], np.float32))
+    A_bits = rng.choice(vals, size=(64, 96))
+    for q in (0.3, 0.6, 0.95, 1.0):
+        _check_outlier(fp4, A_bits, q)
+    _check_outlier(fp4, np.zeros((16, 32), np.uint16), 0.9)          # t = 0, nothing clamped
+
+
+def test_outlier_clamp_repeated_calls_reuse_workspace(fp4):
+    A1 = _t3_bits(11, (128, 256))
+    A2 = _t3_bits(12, (128, 256), 10.0)
+    o = _check_outlier(fp4, A1, 0.99)
+    o2 = fp4.outlier_clamp_quantile(dev_bf16(A2), 0.99, out={"workspace": o["workspace"]})
+    t, _, _ = orc.quantile_threshold(A2, 0.99)
+    assert float(o2["t"].item()) == float(t)
+
+
+# ---------------------------------------------------------------- DGE weight gradient
+
+@pytest.mark.parametrize("M,K,N", [(64, 128, 256), (256, 512, 512), (200, 136, 264), (1000, 384, 520)])
+@pytest.mark.parametrize("k,clip", [(5.0, 3.0), (1.0, 3.0)])
+def test_wgrad_dge(fp4, M, K, N, k, clip):
+    A_bits = _normal_bits(M + 1, (M, K))
+    dY_bits = _normal_bits(N + 2, (M, N), 1e-3)
+    W_bits = _normal_bits(K + 3, (K, N), 0.02)
+    _, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+    dW = fp4.fp4_linear_wgrad_dge(dev_bf16(A_bits), dev_bf16(dY_bits), dev_bf16(W_bits),
+                                  torch.from_numpy(s_w).cuda(), k, clip)
+    ref = orc.wgrad_dge(A_bits, dY_bits, W_bits, s_w, k, clip)
+    err = rel_frobenius(dW.cpu().numpy(), ref)
+    assert err <= FROB_TOL, err
+    assert_no_device_flags(fp4)
+
+
+# ---------------------------------------------------------------- FP4 GEMM
+
+def _random_codes(seed, rows, K):
+    return np.random.default_rng(seed).integers(0, 256, size=(rows, K // 2), dtype=np.uint8)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 512), (300, 520, 1056), (1, 8, 32), (129, 264, 96),
+                                   (640, 1024, 2048)])
+def test_gemm_raw_accumulator_bit_exact(fp4, M, N, K):
+    a = _random_codes(M + K, M, K)
+    w = _random_codes(N + K, N, K)
+    Y = fp4.fp4_linear_fwd(torch.from_numpy(a).cuda(), None, torch.from_numpy(w).cuda(), None, K, out_type="raw")
+    ref = orc.gemm_raw(a, w).astype(np.float32)
+    got = Y.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), np.argwhere(got != ref)[:5]
+    assert_no_device_flags(fp4)
+
+
+@pytest.mark.parametrize("sign_pattern", ["all_pos", "alternating"])
+def test_gemm_raw_exact_at_maximum_K(fp4, sign_pattern):
+    # every product 6*6 = 36: the largest sums the exactness bound allows (K = 16384)
+    M, N, K = 128, 256, 16384
+    a = np.full((M, K // 2), 0x77, np.uint8)
+    w = np.full((N, K // 2), 0x77, np.uint8)
+    if sign_pattern == "alternating":
+        a[::2] = 0xFF                       # rows of -6
+        w[:, ::3] = 0xF7                    # every 3rd byte: (+6, -6)
+    Y = fp4.fp4_linear_fwd(torch.from_numpy(a).cuda(), None, torch.from_numpy(w).cuda(), None, K, out_type="raw")
+    ref = orc.gemm_raw(a, w).astype(np.float32)
+    assert np.array_equal(Y.cpu().numpy(), ref)
+    if sign_pattern == "all_pos":
+        assert float(Y[0, 0]) == 36.0 * K
+
+
+@pytest.mark.parametrize("M,N,K,q", [(256, 512, 512, 0.99), (300, 520, 1056, 0.97), (129, 264, 96, 0.9)])
+def test_linear_fwd_scaled_and_compensated(fp4, M, N, K, q):
+    A_bits = _t3_bits(M, (M, K), 2.0)
+    W_bits = _normal_bits(N, (K, N), 0.02)
+    t, _, _ = orc.quantile_threshold(A_bits, q)
+    A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
+    a_codes, s_a = orc.quantize_rows(A_c)
+    w_codes, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    csr = {"row_ptr": d(rp), "col_idx": d(ci if ci.size else np.zeros(1, np.int32)),
+           "vals": d(cv if cv.size else np.zeros(1, np.float32))}
+    W = dev_bf16(W_bits)
+    args = (d(a_codes), d(s_a), d(w_codes), d(s_w), K)
+    y_comp = orc.linear_fwd(a_codes, s_a, w_codes, s_w, rp, ci, cv, W_bits)
+    y_plain = orc.linear_fwd(a_codes, s_a, w_codes, s_w)
+    # BF16, compensated: within 1 ulp of the correctly rounded fp64 result
+    yb = fp4.fp4_linear_fwd(*args, csr=csr, W=W, out_type="bf16")
+    dist = bf16_ulp_distance(host_bits(yb), orc.f64_to_bf16(y_comp))
+    assert dist.max() <= BF16_ULP_TOL, np.argwhere(dist > BF16_ULP_TOL)[:5]
+    # BF16 without compensation
+    yb0 = fp4.fp4_linear_fwd(*args, out_type="bf16")
+    assert bf16_ulp_distance(host_bits(yb0), orc.f64_to_bf16(y_plain)).max() <= BF16_ULP_TOL
+    # fp32, compensated: relative Frobenius
+    yf = fp4.fp4_linear_fwd(*args, csr=csr, W=W, out_type="fp32")
+    assert rel_frobenius(yf.cpu().numpy(), y_comp) <= FROB_TOL
+    assert_no_device_flags(fp4)
+
+
+def test_linear_fwd_output_leading_dimension(fp4):
+    M, N, K = 130, 48, 64
+    a = _random_codes(1, M, K)
+    w = _random_codes(2, N, K)
+    Y = torch.full((M, 64), -7.0, dtype=torch.float32, device="cuda")
+    fp4.fp4_linear_fwd(torch.from_numpy(a).cuda(), None, torch.from_numpy(w).cuda(), None, K, out_type="raw",
+                       Y=Y[:, :N])
+    got = Y.cpu().numpy()
+    assert np.array_equal(got[:, :N], orc.gemm_raw(a, w).astype(np.float32))
+    assert np.all(got[:, N:] == -7.0)
+
+
+# ---------------------------------------------------------------- whole forward pass
+
+def test_linear_forward_pipeline_c1(fp4):
+    wlc = wl.WORKLOADS["c1_single_linear_256x512x512"]
+    lin = wlc.linears[0]
+    A_bits, W_bits = wlc.activation(lin), wlc.weight(lin)
+    Y, inter = fp4.linear_forward(dev_bf16(A_bits), dev_bf16(W_bits), lin.q)
+    ref = orc.linear_layer_forward(A_bits, W_bits, lin.q)
+    assert float(inter["outlier"]["t"].item()) == float(ref["t"])
+    assert np.array_equal(inter["a_codes"].cpu().numpy(), ref["a_codes"])
+    assert np.array_equal(inter["w_codes_t"].cpu().numpy(), ref["w_codes_t"])
+    assert bf16_ulp_distance(host_bits(Y), orc.f64_to_bf16(ref["Y"])).max() <= BF16_ULP_TOL
+    assert_no_device_flags(fp4)
