@@ -354,7 +354,9 @@ def dge_derivative(x: np.ndarray, k: float, clip: float) -> np.ndarray:
     d = np.where(inside, delta, 1.0)
     u = np.abs(2.0 * (x - lo) / d - 1.0)
     with np.errstate(divide="ignore"):
-        fp = np.where(u > 0, (1.0 / k) * u ** (1.0 / k - 1.0), np.inf)
+        # |u|^e at u = 0 is +inf for e < 0 (clipped), 1 for e = 0 (k = 1: f is
+        # the identity) and 0 for e > 0
+        fp = (1.0 / k) * u ** (1.0 / k - 1.0)
     fp = np.minimum(clip, fp)
     return np.where(inside, fp, 1.0 / k)
 

@@ -166,7 +166,7 @@ def outlier_clamp_quantile(A: torch.Tensor, q: float, want_clamped: bool = False
     o.setdefault("col_idx", torch.empty((max(cap, 1),), dtype=torch.int32, device=dev))
     o.setdefault("vals", torch.empty((max(cap, 1),), dtype=torch.float32, device=dev))
     o.setdefault("nnz", torch.empty((1,), dtype=torch.int64, device=dev))
-    ws_bytes = outlier_clamp_quantile_workspace(M, K, cap)
+    ws_bytes = outlier_clamp_quantile_workspace(M, K, o["col_idx"].numel())
     o.setdefault("workspace", torch.empty((ws_bytes,), dtype=torch.uint8, device=dev))
     if want_clamped:
         o.setdefault("A_clamped", torch.empty_like(A))

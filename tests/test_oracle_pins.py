@@ -352,6 +352,14 @@ def test_dge_derivative_at_grid_points_and_midpoints(k, clip):
     assert np.all(orc.dge_derivative(np.array([6.0, 6.5]), k, clip) == 1.0 / k)
 
 
+def test_dge_k1_is_identity_with_unit_derivative_everywhere():
+    # k = 1: f(x) = lo + delta/2 (1 + u) = x on every interval, so f' = 1,
+    # including the interval midpoints (u = 0) and the grid points.
+    x = np.concatenate([np.linspace(0, 5.999, 4001), [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]])
+    assert np.allclose(orc.dge_surrogate(x, 1.0), x, rtol=0, atol=1e-12)
+    assert np.all(orc.dge_derivative(x, 1.0, 3.0) == 1.0)
+
+
 def test_dge_surrogate_continuous_monotone_and_hits_grid():
     k = 5.0
     grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0])
