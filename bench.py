@@ -1,0 +1,490 @@
+#!/usr/bin/env python
+"""Benchmark of the FP4 quantized linear layer (forward + DGE weight gradient).
+
+One step = one pass of the whole hot path over one batch of synthetic input,
+for every linear of the workload:
+  quantile threshold + clamp + CSR compensation matrix  (outlier_clamp_quantile)
+  row quantization of A_clamped                          (fp4_quantize_rows, fused clamp)
+  column quantization of W                               (fp4_quantize_cols)
+  FP4 GEMM + scales + dA*W compensation -> BF16 Y       (fp4_linear_fwd)
+  BF16 weight-gradient GEMM x DGE factor -> fp32 dW     (fp4_linear_wgrad_dge)
+
+Metric: fwd + wgrad TFLOP/s = sum over linears of 4 M K N / step time, with
+inputs resident in HBM and L2 flushed (256 MiB write) before every step.
+`e2e` is the same metric through the C ABI from pinned HOST buffers: the
+host->device copy of A, W, dY and the device->host copy of Y and dW are inside
+the timed region.  `--impl reference` times the CPU oracle instead (bounded
+sample, single thread).  Under torchrun each rank runs an independent replica
+on its own GPU (the layer has no data-path exchange on one GPU's batch);
+value = work of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "c2_llama1.3b_mlp_up_8192x2048x5504"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP4_PER_BF16 = 13.5 / 2.25      # nominal dense FP4 : BF16 tensor rate
+L2_FLUSH_BYTES = 256 << 20
+HEAD_START_CYCLES = 400_000     # ~0.2 ms GPU spin so the step's launches are all queued
+DGE_K, DGE_CLIP = 5.0, 3.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+_REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+                0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+                0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 3:
+                try:
+                    self.samples.append((float(parts[0]), float(parts[1]), int(parts[2], 16)))
+                except ValueError:
+                    pass
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        busy = [s for s in self.samples if not (s[2] & 0x1)] or self.samples
+        reasons = sorted({name for s in busy for bit, name in _REASON_BITS.items() if s[2] & bit and bit != 0x1})
+        return {"sm_mhz": statistics.median(s[0] for s in busy), "sm_max_mhz": max(s[1] for s in busy),
+                "reasons": reasons, "samples": len(busy)}
+
+
+# ------------------------------------------------------------------ the GPU arm
+
+class LayerStep:
+    """Preallocated buffers and launches for one linear of the workload."""
+
+    def __init__(self, fp4, lin, A, W, dY):
+        import torch
+        self.fp4, self.lin = fp4, lin
+        M, K, N = lin.M, lin.K, lin.N
+        dev = A.device
+        self.A, self.W, self.dY = A, W, dY
+        cap = fp4.outlier_max_nnz(M, K, lin.q)
+        self.out = {
+            "t": torch.empty(1, dtype=torch.float32, device=dev),
+            "row_ptr": torch.empty(M + 1, dtype=torch.int32, device=dev),
+            "col_idx": torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+            "vals": torch.empty(max(cap, 1), dtype=torch.float32, device=dev),
+            "nnz": torch.empty(1, dtype=torch.int64, device=dev),
+        }
+        self.out["workspace"] = torch.empty(fp4.outlier_clamp_quantile_workspace(M, K, max(cap, 1)),
+                                            dtype=torch.uint8, device=dev)
+        self.a_codes = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+        self.s_a = torch.empty(M, dtype=torch.float32, device=dev)
+        self.w_codes = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
+        self.s_w = torch.empty(N, dtype=torch.float32, device=dev)
+        self.ws_cols = torch.empty(max(fp4.fp4_quantize_cols_workspace(N), 16), dtype=torch.uint8, device=dev)
+        self.Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.dW = torch.empty((K, N), dtype=torch.float32, device=dev)
+
+    PHASES = ("outlier_clamp_quantile", "fp4_quantize_rows", "fp4_quantize_cols", "fp4_linear_fwd",
+              "fp4_linear_wgrad_dge")
+    LAUNCHES = {"outlier_clamp_quantile": 4, "fp4_quantize_rows": 1, "fp4_quantize_cols": 2, "fp4_linear_fwd": 1,
+                "fp4_linear_wgrad_dge": 1}
+
+    def phase_fns(self):
+        fp4, lin = self.fp4, self.lin
+        return [
+            lambda: fp4.outlier_clamp_quantile(self.A, lin.q, out=self.out),
+            lambda: fp4.fp4_quantize_rows(self.A, clamp_t=self.out["t"], codes=self.a_codes, scales=self.s_a),
+            lambda: fp4.fp4_quantize_cols(self.W, codes_t=self.w_codes, scales=self.s_w, workspace=self.ws_cols),
+            lambda: fp4.fp4_linear_fwd(self.a_codes, self.s_a, self.w_codes, self.s_w, lin.K, csr=self.out,
+                                       W=self.W, out_type="bf16", Y=self.Y),
+            lambda: fp4.fp4_linear_wgrad_dge(self.A, self.dY, self.W, self.s_w, DGE_K, DGE_CLIP, dW=self.dW),
+        ]
+
+    def run(self, events=None):
+        """One pass of the hot path with direct launches (events: 6 CUDA events, or None)."""
+        for i, fn in enumerate(self.phase_fns()):
+            if events is not None:
+                events[i].record()
+            fn()
+        if events is not None:
+            events[5].record()
+
+    def capture(self):
+        """One CUDA graph per phase (the launches are stream-capture safe)."""
+        import torch
+        self.graphs = []
+        for fn in self.phase_fns():
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            self.graphs.append(g)
+
+    def replay(self, events=None):
+        for i, g in enumerate(self.graphs):
+            if events is not None:
+                events[i].record()
+            g.replay()
+        if events is not None:
+            events[5].record()
+
+    def algorithmic(self, nnz: int):
+        """Algorithmic work per phase: (amount, unit, bound)."""
+        M, K, N = self.lin.M, self.lin.K, self.lin.N
+        n = M * K
+        return {
+            "outlier_clamp_quantile": (2 * n + 2 * n + 8 * nnz + 4 * (M + 1), "B", "hbm"),  # histogram + stage read A
+            "fp4_quantize_rows": (2.5 * n + 4 * M, "B", "hbm"),
+            "fp4_quantize_cols": (2.5 * K * N + 4 * N, "B", "hbm"),
+            "fp4_linear_fwd": (2 * M * K * N, "FLOP", "tensor_fp4"),
+            "fp4_linear_wgrad_dge": (2 * M * K * N, "FLOP", "tensor_bf16"),
+        }
+
+
+def _src_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "precision_gemm_row_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "fp4_linear_wgrad_dge": ["gemm_wgrad.cu", "common.cuh"],
+    "fp4_linear_fwd": ["gemm_fwd.cu", "common.cuh"],
+    "fp4_quantize_rows": ["quantize.cu", "common.cuh"],
+    "fp4_quantize_cols": ["quantize.cu", "common.cuh"],
+    "outlier_clamp_quantile": ["outlier.cu", "common.cuh"],
+}
+
+
+def dram_traffic(phase: str, workload: str):
+    """Per-launch DRAM bytes of `phase` from the committed ncu summary, or None if
+    the kernel source changed since the capture (or none was taken)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(phase)
+    if not e or e.get("source_hash") != _src_hash(KERNEL_SOURCES[phase]):
+        return None
+    return e.get("bytes_per_launch")
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from precision_gemm_row_gb300 import build as fp4build
+    from precision_gemm_row_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    if local == 0 or world == 1:
+        fp4build.build()
+    if world > 1:
+        dist.barrier()
+    from precision_gemm_row_gb300 import fp4lin as fp4
+
+    work = wl.WORKLOADS[args.workload]
+    steps = []
+    host = []
+    for lin in work.linears:
+        A_bits, W_bits, dY_bits = work.activation(lin), work.weight(lin), work.grad(lin)
+        to_pinned = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hA, hW, hG = to_pinned(A_bits), to_pinned(W_bits), to_pinned(dY_bits)
+        A, W, dY = hA.cuda(), hW.cuda(), hG.cuda()
+        steps.append(LayerStep(fp4, lin, A, W, dY))
+        host.append((hA, hW, hG))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flops = sum(4 * l.M * l.K * l.N for l in work.linears)
+
+    for _ in range(args.warmup):
+        for s in steps:
+            s.run()
+    torch.cuda.synchronize()
+    for s in steps:
+        s.capture()
+    torch.cuda.synchronize()
+
+    def one_step(ev=None):
+        for i, s in enumerate(steps):
+            s.replay(ev[i] if ev is not None else None)
+
+    for _ in range(args.warmup):
+        one_step()
+    st, fl = fp4.fp4_device_status()
+    if st != "FP4_OK":
+        raise RuntimeError(f"device status after warm-up: {st} flags={fl}")
+
+    # ---- device-resident timed region: L2 flush, then a short GPU-side head start
+    # so every replay of the step is queued before the first event fires
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in steps] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for k in range(args.steps):
+            flush.fill_(float(k))
+            torch.cuda._sleep(HEAD_START_CYCLES)
+            one_step(ev[k])
+        torch.cuda.synchronize()
+    st, fl = fp4.fp4_device_status()
+    if st != "FP4_OK":
+        raise RuntimeError(f"device status after timed steps: {st} flags={fl}")
+    step_ms = [sum(ev[k][i][0].elapsed_time(ev[k][i][5]) for i in range(len(steps))) for k in range(args.steps)]
+    ms_per_step = sum(step_ms) / len(step_ms)
+    phase_ms = {}
+    for p, name in enumerate(LayerStep.PHASES):
+        phase_ms[name] = sum(ev[k][i][p].elapsed_time(ev[k][i][p + 1]) for k in range(args.steps)
+                             for i in range(len(steps))) / args.steps
+
+    # ---- end to end through the C ABI from pinned host buffers
+    hY = [torch.empty(s.Y.shape, dtype=s.Y.dtype).pin_memory() for s in steps]
+    hdW = [torch.empty(s.dW.shape, dtype=s.dW.dtype).pin_memory() for s in steps]
+    bi = sum(h[0].numel() * 2 + h[1].numel() * 2 + h[2].numel() * 2 for h in host)
+    bo = sum(y.numel() * 2 + d.numel() * 4 for y, d in zip(hY, hdW))
+    e2e_ms = []
+    for k in range(args.warmup + args.steps):
+        flush.fill_(float(k))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i, s in enumerate(steps):
+            s.A.copy_(host[i][0], non_blocking=True)
+            s.W.copy_(host[i][1], non_blocking=True)
+            s.dY.copy_(host[i][2], non_blocking=True)
+            for g in s.graphs:
+                g.replay()
+            hY[i].copy_(s.Y, non_blocking=True)
+            hdW[i].copy_(s.dW, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if k >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_ms_mean = sum(e2e_ms) / len(e2e_ms)
+
+    # ---- max over ranks
+    t = torch.tensor([ms_per_step, e2e_ms_mean], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max, e2e_max = float(t[0]), float(t[1])
+
+    peaks, peak_src = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_PER_BF16
+    nnz = sum(int(s.out["nnz"].item()) for s in steps)
+    kernels = {}
+    for name in LayerStep.PHASES:
+        amount = sum(s.algorithmic(int(s.out["nnz"].item()))[name][0] for s in steps)
+        unit, bound = steps[0].algorithmic(0)[name][1:]
+        per_s = amount / (phase_ms[name] * 1e-3)
+        if unit == "B":
+            ach, u, pk = per_s / 1e9, "GB/s", peaks["hbm_gbs"]
+        elif bound == "tensor_fp4":
+            ach, u, pk = per_s / 1e12, "TFLOP/s", fp4_peak
+        else:
+            ach, u, pk = per_s / 1e12, "TFLOP/s", peaks["bf16_tflops"]
+        kernels[name] = {"ms": round(phase_ms[name], 5), "achieved": round(ach, 2), "unit": u, "peak": pk,
+                         "frac": round(ach / pk, 4), "bound": "hbm" if unit == "B" else "tensor"}
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    kd = kernels[dom]
+    tr = dram_traffic(dom, args.workload)
+    roofline = {"bound": kd["bound"], "kernel": dom, "achieved": kd["achieved"], "peak": kd["peak"],
+                "peak_source": f"{peak_src}" + (" x nominal FP4/BF16 ratio 6" if dom == "fp4_linear_fwd" else ""),
+                "unit": kd["unit"], "frac": kd["frac"], "traffic": tr}
+    quant_bytes = sum(kernels[n]["achieved"] * kernels[n]["ms"] * 1e-3 * 1e9 for n in
+                      ("outlier_clamp_quantile", "fp4_quantize_rows", "fp4_quantize_cols"))
+    quant_ms = sum(kernels[n]["ms"] for n in ("outlier_clamp_quantile", "fp4_quantize_rows", "fp4_quantize_cols"))
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    e2e_value = world * flops / (e2e_max * 1e-3) / 1e12
+    line = {
+        "metric": "FP4 linear fwd+bwd TFLOPS on 1 GB300, % of dense FP4 peak; quantize GB/s vs HBM",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp4_e2m1 fwd / bf16 wgrad, fp32 accumulate", "data": "synthetic (seeded, LLaMA-shaped)",
+        "config": {"workload": args.workload, "linears": [[l.name, l.M, l.K, l.N, l.q] for l in work.linears],
+                   "bwd": "weight gradient with DGE (dgrad not on the pages)", "l2": "flushed before every step",
+                   "launch": "one CUDA graph per phase, replayed after a 0.2 ms GPU head start",
+                   "parallelism": f"replicas x{world}"},
+        "fp4_peak_frac": round(value / world / fp4_peak, 4),
+        "quantize": {"gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1), "frac_of_hbm": round(
+            quant_bytes / (quant_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+        "kernels": kernels, "nnz": nnz,
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                "ms_per_step": round(e2e_max, 5)},
+        "gpu_launches": args.steps * len(steps) * sum(LayerStep.LAUNCHES.values()),
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+# ------------------------------------------------------------------ the CPU oracle
+
+_ORACLE_SAMPLE = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+from oracle import fp4_linear as orc
+from precision_gemm_row_gb300 import workloads as wl
+work = wl.WORKLOADS[sys.argv[2]]
+rows_sample = int(sys.argv[3])
+nsteps = int(sys.argv[4])
+inputs = [(lin, work.activation(lin), work.weight(lin), work.grad(lin)) for lin in work.linears]
+flops = sum(4 * lin.M * lin.K * lin.N for lin in work.linears)
+steps = []
+for _ in range(nsteps):
+    total_est = 0.0
+    for lin, A_bits, W_bits, dY_bits in inputs:
+        t0 = time.perf_counter()
+        t, _, _ = orc.quantile_threshold(A_bits, lin.q)
+        A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
+        t1 = time.perf_counter()
+        rs = np.arange(min(rows_sample, lin.M))
+        a_codes_s, s_a_s = orc.quantize_rows(A_c[rs])
+        t2 = time.perf_counter()
+        w_codes, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+        t3 = time.perf_counter()
+        a_full = np.zeros((lin.M, lin.K // 2), np.uint8)
+        a_full[rs] = a_codes_s
+        s_a_full = np.ones(lin.M, np.float32)
+        s_a_full[rs] = s_a_s
+        orc.linear_fwd(a_full, s_a_full, w_codes, s_w, rp, ci, cv, W_bits, rows=rs)
+        t4 = time.perf_counter()
+        ks = np.arange(min(rows_sample, lin.K))
+        orc.wgrad_dge(A_bits, dY_bits, W_bits, s_w, 5.0, 3.0, rows=ks)
+        t5 = time.perf_counter()
+        total_est += ((t1 - t0) + (t2 - t1) * lin.M / len(rs) + (t3 - t2) + (t4 - t3) * lin.M / len(rs)
+                      + (t5 - t4) * lin.K / len(ks))
+    steps.append(total_est)
+print(json.dumps(dict(steps=steps, flops=flops)))
+"""
+
+
+def _oracle_steps(workload: str, rows_sample: int, nsteps: int):
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", _ORACLE_SAMPLE, ROOT, workload, str(rows_sample), str(nsteps)],
+                       env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError("oracle baseline failed: " + r.stderr[-800:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _sample_text(rows_sample: int) -> str:
+    return (f"per step: quantile + clamp + CSR of A and column quantization of W in full; row quantization and "
+            f"FP4 GEMM + epilogue on the first {rows_sample} rows, DGE wgrad on the first {rows_sample} feature "
+            f"rows, each scaled linearly to the full size; one thread (OPENBLAS/OMP threads = 1)")
+
+
+def cpu_baseline(workload: str, rows_sample: int = 64):
+    """The oracle, as it stands, timed in a fresh single-thread interpreter on a
+    bounded sample of one step of the workload (see _sample_text)."""
+    t0 = time.time()
+    d = _oracle_steps(workload, rows_sample, 1)
+    est = d["steps"][0]
+    return {"value": round(d["flops"] / est / 1e12, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": _sample_text(rows_sample), "est_step_s": round(est, 3), "wall_s": round(time.time() - t0, 1)}
+
+
+def run_reference(args):
+    """`--impl reference`: the oracle on the host cores, W + K steps in one
+    process (inputs drawn once), median of the K timed steps."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    t0 = time.time()
+    d = _oracle_steps(args.workload, args.cpu_budget, args.warmup + args.steps)
+    timed = d["steps"][args.warmup:]
+    est = statistics.median(timed)
+    v = round(d["flops"] / est / 1e12, 8)
+    cb = {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": _sample_text(args.cpu_budget),
+          "est_step_s": round(est, 3), "wall_s": round(time.time() - t0, 1)}
+    return {"impl": "reference", "metric": "FP4 linear fwd+bwd TFLOPS on 1 GB300, % of dense FP4 peak; quantize GB/s "
+            "vs HBM", "value": v, "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(est * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64/f32 (oracle)", "data": "synthetic (seeded, LLaMA-shaped)",
+            "config": {"workload": args.workload}, "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=int, default=64, help="rows sampled by the oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_gpu(args)
+    if line is not None:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -312,6 +312,23 @@ def linear_fwd(a_codes, s_a, w_codes_t, s_w, row_ptr=None, col_idx=None, vals=No
     return Y
 
 
+def linear_fwd_magnitude(a_codes, s_a, w_codes_t, s_w, row_ptr, col_idx, vals, W_bits,
+                         rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """|acc / (s_A s_W)| + sum_k |dA[i,k]| |W[k,j]| in fp64: the size of the two
+    terms the compensated output adds.  An fp32 evaluation of Y carries an
+    absolute rounding error of a few fp32 ulps of this magnitude, which can be
+    many BF16 ulps of Y when the terms cancel."""
+    t1 = np.abs(linear_fwd(a_codes, s_a, w_codes_t, s_w, rows=rows))
+    rows = np.arange(np.asarray(a_codes).shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+    W = np.abs(bf16_to_f32(W_bits).astype(np.float64))
+    rp = np.asarray(row_ptr, dtype=np.int64)
+    for r, i in enumerate(rows):
+        a, b = rp[i], rp[i + 1]
+        if b > a:
+            t1[r] += np.abs(np.asarray(vals[a:b], dtype=np.float64)) @ W[np.asarray(col_idx[a:b], dtype=np.int64)]
+    return t1
+
+
 # --------------------------------------------------------------------------
 # Differentiable gradient estimator (weight gradient)
 # --------------------------------------------------------------------------

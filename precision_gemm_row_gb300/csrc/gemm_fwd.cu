@@ -13,10 +13,17 @@
 // the K-sum: A is quantized per token and W per channel, granularity passage)
 // and adds the sparse compensation dA*W (outlier passage), then stores Y.
 //
-// Structure: persistent CTAs (one per SM), 192 threads:
-//   warp 0  TMA producer (one elected lane issues),
-//   warp 1  TMEM allocator and MMA issuer (one lane issues, commits to mbarriers),
-//   warps 2-5 epilogue, warp w reading TMEM lanes 32*(w%4) .. +31 (one output row per thread).
+// Structure: persistent CTAs (one per SM), 320 threads:
+//   warp 0    TMA producer (one elected lane issues),
+//   warp 1    TMEM allocator and MMA issuer (one lane issues, commits to mbarriers),
+//   warps 2-9 epilogue: warp w owns TMEM lanes 32*(w%4)..+31 (one output row per
+//             thread) and columns (w-2)/4 * BN/2 .. +BN/2 of the tile.
+// Tiles are 128 x 240: two 240-column fp32 accumulators plus the 32 scale-factor
+// columns fill the 512 TMEM columns exactly, so the epilogue of one tile
+// overlaps the main loop of the next.  The epilogue copies its accumulator
+// slice into registers, releases the TMEM buffer, then scales, adds the
+// compensation (one row of W per dA entry, all its loads in flight at once)
+// and stores.
 // Every mbarrier wait is bounded; on expiry the CTA records FP4_FLAG_TIMEOUT,
 // drains its TMA loads and MMAs, frees TMEM and exits.
 #include "common.cuh"
@@ -27,7 +34,8 @@ namespace {
 constexpr int kBM = 128;          // rows of A per tile (TMEM lanes)
 constexpr int kBKBytes = 128;     // bytes of K per stage = 256 E2M1 values (one swizzle row)
 constexpr int kMmaKBytes = 32;    // 64 E2M1 values per MMA
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
 
 template <int BN, int NACC>
@@ -40,7 +48,10 @@ struct FwdCfg {
   static constexpr uint32_t kSfaCol = ((NACC * BN + 15) / 16) * 16;
   static constexpr uint32_t kSfbCol = kSfaCol + 16;
   static constexpr int kBarBytes = 8 * (2 * kStages + 2 * NACC + 1) + 16;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kInvSwBytes = kEpiWarps * (BN / 2) * 4;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kInvSwBytes;
+  static constexpr int kEpiCols = BN / 2;  // columns per epilogue warp
+  static_assert(kEpiCols % 8 == 0, "epilogue slices are groups of 8 columns");
   static_assert(kSfbCol + 16 <= kTmemCols, "accumulators and scale factors exceed TMEM");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "invalid N tile");
   static_assert(kStages >= 2, "too few pipeline stages");
@@ -80,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sB = smem + C::kStages * C::kAStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 2 * NACC + 1);
+  float* inv_sw_s = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes + C::kBarBytes);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * C::kStages;
   const uint32_t accf0 = empty0 + 8 * C::kStages;
@@ -96,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < NACC; ++b) {
       mbar_init(accf0 + 8 * b, 1);
-      mbar_init(acce0 + 8 * b, 4);
+      mbar_init(acce0 + 8 * b, kEpiWarps);
     }
     mbar_init(done_bar, 1);
     fence_mbar_init();
@@ -110,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 2) {  // unit block scales: every scale byte = 0x7F (2^0)
+  if (warp >= 2 && warp < 6) {  // unit block scales: every scale byte = 0x7F (2^0)
     const uint32_t lb = uint32_t((warp & 3) * 32) << 16;
     tmem_st8_fill(tmem + lb + C::kSfaCol, 0x7F7F7F7Fu);
     tmem_st8_fill(tmem + lb + C::kSfaCol + 8, 0x7F7F7F7Fu);
@@ -215,7 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   } else {
     // ------------------------------------------------ epilogue
+    constexpr int EC = C::kEpiCols;
     const int q = warp & 3;
+    const int c_base = ((warp - 2) / 4) * EC;
+    float* inv_sw_w = inv_sw_s + (warp - 2) * EC;
     const int r_local = q * 32 + lane;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     int acc = 0;
@@ -224,11 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool raw = (p.y_type == FP4_OUT_RAW_ACC_FP32);
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
       const int mb = tile % num_m, nb = tile / num_m;
-      if (!mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns)) {
-        ok = false;
-        break;
+      // this warp's column scales 1/s_W in its own shared-memory slice (no
+      // cross-warp barrier, so a warp that gives up on a wait cannot strand others)
+      __syncwarp();
+      for (int c = lane; c < EC; c += 32) {
+        const int col = nb * BN + c_base + c;
+        inv_sw_w[c] = (!raw && col < p.N) ? 1.0f / __ldg(p.s_w + col) : 1.0f;
       }
-      tc_fence_after();
+      __syncwarp();
       const int row = mb * kBM + r_local;
       const bool row_ok = row < p.M;
       float inv_sa = 1.0f;
@@ -240,63 +258,74 @@ __global__ void __launch_bounds__(kThreads, 1)
           e1 = __ldg(p.rp + row + 1);
         }
       }
-      for (int c = 0; c < BN; c += 16) {
-        const int col0 = nb * BN + c;
-        if (col0 >= p.N) break;  // same for the whole warp
-        const int nvalid = (p.N - col0) >= 16 ? 16 : (p.N - col0);  // 8 or 16 (N % 8 == 0)
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_base + uint32_t(acc * BN + c), r);
+      if (!mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float y[EC];
+#pragma unroll
+      for (int c = 0; c < EC; c += 8) {
+        uint32_t r[8];
+        tmem_ld8(tmem + lane_base + uint32_t(acc * BN + c_base + c), r);
         tmem_wait_ld();
-        float y[16];
-        if (raw) {
 #pragma unroll
-          for (int t = 0; t < 16; ++t) y[t] = __uint_as_float(r[t]);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const float sw = t < nvalid ? __ldg(p.s_w + col0 + t) : 1.0f;
-            y[t] = __uint_as_float(r[t]) * inv_sa * (1.0f / sw);
-          }
-          for (int e = e0; e < e1; ++e) {
-            const int k = __ldg(p.ci + e);
-            const float v = __ldg(p.cv + e);
-            const uint4* wr = reinterpret_cast<const uint4*>(p.W + int64_t(k) * p.ldw + col0);
-            uint4 w0 = __ldg(wr);
-            uint4 w1 = nvalid > 8 ? __ldg(wr + 1) : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-            for (int t = 0; t < 16; ++t)
-              y[t] = fmaf(v, bf16_bits_to_float((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu), y[t]);
-          }
-        }
-        if (row_ok) {
-          if (p.y_type == FP4_OUT_BF16) {
-            uint32_t packed[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * t], y[2 * t + 1]);
-              packed[t] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.Y) + int64_t(row) * p.ldy + col0);
-            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            if (nvalid > 8) dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + int64_t(row) * p.ldy + col0);
-            dst[0] = make_float4(y[0], y[1], y[2], y[3]);
-            dst[1] = make_float4(y[4], y[5], y[6], y[7]);
-            if (nvalid > 8) {
-              dst[2] = make_float4(y[8], y[9], y[10], y[11]);
-              dst[3] = make_float4(y[12], y[13], y[14], y[15]);
-            }
-          }
-        }
+        for (int t = 0; t < 8; ++t) y[c + t] = __uint_as_float(r[t]);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+      if (lane == 0) mbar_arrive(acce0 + 8 * acc);   // TMEM buffer free for the next tile
       if (++acc == NACC) {
         acc = 0;
         acc_phase ^= 1u;
+      }
+      const int col_base = nb * BN + c_base;
+      int nvalid = p.N - col_base;  // columns of this slice inside the matrix (multiple of 8)
+      nvalid = nvalid < 0 ? 0 : (nvalid > EC ? EC : nvalid);
+      if (!raw) {
+#pragma unroll
+        for (int c = 0; c < EC; ++c) y[c] = y[c] * inv_sa * inv_sw_w[c];
+        for (int e = e0; e < e1; ++e) {
+          const int k = __ldg(p.ci + e);
+          const float v = __ldg(p.cv + e);
+          const uint4* wr = reinterpret_cast<const uint4*>(p.W + int64_t(k) * p.ldw + col_base);
+          uint4 w[EC / 8];
+#pragma unroll
+          for (int g = 0; g < EC / 8; ++g) w[g] = (8 * g < nvalid) ? __ldg(wr + g) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int g = 0; g < EC / 8; ++g) {
+            const uint32_t wv[4] = {w[g].x, w[g].y, w[g].z, w[g].w};
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              y[8 * g + t] = fmaf(v, bf16_bits_to_float((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu), y[8 * g + t]);
+          }
+        }
+      }
+      if (row_ok) {
+        if (p.y_type == FP4_OUT_BF16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.Y) + int64_t(row) * p.ldy + col_base);
+#pragma unroll
+          for (int g = 0; g < EC / 8; ++g) {
+            if (8 * g < nvalid) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(y[8 * g + 2 * t], y[8 * g + 2 * t + 1]);
+                pk[t] = *reinterpret_cast<const uint32_t*>(&h);
+              }
+              dst[g] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + int64_t(row) * p.ldy + col_base);
+#pragma unroll
+          for (int g = 0; g < EC / 8; ++g) {
+            if (8 * g < nvalid) {
+              dst[2 * g] = make_float4(y[8 * g], y[8 * g + 1], y[8 * g + 2], y[8 * g + 3]);
+              dst[2 * g + 1] = make_float4(y[8 * g + 4], y[8 * g + 5], y[8 * g + 6], y[8 * g + 7]);
+            }
+          }
+        }
       }
     }
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
@@ -309,8 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-constexpr int kFwdBN = 256;
-constexpr int kFwdAcc = 1;
+constexpr int kFwdBN = 240;
+constexpr int kFwdAcc = 2;
 
 }  // namespace
 }  // namespace fp4

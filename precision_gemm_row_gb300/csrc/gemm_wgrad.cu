@@ -14,10 +14,21 @@
 // G = A^T dY is a BF16 GEMM with both operands stored with the reduction
 // (token) dimension strided, i.e. MN-major: TMA loads [64 tokens x 64
 // features] boxes with 128-byte swizzle and tcgen05.mma kind::f16 reads them
-// through MN-major descriptors, so no transpose copy is ever made.  The fp32
-// accumulator is double-buffered in TMEM (2 x 256 columns) so the DGE epilogue
-// of one tile overlaps the main loop of the next.  Same warp roles and bounded
-// waits as the forward kernel.
+// through MN-major descriptors, so no transpose copy is ever made.
+//
+// Accumulation precision: the tensor core's fp32 accumulation drifts by about
+// 1e-9 x (number of accumulated tokens) relative (a biased, truncation-like
+// error), which would exceed 1e-5 at 16k tokens.  The token range of every
+// tile is therefore split into chunks of kChunkStages x 64 tokens; each chunk
+// is accumulated in one of two TMEM buffers and the epilogue warps add it into
+// fp32 registers (round to nearest), so the error stays at the chunk level.
+// While the epilogue drains one buffer the MMA warp fills the other.
+//
+// Roles (10 warps): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
+// warps 2-9 epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (one dW row per
+// thread) and columns (w-2)/4 * 128 .. +127 of the 256-wide tile.  Every
+// mbarrier wait is bounded; on expiry the CTA records FP4_FLAG_TIMEOUT,
+// drains its TMA loads and MMAs, frees TMEM and exits.
 #include "common.cuh"
 
 namespace fp4 {
@@ -27,8 +38,11 @@ constexpr int kBM = 128;      // rows of dW (input features) per tile
 constexpr int kBN = 256;      // columns of dW (output features) per tile
 constexpr int kBT = 64;       // tokens per stage
 constexpr int kMmaT = 16;     // tokens per MMA (BF16 K = 16)
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kNAcc = 2;
+constexpr int kChunkStages = 16;                 // 1024 tokens per TMEM accumulation chunk
+constexpr int kEpiCols = kBN / 2;                // columns per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 64;                          // features per TMA box (128 bytes of BF16)
 constexpr int kBoxBytes = kBox * kBT * 2;         // 8 KB
@@ -99,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < kNAcc; ++b) {
       mbar_init(accf0 + 8 * b, 1);
-      mbar_init(acce0 + 8 * b, 4);
+      mbar_init(acce0 + 8 * b, kEpiWarps);
     }
     mbar_init(done_bar, 1);
     fence_mbar_init();
@@ -164,42 +178,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-      if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem + uint32_t(acc * kBN);
-      for (int tb = 0; tb < tblocks; ++tb) {
-        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_ns)) {
+      for (int tb0 = 0; tb0 < tblocks && ok; tb0 += kChunkStages) {
+        const int tb1 = tb0 + kChunkStages < tblocks ? tb0 + kChunkStages : tblocks;
+        if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = a_base + stage * kAStage, b0 = b_base + stage * kBStage;
-#pragma unroll
-          for (int k = 0; k < kBT / kMmaT; ++k) {
-            // MN-major, 128-byte swizzle: 64-feature atoms kBoxBytes apart (LBO),
-            // 8-token groups 1024 bytes apart (SBO); 16 tokens = 2048 bytes per MMA.
-            const uint64_t ad = smem_desc_sw128(a0 + k * (kMmaT * 128), kBoxBytes, 1024);
-            const uint64_t bd = smem_desc_sw128(b0 + k * (kMmaT * 128), kBoxBytes, 1024);
-            mma_f16(d_tmem, ad, bd, kIdesc, (tb | k) != 0 ? 1u : 0u);
+        const uint32_t d_tmem = tmem + uint32_t(acc * kBN);
+        for (int tb = tb0; tb < tb1; ++tb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, p.wait_ns)) {
+            ok = false;
+            break;
           }
-          tc_commit(empty0 + 8 * stage);
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = a_base + stage * kAStage, b0 = b_base + stage * kBStage;
+#pragma unroll
+            for (int k = 0; k < kBT / kMmaT; ++k) {
+              // MN-major, 128-byte swizzle: 64-feature atoms kBoxBytes apart (LBO),
+              // 8-token groups 1024 bytes apart (SBO); 16 tokens = 2048 bytes per MMA.
+              const uint64_t ad = smem_desc_sw128(a0 + k * (kMmaT * 128), kBoxBytes, 1024);
+              const uint64_t bd = smem_desc_sw128(b0 + k * (kMmaT * 128), kBoxBytes, 1024);
+              mma_f16(d_tmem, ad, bd, kIdesc, (tb != tb0 || k != 0) ? 1u : 0u);
+            }
+            tc_commit(empty0 + 8 * stage);
+          }
+          __syncwarp();
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
+        if (!ok) break;
+        if (lane == 0) tc_commit(accf0 + 8 * acc);
         __syncwarp();
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+        if (++acc == kNAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
         }
-      }
-      if (!ok) break;
-      if (lane == 0) tc_commit(accf0 + 8 * acc);
-      __syncwarp();
-      if (++acc == kNAcc) {
-        acc = 0;
-        acc_phase ^= 1u;
       }
     }
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
@@ -207,57 +224,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   } else {
-    // ------------------------------------------------ DGE epilogue
+    // ------------------------------------------------ chunk promotion + DGE epilogue
     const int q = warp & 3;
+    const int c_base = ((warp - 2) / 4) * kEpiCols;
     const int r_local = q * 32 + lane;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       const int rb = tile % num_r, nb = tile / num_r;
-      if (!mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int row = rb * kBM + r_local;
-      const bool row_ok = row < p.K;
-      for (int c = 0; c < kBN; c += 16) {
-        const int col0 = nb * kBN + c;
-        if (col0 >= p.N) break;
-        const int nvalid = (p.N - col0) >= 16 ? 16 : (p.N - col0);
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_base + uint32_t(acc * kBN + c), r);
-        tmem_wait_ld();
-        if (row_ok) {
-          const uint4* wr = reinterpret_cast<const uint4*>(p.W + int64_t(row) * p.ldw + col0);
-          const uint4 w0 = __ldg(wr);
-          const uint4 w1 = nvalid > 8 ? __ldg(wr + 1) : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-          float o[16];
+      float sum[kEpiCols];
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const float sw = t < nvalid ? __ldg(p.s_w + col0 + t) : 1.0f;
-            const float w = bf16_bits_to_float((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu);
-            const float x = fabsf(__fmul_rn(w, sw));
-            o[t] = __uint_as_float(r[t]) * dge_factor(x, p.inv_k, p.expo, p.clip);
-          }
-          float4* dst = reinterpret_cast<float4*>(p.dW + int64_t(row) * p.lddw + col0);
-          dst[0] = make_float4(o[0], o[1], o[2], o[3]);
-          dst[1] = make_float4(o[4], o[5], o[6], o[7]);
-          if (nvalid > 8) {
-            dst[2] = make_float4(o[8], o[9], o[10], o[11]);
-            dst[3] = make_float4(o[12], o[13], o[14], o[15]);
-          }
+      for (int c = 0; c < kEpiCols; ++c) sum[c] = 0.0f;
+      for (int tb0 = 0; tb0 < tblocks; tb0 += kChunkStages) {
+        if (!mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kEpiCols; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_base + uint32_t(acc * kBN + c_base + c), r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int t = 0; t < 16; ++t) sum[c + t] += __uint_as_float(r[t]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+        if (++acc == kNAcc) {
+          acc = 0;
+          acc_phase ^= 1u;
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce0 + 8 * acc);
-      if (++acc == kNAcc) {
-        acc = 0;
-        acc_phase ^= 1u;
+      if (!ok) break;
+      const int row = rb * kBM + r_local;
+      if (row < p.K) {
+        const uint16_t* wrow = p.W + int64_t(row) * p.ldw;
+        float* drow = p.dW + int64_t(row) * p.lddw;
+#pragma unroll
+        for (int c = 0; c < kEpiCols; c += 8) {
+          const int col0 = nb * kBN + c_base + c;
+          if (col0 < p.N) {  // N % 8 == 0: a group of 8 columns is all in or all out
+            const uint4 w8 = __ldg(reinterpret_cast<const uint4*>(wrow + col0));
+            const uint32_t wv[4] = {w8.x, w8.y, w8.z, w8.w};
+            float o[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float w = bf16_bits_to_float((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu);
+              const float x = fabsf(__fmul_rn(w, __ldg(p.s_w + col0 + t)));
+              o[t] = sum[c + t] * dge_factor(x, p.inv_k, p.expo, p.clip);
+            }
+            float4* dst = reinterpret_cast<float4*>(drow + col0);
+            dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+          }
+        }
       }
     }
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);

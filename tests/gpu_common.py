@@ -6,6 +6,7 @@ import torch
 
 BF16_ULP_TOL = 1          # final BF16 outputs: within 1 BF16 ulp
 FROB_TOL = 1e-5           # compensated fp32 outputs and DGE weight gradients
+FP32_SUM_BOUND = 2.0 ** -20   # fp32 epilogue rounding, relative to the terms' magnitude
 
 
 def dev_bf16(bits: np.ndarray) -> torch.Tensor:
@@ -35,3 +36,23 @@ def rel_frobenius(got: np.ndarray, ref: np.ndarray) -> float:
 def assert_no_device_flags(fp4lin):
     name, flags = fp4lin.fp4_device_status()
     assert flags == 0 and name == "FP4_OK", (name, flags)
+
+
+def bf16_ulp_of(y: np.ndarray) -> np.ndarray:
+    """Spacing of BF16 values at |y| (8 significant bits)."""
+    y = np.abs(np.asarray(y, dtype=np.float64))
+    _, e = np.frexp(np.where(y > 0, y, 2.0 ** -126))
+    return np.exp2(e.astype(np.float64) - 8.0)
+
+
+def assert_bf16_compensated_close(got_bits: np.ndarray, y_ref: np.ndarray, magnitude: np.ndarray):
+    """Compensated BF16 output: within 1 BF16 ulp of the fp64 result plus the
+    fp32 rounding bound of the epilogue's sum (FP32_SUM_BOUND x the magnitude of
+    the two added terms), which is what any fp32 epilogue can guarantee when
+    the GEMM term and the compensation cancel."""
+    from oracle import fp4_linear as orc
+    got = orc.bf16_to_f32(got_bits).astype(np.float64)
+    allowed = bf16_ulp_of(y_ref) + FP32_SUM_BOUND * magnitude
+    bad = np.abs(got - y_ref) > allowed
+    assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], y_ref[bad][:5])
+    return int(np.count_nonzero(bf16_ulp_distance(got_bits, orc.f64_to_bf16(y_ref)) > BF16_ULP_TOL))
