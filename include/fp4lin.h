@@ -118,6 +118,30 @@ fp4_status fp4_quantize_cols(const void* W, int64_t K, int64_t N, int64_t ldw, u
                              fp4_stream_t stream);
 
 /*
+ * fp4_quantize_cols_noalloc -- fp4_quantize_cols for callers that cannot give
+ * the library any scratch memory.
+ *
+ * There is no counterpart on the pages: this is an interface variant, not part
+ * of the method.  Callers that cannot allocate -- code inside a framework that
+ * owns every device allocation, real-time paths that must not call cudaMalloc
+ * (it can synchronize the device), embedded users with a fixed memory budget --
+ * get the same result as fp4_quantize_cols (bit for bit) without a workspace.
+ * The column maxima are kept in a fixed device array built into the library
+ * (64 Ki entries, 256 KiB, held on every GPU that loads the library until the
+ * process exits); N above 65536 returns FP4_ERR_SHAPE.  Arguments, alignment
+ * and errors are those of fp4_quantize_cols without the workspace pair.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call outside any
+ * stream capture.  All calls share the one array, and each call clears the
+ * part it uses before using it, so calls must not overlap on the GPU: two
+ * calls in flight at the same time on different streams race on the array.
+ * No device or host memory is allocated by this call.
+ */
+fp4_status fp4_quantize_cols_noalloc(const void* W, int64_t K, int64_t N, int64_t ldw, uint8_t* codes_t,
+                                     int64_t ldc_bytes, float* scales, fp4_stream_t stream);
+
+/*
  * outlier_clamp_quantile -- quantile threshold of |A|, clamp, and the sparse
  * compensation matrix dA = A - A_clamped in CSR form.
  *

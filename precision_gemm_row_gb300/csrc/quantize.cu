@@ -5,6 +5,8 @@
 //
 // Both are HBM-bound streaming kernels: 16-byte loads, one row or column strip
 // per warp / CTA, absmax by warp shuffles, two codes per byte.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace fp4 {
@@ -245,6 +247,74 @@ FP4_API fp4_status fp4_quantize_cols(const void* W, int64_t K, int64_t N, int64_
   if (st != FP4_OK) return st;
   auto s = reinterpret_cast<cudaStream_t>(stream);
   auto* colmax = static_cast<uint32_t*>(workspace);
+  if (cudaMemsetAsync(colmax, 0, size_t(N) * 4, s) != cudaSuccess) return FP4_ERR_CUDA;
+  const int col_blocks = int((N + 255) / 256);
+  int splits = (4 * sms + col_blocks - 1) / col_blocks;
+  const int max_splits = int((K + 63) / 64);
+  if (splits > max_splits) splits = max_splits;
+  if (splits < 1) splits = 1;
+  const int rows_per_split = int((K + splits - 1) / splits);
+  splits = int((K + rows_per_split - 1) / rows_per_split);
+  const auto* w = static_cast<const uint16_t*>(W);
+  col_absmax_kernel<<<dim3(col_blocks, splits), 256, 0, s>>>(w, int(K), int(N), ldw, rows_per_split, colmax);
+  if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
+  quantize_cols_kernel<<<dim3(unsigned((N + 63) / 64), unsigned((K + 63) / 64)), 256, 0, s>>>(
+      w, int(K), int(N), ldw, colmax, codes_t, ldc_bytes, scales);
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// Column quantization without caller-provided scratch.
+//
+// Some callers cannot hand the library any scratch memory: code that runs
+// inside a framework which owns every device allocation (so it has no handle
+// to allocate a workspace), real-time paths that must not call cudaMalloc
+// because it can synchronize the device, and embedded users with a fixed
+// memory budget.  For them the column maxima live in a fixed device array
+// that is part of the library image: every GPU that loads the library holds
+// it (256 KiB) until the process exits, and it bounds N.
+namespace fp4 {
+namespace {
+constexpr int64_t kNoAllocMaxN = 65536;
+static __device__ __align__(256) uint32_t g_colmax_scratch[kNoAllocMaxN];
+
+std::mutex g_scratch_mu;
+uint32_t* g_scratch_ptr[64];
+
+// Device address of g_colmax_scratch for the current device, looked up once
+// per device (host code cannot use the symbol itself as a device pointer).
+fp4_status scratch_address(uint32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP4_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_colmax_scratch) != cudaSuccess || !ptr) return FP4_ERR_CUDA;
+    g_scratch_ptr[dev] = static_cast<uint32_t*>(ptr);
+  }
+  *out = g_scratch_ptr[dev];
+  return FP4_OK;
+}
+}  // namespace
+}  // namespace fp4
+
+FP4_API fp4_status fp4_quantize_cols_noalloc(const void* W, int64_t K, int64_t N, int64_t ldw, uint8_t* codes_t,
+                                             int64_t ldc_bytes, float* scales, fp4_stream_t stream) {
+  using namespace fp4;
+  if (K <= 0 || N <= 0) return FP4_ERR_SHAPE;
+  if (!W || !codes_t || !scales) return FP4_ERR_INVALID_ARG;
+  if (N > kNoAllocMaxN) return FP4_ERR_SHAPE;  // the built-in scratch holds at most 65536 column maxima
+  if (K % 32 != 0 || N % 8 != 0 || K >= (int64_t(1) << 31) || ldw < N || ldc_bytes < K / 2) return FP4_ERR_SHAPE;
+  if (ldw % 8 != 0 || ldc_bytes % 16 != 0 || !aligned16(W) || !aligned16(codes_t) || !aligned16(scales))
+    return FP4_ERR_ALIGNMENT;
+  int sms = 0;
+  fp4_status st = check_device(&sms);
+  if (st != FP4_OK) return st;
+  uint32_t* colmax = nullptr;
+  st = scratch_address(&colmax);
+  if (st != FP4_OK) return st;
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  // the maxima are merged with atomic max, so the shared array must start at zero on every call
   if (cudaMemsetAsync(colmax, 0, size_t(N) * 4, s) != cudaSuccess) return FP4_ERR_CUDA;
   const int col_blocks = int((N + 255) / 256);
   int splits = (4 * sms + col_blocks - 1) / col_blocks;

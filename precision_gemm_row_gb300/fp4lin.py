@@ -25,7 +25,7 @@ FLAG_TIMEOUT, FLAG_CAPACITY, FLAG_INTERNAL = 0x1, 0x2, 0x4
 # exported symbols, in the order include/fp4lin.h declares them
 EXPORTS = (
     "fp4_status_string", "fp4_abi_version", "fp4_quantize_rows", "fp4_quantize_cols_workspace",
-    "fp4_quantize_cols", "outlier_max_nnz", "outlier_clamp_quantile_workspace", "outlier_clamp_quantile",
+    "fp4_quantize_cols", "fp4_quantize_cols_noalloc", "outlier_max_nnz", "outlier_clamp_quantile_workspace", "outlier_clamp_quantile",
     "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_device_status", "fp4_selftest_bounded_wait",
 )
 
@@ -51,6 +51,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "fp4_quantize_rows": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp]),
         "fp4_quantize_cols_workspace": (_c_sz, [_c_i64]),
         "fp4_quantize_cols": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]),
+        "fp4_quantize_cols_noalloc": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_i64, _c_vp, _c_vp]),
         "outlier_max_nnz": (_c_i64, [_c_i64, _c_i64, _c_d]),
         "outlier_clamp_quantile_workspace": (_c_sz, [_c_i64, _c_i64, _c_i64]),
         "outlier_clamp_quantile": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_d, _c_vp, _c_vp, _c_vp, _c_vp,
@@ -137,6 +138,18 @@ def fp4_quantize_cols(W: torch.Tensor, codes_t: Optional[torch.Tensor] = None, s
     ldc = _rowmajor(codes_t, "codes_t", torch.uint8)
     _check("fp4_quantize_cols", _lib.fp4_quantize_cols(_p(W), K, N, ldw, _p(codes_t), ldc, _p(scales), _p(workspace),
                                                        workspace.numel() * workspace.element_size(), _s(stream)))
+    return codes_t, scales
+
+
+def fp4_quantize_cols_noalloc(W: torch.Tensor, codes_t: torch.Tensor, scales: torch.Tensor, stream=None):
+    """fp4_quantize_cols without a workspace (the library's built-in scratch;
+    N <= 65536; calls must not overlap on the GPU).  Outputs must be passed in:
+    this path is for callers that allocate nothing per call."""
+    ldw = _rowmajor(W, "W", torch.bfloat16)
+    K, N = W.shape
+    ldc = _rowmajor(codes_t, "codes_t", torch.uint8)
+    _check("fp4_quantize_cols_noalloc", _lib.fp4_quantize_cols_noalloc(_p(W), K, N, ldw, _p(codes_t), ldc,
+                                                                       _p(scales), _s(stream)))
     return codes_t, scales
 
 
