@@ -20,10 +20,10 @@
 //             thread) and columns (w-2)/4 * BN/2 .. +BN/2 of the tile.
 // Tiles are 128 x 240: two 240-column fp32 accumulators plus the 32 scale-factor
 // columns fill the 512 TMEM columns exactly, so the epilogue of one tile
-// overlaps the main loop of the next.  The epilogue copies its accumulator
-// slice into registers, releases the TMEM buffer, then scales, adds the
-// compensation (one row of W per dA entry, all its loads in flight at once)
-// and stores.
+// overlaps the main loop of the next.  Each epilogue thread first forms its
+// row's compensation sum over the dA entries (one row segment of W per entry,
+// all its loads in flight at once) while the tile's main loop still runs, then
+// reads the accumulator in groups of 8 columns, scales, adds and stores.
 // Every mbarrier wait is bounded; on expiry the CTA records FP4_FLAG_TIMEOUT,
 // drains its TMA loads and MMAs, frees TMEM and exits.
 #include "common.cuh"
@@ -49,7 +49,10 @@ struct FwdCfg {
   static constexpr uint32_t kSfbCol = kSfaCol + 16;
   static constexpr int kBarBytes = 8 * (2 * kStages + 2 * NACC + 1) + 16;
   static constexpr int kInvSwBytes = kEpiWarps * (BN / 2) * 4;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kInvSwBytes;
+  // per-warp output staging for the TMA store: 32 rows x 80 bytes (40 BF16 or 20 fp32 columns)
+  static constexpr int kOutRowBytes = 80;
+  static constexpr int kOutBytes = 32 * kOutRowBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiWarps * kOutBytes + kBarBytes + kInvSwBytes;
   static constexpr int kEpiCols = BN / 2;  // columns per epilogue warp
   static_assert(kEpiCols % 8 == 0, "epilogue slices are groups of 8 columns");
   static_assert(kSfbCol + 16 <= kTmemCols, "accumulators and scale factors exceed TMEM");
@@ -83,15 +86,16 @@ struct FwdParams {
 template <int BN, int NACC>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const FwdParams p) {
+                   const __grid_constant__ CUtensorMap tmY, const FwdParams p) {
   using C = FwdCfg<BN, NACC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::kStages * C::kAStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint8_t* sOut = smem + C::kStages * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + kEpiWarps * C::kOutBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 2 * NACC + 1);
-  float* inv_sw_s = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes + C::kBarBytes);
+  float* inv_sw_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + C::kBarBytes);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * C::kStages;
   const uint32_t accf0 = empty0 + 8 * C::kStages;
@@ -102,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmY);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -231,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int c_base = ((warp - 2) / 4) * EC;
     float* inv_sw_w = inv_sw_s + (warp - 2) * EC;
+    uint8_t* out_s = sOut + (warp - 2) * C::kOutBytes;
     const int r_local = q * 32 + lane;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     int acc = 0;
@@ -258,19 +264,88 @@ __global__ void __launch_bounds__(kThreads, 1)
           e1 = __ldg(p.rp + row + 1);
         }
       }
+      const int col_base = nb * BN + c_base;
+      int nvalid = p.N - col_base;  // columns of this slice inside the matrix (multiple of 8)
+      nvalid = nvalid < 0 ? 0 : (nvalid > EC ? EC : nvalid);
+      // compensation sum_e dA[row,k_e] W[k_e, cols] for this row, formed while the
+      // tile's main loop still runs (one W row segment per entry, all loads in flight)
+      float comp[EC];
+#pragma unroll
+      for (int c = 0; c < EC; ++c) comp[c] = 0.0f;
+      for (int e = e0; e < e1; ++e) {
+        const int k = __ldg(p.ci + e);
+        const float v = __ldg(p.cv + e);
+        const uint4* wr = reinterpret_cast<const uint4*>(p.W + int64_t(k) * p.ldw + col_base);
+        uint4 w[EC / 8];
+#pragma unroll
+        for (int g = 0; g < EC / 8; ++g) w[g] = (8 * g < nvalid) ? __ldg(wr + g) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int g = 0; g < EC / 8; ++g) {
+          const uint32_t wv[4] = {w[g].x, w[g].y, w[g].z, w[g].w};
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            comp[8 * g + t] =
+                fmaf(v, bf16_bits_to_float((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu), comp[8 * g + t]);
+        }
+      }
       if (!mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float y[EC];
+      // Y leaves through a per-warp staging buffer (32 rows x 80 bytes) and a TMA
+      // store, which writes whole rows and drops what falls outside M x N:
+      // 40 columns per pass, as one BF16 store or two fp32 stores of 20 columns.
+      const bool bf16_out = (p.y_type == FP4_OUT_BF16);
+      const int row0 = mb * kBM + q * 32;
+      uint8_t* orow = out_s + lane * C::kOutRowBytes;
 #pragma unroll
-      for (int c = 0; c < EC; c += 8) {
-        uint32_t r[8];
-        tmem_ld8(tmem + lane_base + uint32_t(acc * BN + c_base + c), r);
-        tmem_wait_ld();
+      for (int pc = 0; pc < EC; pc += 40) {
+        if (col_base + pc < p.N) {   // warp-uniform
+          float y[40];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) y[c + t] = __uint_as_float(r[t]);
+          for (int g = 0; g < 5; ++g) {
+            uint32_t r[8];
+            tmem_ld8(tmem + lane_base + uint32_t(acc * BN + c_base + pc + 8 * g), r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const int c = pc + 8 * g + t;
+              y[8 * g + t] = raw ? __uint_as_float(r[t]) : __uint_as_float(r[t]) * inv_sa * inv_sw_w[c] + comp[c];
+            }
+          }
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            if (bf16_out && part == 1) break;
+            if (lane == 0) bulk_wait_read_all();   // the previous store has read the buffer
+            __syncwarp();
+            if (bf16_out) {
+#pragma unroll
+              for (int g = 0; g < 5; ++g) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  const __nv_bfloat162 h = __floats2bfloat162_rn(y[8 * g + 2 * t], y[8 * g + 2 * t + 1]);
+                  pk[t] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                *reinterpret_cast<uint4*>(orow + 16 * g) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              }
+            } else {
+#pragma unroll
+              for (int g = 0; g < 5; ++g)
+                *reinterpret_cast<float4*>(orow + 16 * g) =
+                    make_float4(y[20 * part + 4 * g], y[20 * part + 4 * g + 1], y[20 * part + 4 * g + 2],
+                                y[20 * part + 4 * g + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int xcol = col_base + pc + 20 * part;
+            if (lane == 0 && row0 < p.M && xcol < p.N) {
+              tma_store_2d(&tmY, smem_u32(out_s), xcol, row0);
+              bulk_commit_group();
+            }
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -279,55 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
-      const int col_base = nb * BN + c_base;
-      int nvalid = p.N - col_base;  // columns of this slice inside the matrix (multiple of 8)
-      nvalid = nvalid < 0 ? 0 : (nvalid > EC ? EC : nvalid);
-      if (!raw) {
-#pragma unroll
-        for (int c = 0; c < EC; ++c) y[c] = y[c] * inv_sa * inv_sw_w[c];
-        for (int e = e0; e < e1; ++e) {
-          const int k = __ldg(p.ci + e);
-          const float v = __ldg(p.cv + e);
-          const uint4* wr = reinterpret_cast<const uint4*>(p.W + int64_t(k) * p.ldw + col_base);
-          uint4 w[EC / 8];
-#pragma unroll
-          for (int g = 0; g < EC / 8; ++g) w[g] = (8 * g < nvalid) ? __ldg(wr + g) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int g = 0; g < EC / 8; ++g) {
-            const uint32_t wv[4] = {w[g].x, w[g].y, w[g].z, w[g].w};
-#pragma unroll
-            for (int t = 0; t < 8; ++t)
-              y[8 * g + t] = fmaf(v, bf16_bits_to_float((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu), y[8 * g + t]);
-          }
-        }
-      }
-      if (row_ok) {
-        if (p.y_type == FP4_OUT_BF16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.Y) + int64_t(row) * p.ldy + col_base);
-#pragma unroll
-          for (int g = 0; g < EC / 8; ++g) {
-            if (8 * g < nvalid) {
-              uint32_t pk[4];
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(y[8 * g + 2 * t], y[8 * g + 2 * t + 1]);
-                pk[t] = *reinterpret_cast<const uint32_t*>(&h);
-              }
-              dst[g] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-          }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + int64_t(row) * p.ldy + col_base);
-#pragma unroll
-          for (int g = 0; g < EC / 8; ++g) {
-            if (8 * g < nvalid) {
-              dst[2 * g] = make_float4(y[8 * g], y[8 * g + 1], y[8 * g + 2], y[8 * g + 3]);
-              dst[2 * g + 1] = make_float4(y[8 * g + 4], y[8 * g + 5], y[8 * g + 6], y[8 * g + 7]);
-            }
-          }
-        }
-      }
     }
+    if (lane == 0) bulk_wait_all();
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   }
 
@@ -378,6 +406,12 @@ FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_byte
                       uint64_t(ldw_codes_bytes), kBKBytes, kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != FP4_OK) return st;
 
+  CUtensorMap tmY;
+  const bool bf16_out = (y_type == FP4_OUT_BF16);
+  st = encode_tmap_2d(&tmY, bf16_out ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Y,
+                      uint64_t(N), uint64_t(M), uint64_t(ldy) * (bf16_out ? 2 : 4), bf16_out ? 40 : 20, 32,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != FP4_OK) return st;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -405,6 +439,6 @@ FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_byte
   p.wait_ns = kWaitLimitNs;
   const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kFwdBN - 1) / kFwdBN);
   const int grid = int(tiles < sms ? tiles : sms);
-  kern<<<grid, kThreads, C::kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmB, p);
+  kern<<<grid, kThreads, C::kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmB, tmY, p);
   return launch_status();
 }

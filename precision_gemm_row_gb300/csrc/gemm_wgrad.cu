@@ -43,15 +43,22 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kNAcc = 2;
 constexpr int kChunkStages = 16;                 // 1024 tokens per TMEM accumulation chunk
 constexpr int kEpiCols = kBN / 2;                // columns per epilogue warp
+constexpr int kBlk = 32;                         // epilogue block: 32 rows x 32 columns per warp
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 64;                          // features per TMA box (128 bytes of BF16)
 constexpr int kBoxBytes = kBox * kBT * 2;         // 8 KB
 constexpr int kAStage = (kBM / kBox) * kBoxBytes; // 16 KB
 constexpr int kBStage = (kBN / kBox) * kBoxBytes; // 32 KB
 constexpr int kStageBytes = kAStage + kBStage;
-constexpr int kStages = 4;
-constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNAcc + 1) + 16;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+constexpr int kStages = 3;
+// epilogue staging per warp: dW block 32 x 32 fp32 (128-byte swizzle) and two
+// W blocks 32 x 32 BF16 (64-byte swizzle), all moved by TMA
+constexpr int kOutBytes = kBlk * kBlk * 4;        // 4 KB
+constexpr int kWBytes = kBlk * kBlk * 2;          // 2 KB
+constexpr int kEpiWarpBytes = kOutBytes + 2 * kWBytes;
+constexpr int kDataBytes = kStages * kStageBytes + kEpiWarps * kEpiWarpBytes;
+constexpr int kNumBars = 2 * kStages + 2 * kNAcc + 1 + 2 * kEpiWarps;
+constexpr int kSmemBytes = 1024 + kDataBytes + 8 * kNumBars + 16;
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B BF16, both
 // MN-major, N = 256, M = 128.
@@ -70,43 +77,45 @@ struct WgradParams {
   uint64_t wait_ns;
 };
 
-// DGE factor f'(x) for the scaled weight magnitude x.
+// DGE factor f'(x) for the scaled weight magnitude x.  |u|^e uses the fast
+// power intrinsic (relative error a few fp32 ulps); u = 0 follows the limit of
+// |u|^e: +inf for e < 0 (then clipped), 1 for e = 0, 0 for e > 0.
 __device__ __forceinline__ float dge_factor(float x, float inv_k, float expo, float clip) {
   if (!(x < 6.0f)) return inv_k;
-  float lo, delta;
-  if (x < 2.0f) {
-    delta = 0.5f;
-    lo = floorf(x * 2.0f) * 0.5f;
-  } else if (x < 4.0f) {
-    delta = 1.0f;
-    lo = floorf(x);
-  } else {
-    delta = 2.0f;
-    lo = 4.0f;
-  }
-  const float u = fabsf(2.0f * (x - lo) / delta - 1.0f);
-  return fminf(clip, inv_k * powf(u, expo));  // u = 0 gives +inf, clipped
+  // interval [lo, lo + delta]: delta 0.5 below 2, 1 below 4, 2 below 6; 2/delta is a
+  // power of two, so (x - lo) * (2/delta) equals 2 (x - lo) / delta exactly
+  const bool a = x < 2.0f, b = x < 4.0f;
+  const float lo = a ? floorf(x * 2.0f) * 0.5f : (b ? floorf(x) : 4.0f);
+  const float two_over_delta = a ? 4.0f : (b ? 2.0f : 1.0f);
+  const float u = fabsf(fmaf(x - lo, two_over_delta, -1.0f));
+  const float pw = u > 0.0f ? __powf(u, expo) : (expo < 0.0f ? INFINITY : (expo == 0.0f ? 1.0f : 0.0f));
+  return fminf(clip, inv_k * pw);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     wgrad_dge_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
+                     const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmD,
                      const WgradParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kAStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2 * kNAcc + 1);
+  uint8_t* sEpi = smem + kStages * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDataBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kStages;
   const uint32_t accf0 = empty0 + 8 * kStages;
   const uint32_t acce0 = accf0 + 8 * kNAcc;
   const uint32_t done_bar = acce0 + 8 * kNAcc;
+  const uint32_t wbar0 = done_bar + 8;  // two per epilogue warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmG);
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmD);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -116,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(acce0 + 8 * b, kEpiWarps);
     }
     mbar_init(done_bar, 1);
+    for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(wbar0 + 8 * b, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -225,10 +235,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   } else {
     // ------------------------------------------------ chunk promotion + DGE epilogue
+    const int ew = warp - 2;
     const int q = warp & 3;
-    const int c_base = ((warp - 2) / 4) * kEpiCols;
-    const int r_local = q * 32 + lane;
+    const int c_base = (ew / 4) * kEpiCols;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
+    uint8_t* out_s = sEpi + ew * kEpiWarpBytes;          // 32 x 32 fp32, 128-byte swizzle
+    uint8_t* w_s = out_s + kOutBytes;                     // 2 x (32 x 32 BF16), 64-byte swizzle
+    const uint32_t wbar = wbar0 + 16 * ew;
+    uint32_t wuse[2] = {0u, 0u};                          // completed uses of each W buffer
+    uint32_t wissued[2] = {0u, 0u};                       // loads issued into each W buffer
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -244,12 +259,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < kEpiCols; c += 16) {
-          uint32_t r[16];
-          tmem_ld16(tmem + lane_base + uint32_t(acc * kBN + c_base + c), r);
+        for (int c = 0; c < kEpiCols; c += 32) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(tmem + lane_base + uint32_t(acc * kBN + c_base + c), r0);
+          tmem_ld16(tmem + lane_base + uint32_t(acc * kBN + c_base + c + 16), r1);
           tmem_wait_ld();
 #pragma unroll
-          for (int t = 0; t < 16; ++t) sum[c + t] += __uint_as_float(r[t]);
+          for (int t = 0; t < 16; ++t) {
+            sum[c + t] += __uint_as_float(r0[t]);
+            sum[c + 16 + t] += __uint_as_float(r1[t]);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -260,30 +279,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      const int row = rb * kBM + r_local;
-      if (row < p.K) {
-        const uint16_t* wrow = p.W + int64_t(row) * p.ldw;
-        float* drow = p.dW + int64_t(row) * p.lddw;
+      // DGE and store, one 32 x 32 block at a time: W block in by TMA (next
+      // block prefetched), factor per element, dW block out by TMA store.
+      const int row0 = rb * kBM + q * 32;
+      if (row0 >= p.K) continue;
+      constexpr int kNBlk = kEpiCols / kBlk;
+      auto issue_w = [&](int j) {
+        const int buf = j & 1;
+        ++wissued[buf];
+        if (lane == 0) {
+          mbar_arrive_expect_tx(wbar + 8 * buf, kWBytes);
+          tma_load_2d(smem_u32(w_s + buf * kWBytes), &tmW, wbar + 8 * buf, nb * kBN + c_base + j * kBlk, row0);
+        }
+      };
+      if (nb * kBN + c_base < p.N) issue_w(0);
 #pragma unroll
-        for (int c = 0; c < kEpiCols; c += 8) {
-          const int col0 = nb * kBN + c_base + c;
-          if (col0 < p.N) {  // N % 8 == 0: a group of 8 columns is all in or all out
-            const uint4 w8 = __ldg(reinterpret_cast<const uint4*>(wrow + col0));
-            const uint32_t wv[4] = {w8.x, w8.y, w8.z, w8.w};
-            float o[8];
+      for (int j = 0; j < kNBlk; ++j) {
+        const int col0 = nb * kBN + c_base + j * kBlk;
+        if (col0 >= p.N) break;  // same for the whole warp
+        if (j + 1 < kNBlk && col0 + kBlk < p.N) issue_w(j + 1);
+        const int buf = j & 1;
+        if (!mbar_wait(wbar + 8 * buf, wuse[buf] & 1u, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        ++wuse[buf];
+        // the previous block's TMA store must have read out_s before it is overwritten
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        // this lane's row of the W block: 4 chunks of 8 BF16, chunk c at physical c ^ ((lane >> 1) & 3);
+        // its row of the dW block: 8 chunks of 4 fp32, chunk c at physical c ^ (lane & 7)
+        const uint8_t* wrow = w_s + buf * kWBytes + lane * 64;
+        uint8_t* orow = out_s + lane * 128;
+        const float sw_lane = (col0 + lane < p.N) ? __ldg(p.s_w + col0 + lane) : 1.0f;  // column col0 + lane
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const float w = bf16_bits_to_float((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu);
-              const float x = fabsf(__fmul_rn(w, __ldg(p.s_w + col0 + t)));
-              o[t] = sum[c + t] * dge_factor(x, p.inv_k, p.expo, p.clip);
+        for (int c = 0; c < 4; ++c) {
+          const uint4 w8 = *reinterpret_cast<const uint4*>(wrow + ((c ^ ((lane >> 1) & 3)) << 4));
+          const uint32_t wv[4] = {w8.x, w8.y, w8.z, w8.w};
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float o[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int cc = 8 * c + 4 * half + t;
+              const float sw = __shfl_sync(0xFFFFFFFFu, sw_lane, cc);
+              const float w = bf16_bits_to_float((wv[(4 * half + t) >> 1] >> (16 * (t & 1))) & 0xFFFFu);
+              o[t] = sum[j * kBlk + cc] * dge_factor(fabsf(__fmul_rn(w, sw)), p.inv_k, p.expo, p.clip);
             }
-            float4* dst = reinterpret_cast<float4*>(drow + col0);
-            dst[0] = make_float4(o[0], o[1], o[2], o[3]);
-            dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+            const int oc = 2 * c + half;
+            *reinterpret_cast<float4*>(orow + ((oc ^ (lane & 7)) << 4)) = make_float4(o[0], o[1], o[2], o[3]);
           }
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmD, smem_u32(out_s), col0, row0);
+          bulk_commit_group();
+        }
       }
+      if (!ok) break;
     }
+    // on an early exit a prefetched W block may still be in flight: wait for it
+    for (int b = 0; b < 2; ++b)
+      if (wissued[b] > wuse[b] && !mbar_wait(wbar + 8 * b, wuse[b] & 1u, p.wait_ns)) ok = false;
+    if (lane == 0) bulk_wait_all();
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   }
 
@@ -320,6 +379,13 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   st = encode_tmap_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, uint64_t(N), uint64_t(M), uint64_t(lddy) * 2, kBox,
                       kBT, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != FP4_OK) return st;
+  CUtensorMap tmW, tmD;
+  st = encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, uint64_t(N), uint64_t(K), uint64_t(ldw) * 2, kBlk,
+                      kBlk, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (st != FP4_OK) return st;
+  st = encode_tmap_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, uint64_t(N), uint64_t(K), uint64_t(lddw) * 4, kBlk,
+                      kBlk, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != FP4_OK) return st;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -345,6 +411,6 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   p.wait_ns = kWaitLimitNs;
   const int64_t tiles = ((K + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
   const int grid = int(tiles < sms ? tiles : sms);
-  wgrad_dge_kernel<<<grid, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmG, p);
+  wgrad_dge_kernel<<<grid, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmG, tmW, tmD, p);
   return launch_status();
 }

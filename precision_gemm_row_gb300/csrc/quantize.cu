@@ -16,17 +16,19 @@ constexpr int kRowThreads = 256;  // 8 warps
 
 // Scales 8 BF16 values by s after clamping |x| to t, and packs their 8 E2M1
 // codes into one 32-bit word (element 0 in the lowest nibble).
+template <bool CLAMP>
 __device__ __forceinline__ uint32_t quantize8(const uint4 v, float s, float t) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t out = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float x = bf16_bits_to_float((w[i] >> (16 * h)) & 0xFFFFu);
-      if (fabsf(x) > t) x = copysignf(t, x);
-      out |= e2m1_encode(__fmul_rn(x, s)) << (4 * (2 * i + h));
+    float lo = bf16_bits_to_float(w[i] & 0xFFFFu);
+    float hi = bf16_bits_to_float(w[i] >> 16);
+    if (CLAMP) {
+      if (fabsf(lo) > t) lo = copysignf(t, lo);
+      if (fabsf(hi) > t) hi = copysignf(t, hi);
     }
+    out |= e2m1x2_encode(__fmul_rn(lo, s), __fmul_rn(hi, s)) << (8 * i);
   }
   return out;
 }
@@ -44,7 +46,7 @@ __device__ __forceinline__ float absmax8(const uint4 v, float t) {
 
 // Each row is handled by `wpr` warps; each lane keeps up to CH 16-byte chunks
 // of the row in registers, so A is read from HBM exactly once.
-template <int CH>
+template <int CH, bool CLAMP>
 __global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(const uint16_t* __restrict__ A, int64_t M,
                                                                     int K, int64_t lda,
                                                                     const float* __restrict__ clamp_t,
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(const uint16
   const int rows_per_cta = (kRowThreads / 32) / wpr;
   const int r_in_cta = warp / wpr, w_in_row = warp % wpr;
   const int nchunk = K >> 3;
-  const float t = clamp_t ? __ldg(clamp_t) : INFINITY;
+  const float t = CLAMP ? __ldg(clamp_t) : INFINITY;
 
   for (int64_t row0 = int64_t(blockIdx.x) * rows_per_cta; row0 < M; row0 += int64_t(gridDim.x) * rows_per_cta) {
     const int64_t row = row0 + r_in_cta;
@@ -84,7 +86,7 @@ __global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(const uint16
 #pragma unroll
       for (int c = 0; c < CH; ++c) {
         const int ci = lane + 32 * (w_in_row + wpr * c);
-        if (ci < nchunk) dst[ci] = quantize8(v[c], s, t);
+        if (ci < nchunk) dst[ci] = quantize8<CLAMP>(v[c], s, t);
       }
     }
   }
@@ -157,9 +159,12 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const uint16_t* __re
       w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float x = bf16_bits_to_float((w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
-      tile[cc * 8 + i][r] = static_cast<uint8_t>(e2m1_encode(__fmul_rn(x, s_col[cc * 8 + i])));
+    for (int i = 0; i < 8; i += 2) {
+      const float x0 = bf16_bits_to_float(w[i >> 1] & 0xFFFFu);
+      const float x1 = bf16_bits_to_float(w[i >> 1] >> 16);
+      const uint32_t c2 = e2m1x2_encode(__fmul_rn(x0, s_col[cc * 8 + i]), __fmul_rn(x1, s_col[cc * 8 + i + 1]));
+      tile[cc * 8 + i][r] = static_cast<uint8_t>(c2 & 0xFu);
+      tile[cc * 8 + i + 1][r] = static_cast<uint8_t>(c2 >> 4);
     }
   }
   __syncthreads();
@@ -188,8 +193,12 @@ void launch_rows(const uint16_t* A, int64_t M, int K, int64_t lda, const float* 
   const int64_t cap = int64_t(sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  quantize_rows_kernel<CH><<<unsigned(blocks), kRowThreads, 0, stream>>>(A, M, K, lda, clamp_t, codes, ldc, scales,
-                                                                         wpr);
+  if (clamp_t)
+    quantize_rows_kernel<CH, true><<<unsigned(blocks), kRowThreads, 0, stream>>>(A, M, K, lda, clamp_t, codes, ldc,
+                                                                               scales, wpr);
+  else
+    quantize_rows_kernel<CH, false><<<unsigned(blocks), kRowThreads, 0, stream>>>(A, M, K, lda, clamp_t, codes, ldc,
+                                                                                scales, wpr);
 }
 
 }  // namespace

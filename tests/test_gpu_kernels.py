@@ -61,6 +61,30 @@ def test_quantize_rows_bit_exact(fp4, M, K):
     assert_no_device_flags(fp4)
 
 
+@pytest.mark.parametrize("absmax", [6.0, 3.0, 12.0, 0.375, 1.5 * 2.0 ** -100])
+def test_quantize_rows_every_bf16_value_bit_exact(fp4, absmax):
+    # every finite BF16 magnitude up to absmax, both signs, in rows that each hold
+    # absmax once: the scale is 6/absmax for every row, so all scaled values
+    # (grid points, ties, boundaries, subnormals, zeros) are exercised
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = orc.bf16_to_f32(bits)
+    keep = np.isfinite(vals) & (np.abs(vals) <= np.float32(absmax))
+    bits = bits[keep]
+    per_row = 255
+    n_rows = -(-bits.size // per_row)
+    pad = np.zeros(n_rows * per_row, np.uint16)
+    pad[:bits.size] = bits
+    top = wl.f32_to_bf16_bits(np.array([absmax], np.float32))[0]
+    A_bits = np.concatenate([pad.reshape(n_rows, per_row), np.full((n_rows, 1), top, np.uint16)], axis=1)
+    codes, s = fp4.fp4_quantize_rows(dev_bf16(A_bits))
+    ref_codes, ref_s = orc.quantize_rows(orc.bf16_to_f32(A_bits))
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    got = codes.cpu().numpy()
+    bad = np.argwhere(got != ref_codes)
+    assert bad.size == 0, [(int(A_bits[r, 2 * c]), int(A_bits[r, 2 * c + 1]), int(got[r, c]), int(ref_codes[r, c]))
+                           for r, c in bad[:8]]
+
+
 def test_quantize_rows_with_fused_clamp_bit_exact(fp4):
     A_bits = _t3_bits(1, (96, 640), 2.0)
     t, _, _ = orc.quantile_threshold(A_bits, 0.97)
