@@ -1,10 +1,10 @@
 #!/usr/bin/env python
 """Benchmark of the FP4 quantized linear layer (forward + DGE weight gradient).
 
-One step = one pass of the whole hot path over one batch of synthetic input,
-for every linear of the workload:
-  quantile threshold + clamp + CSR compensation matrix  (outlier_clamp_quantile)
-  row quantization of A_clamped                          (fp4_quantize_rows, fused clamp)
+One step = one pass of the whole hot path over one batch of synthetic input:
+for every distinct activation (linears that share an input share this phase)
+  quantile threshold + clamp + CSR of dA + row codes of A_clamped (fp4_quantize_rows_outliers)
+and for every linear of the workload
   column quantization of W                               (fp4_quantize_cols)
   FP4 GEMM + scales + dA*W compensation -> BF16 Y       (fp4_linear_fwd)
   BF16 weight-gradient GEMM x DGE factor -> fp32 dW     (fp4_linear_wgrad_dge)
@@ -106,63 +106,102 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ the GPU arm
 
-class LayerStep:
-    """Preallocated buffers and launches for one linear of the workload."""
+class ActStep:
+    """One distinct activation (and clamp quantile): threshold, clamp, CSR of dA
+    and the row codes / scales of A_clamped, all in fp4_quantize_rows_outliers."""
 
-    def __init__(self, fp4, lin, A, W, dY):
+    PHASE = "fp4_quantize_rows_outliers"
+    LAUNCHES = 4   # histogram, fused row pass, row scan, CSR gather
+
+    def __init__(self, fp4, A, q):
         import torch
-        self.fp4, self.lin = fp4, lin
-        M, K, N = lin.M, lin.K, lin.N
+        self.fp4, self.A, self.q = fp4, A, q
+        M, K = A.shape
+        cap = fp4.outlier_max_nnz(M, K, q)
         dev = A.device
-        self.A, self.W, self.dY = A, W, dY
-        cap = fp4.outlier_max_nnz(M, K, lin.q)
         self.out = {
             "t": torch.empty(1, dtype=torch.float32, device=dev),
             "row_ptr": torch.empty(M + 1, dtype=torch.int32, device=dev),
             "col_idx": torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
             "vals": torch.empty(max(cap, 1), dtype=torch.float32, device=dev),
             "nnz": torch.empty(1, dtype=torch.int64, device=dev),
+            "codes": torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+            "scales": torch.empty(M, dtype=torch.float32, device=dev),
         }
         self.out["workspace"] = torch.empty(fp4.outlier_clamp_quantile_workspace(M, K, max(cap, 1)),
                                             dtype=torch.uint8, device=dev)
-        self.a_codes = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
-        self.s_a = torch.empty(M, dtype=torch.float32, device=dev)
+
+    def fn(self):
+        return lambda: self.fp4.fp4_quantize_rows_outliers(self.A, self.q, out=self.out)
+
+    def algorithmic_bytes(self) -> float:
+        """Two reads of A (the exact global quantile must be known before any
+        element is clamped), codes 0.5 B/elem, scales 4 B/row, CSR 8 B/entry + row_ptr."""
+        M, K = self.A.shape
+        nnz = int(self.out["nnz"].item())
+        return 4.0 * M * K + 0.5 * M * K + 4 * M + 8 * nnz + 4 * (M + 1)
+
+
+class LinStep:
+    """One linear: column quantization of W, FP4 GEMM, DGE weight gradient."""
+
+    PHASES = ("fp4_quantize_cols", "fp4_linear_fwd", "fp4_linear_wgrad_dge")
+    LAUNCHES = {"fp4_quantize_cols": 2, "fp4_linear_fwd": 1, "fp4_linear_wgrad_dge": 1}
+
+    def __init__(self, fp4, lin, act: ActStep, W, dY):
+        import torch
+        self.fp4, self.lin, self.act = fp4, lin, act
+        K, N = lin.K, lin.N
+        dev = W.device
+        self.W, self.dY = W, dY
         self.w_codes = torch.empty((N, K // 2), dtype=torch.uint8, device=dev)
         self.s_w = torch.empty(N, dtype=torch.float32, device=dev)
         self.ws_cols = torch.empty(max(fp4.fp4_quantize_cols_workspace(N), 16), dtype=torch.uint8, device=dev)
-        self.Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.Y = torch.empty((lin.M, N), dtype=torch.bfloat16, device=dev)
         self.dW = torch.empty((K, N), dtype=torch.float32, device=dev)
 
-    PHASES = ("outlier_clamp_quantile", "fp4_quantize_rows", "fp4_quantize_cols", "fp4_linear_fwd",
-              "fp4_linear_wgrad_dge")
-    LAUNCHES = {"outlier_clamp_quantile": 4, "fp4_quantize_rows": 1, "fp4_quantize_cols": 2, "fp4_linear_fwd": 1,
-                "fp4_linear_wgrad_dge": 1}
-
-    def phase_fns(self):
-        fp4, lin = self.fp4, self.lin
+    def fns(self):
+        fp4, lin, a = self.fp4, self.lin, self.act
         return [
-            lambda: fp4.outlier_clamp_quantile(self.A, lin.q, out=self.out),
-            lambda: fp4.fp4_quantize_rows(self.A, clamp_t=self.out["t"], codes=self.a_codes, scales=self.s_a),
             lambda: fp4.fp4_quantize_cols(self.W, codes_t=self.w_codes, scales=self.s_w, workspace=self.ws_cols),
-            lambda: fp4.fp4_linear_fwd(self.a_codes, self.s_a, self.w_codes, self.s_w, lin.K, csr=self.out,
+            lambda: fp4.fp4_linear_fwd(a.out["codes"], a.out["scales"], self.w_codes, self.s_w, lin.K, csr=a.out,
                                        W=self.W, out_type="bf16", Y=self.Y),
-            lambda: fp4.fp4_linear_wgrad_dge(self.A, self.dY, self.W, self.s_w, DGE_K, DGE_CLIP, dW=self.dW),
+            lambda: fp4.fp4_linear_wgrad_dge(a.A, self.dY, self.W, self.s_w, DGE_K, DGE_CLIP, dW=self.dW),
         ]
 
-    def run(self, events=None):
-        """One pass of the hot path with direct launches (events: 6 CUDA events, or None)."""
-        for i, fn in enumerate(self.phase_fns()):
-            if events is not None:
-                events[i].record()
+    def algorithmic(self):
+        M, K, N = self.lin.M, self.lin.K, self.lin.N
+        return {
+            "fp4_quantize_cols": (2.5 * K * N + 4 * N, "B", "hbm"),
+            "fp4_linear_fwd": (2 * M * K * N, "FLOP", "tensor_fp4"),
+            "fp4_linear_wgrad_dge": (2 * M * K * N, "FLOP", "tensor_bf16"),
+        }
+
+
+class StepPlan:
+    """All launches of one step: each distinct (activation, q) once, then every linear."""
+
+    def __init__(self, fp4, work, device_inputs):
+        self.acts = {}
+        self.lins = []
+        for lin, (A, W, dY) in zip(work.linears, device_inputs):
+            key = (lin.act, lin.q)
+            if key not in self.acts:
+                self.acts[key] = ActStep(fp4, A, lin.q)
+            self.lins.append(LinStep(fp4, lin, self.acts[key], W, dY))
+        # (phase name, callable) in launch order
+        self.calls = [(ActStep.PHASE, a.fn()) for a in self.acts.values()]
+        for l in self.lins:
+            self.calls += list(zip(LinStep.PHASES, l.fns()))
+
+    def run(self):
+        for _, fn in self.calls:
             fn()
-        if events is not None:
-            events[5].record()
 
     def capture(self):
-        """One CUDA graph per phase (the launches are stream-capture safe)."""
         import torch
         self.graphs = []
-        for fn in self.phase_fns():
+        for _, fn in self.calls:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 fn()
@@ -174,19 +213,10 @@ class LayerStep:
                 events[i].record()
             g.replay()
         if events is not None:
-            events[5].record()
+            events[len(self.graphs)].record()
 
-    def algorithmic(self, nnz: int):
-        """Algorithmic work per phase: (amount, unit, bound)."""
-        M, K, N = self.lin.M, self.lin.K, self.lin.N
-        n = M * K
-        return {
-            "outlier_clamp_quantile": (2 * n + 2 * n + 8 * nnz + 4 * (M + 1), "B", "hbm"),  # histogram + stage read A
-            "fp4_quantize_rows": (2.5 * n + 4 * M, "B", "hbm"),
-            "fp4_quantize_cols": (2.5 * K * N + 4 * N, "B", "hbm"),
-            "fp4_linear_fwd": (2 * M * K * N, "FLOP", "tensor_fp4"),
-            "fp4_linear_wgrad_dge": (2 * M * K * N, "FLOP", "tensor_bf16"),
-        }
+    def launches(self):
+        return ActStep.LAUNCHES * len(self.acts) + sum(LinStep.LAUNCHES.values()) * len(self.lins)
 
 
 def _src_hash(files):
@@ -200,9 +230,8 @@ def _src_hash(files):
 KERNEL_SOURCES = {
     "fp4_linear_wgrad_dge": ["gemm_wgrad.cu", "common.cuh"],
     "fp4_linear_fwd": ["gemm_fwd.cu", "common.cuh"],
-    "fp4_quantize_rows": ["quantize.cu", "common.cuh"],
     "fp4_quantize_cols": ["quantize.cu", "common.cuh"],
-    "outlier_clamp_quantile": ["outlier.cu", "common.cuh"],
+    "fp4_quantize_rows_outliers": ["outlier.cu", "common.cuh"],
 }
 
 
@@ -241,39 +270,41 @@ def run_gpu(args):
     from precision_gemm_row_gb300 import fp4lin as fp4
 
     work = wl.WORKLOADS[args.workload]
-    steps = []
     host = []
+    dev_inputs = []
+    pinned_cache = {}
+    to_pinned = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory()
     for lin in work.linears:
-        A_bits, W_bits, dY_bits = work.activation(lin), work.weight(lin), work.grad(lin)
-        to_pinned = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory()
-        hA, hW, hG = to_pinned(A_bits), to_pinned(W_bits), to_pinned(dY_bits)
-        A, W, dY = hA.cuda(), hW.cuda(), hG.cuda()
-        steps.append(LayerStep(fp4, lin, A, W, dY))
+        akey = (lin.act,)
+        if akey not in pinned_cache:
+            pinned_cache[akey] = to_pinned(work.activation(lin))
+        hA = pinned_cache[akey]
+        hW, hG = to_pinned(work.weight(lin)), to_pinned(work.grad(lin))
         host.append((hA, hW, hG))
+    dev_cache = {}
+    for lin, (hA, hW, hG) in zip(work.linears, host):
+        if id(hA) not in dev_cache:
+            dev_cache[id(hA)] = hA.cuda()
+        dev_inputs.append((dev_cache[id(hA)], hW.cuda(), hG.cuda()))
+    plan = StepPlan(fp4, work, dev_inputs)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     flops = sum(4 * l.M * l.K * l.N for l in work.linears)
 
     for _ in range(args.warmup):
-        for s in steps:
-            s.run()
+        plan.run()
     torch.cuda.synchronize()
-    for s in steps:
-        s.capture()
+    plan.capture()
     torch.cuda.synchronize()
-
-    def one_step(ev=None):
-        for i, s in enumerate(steps):
-            s.replay(ev[i] if ev is not None else None)
-
     for _ in range(args.warmup):
-        one_step()
+        plan.replay()
     st, fl = fp4.fp4_device_status()
     if st != "FP4_OK":
         raise RuntimeError(f"device status after warm-up: {st} flags={fl}")
 
     # ---- device-resident timed region: L2 flush, then a short GPU-side head start
     # so every replay of the step is queued before the first event fires
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in steps] for _ in range(args.steps)]
+    ncalls = len(plan.calls)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ncalls + 1)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -281,36 +312,41 @@ def run_gpu(args):
         for k in range(args.steps):
             flush.fill_(float(k))
             torch.cuda._sleep(HEAD_START_CYCLES)
-            one_step(ev[k])
+            plan.replay(ev[k])
         torch.cuda.synchronize()
     st, fl = fp4.fp4_device_status()
     if st != "FP4_OK":
         raise RuntimeError(f"device status after timed steps: {st} flags={fl}")
-    step_ms = [sum(ev[k][i][0].elapsed_time(ev[k][i][5]) for i in range(len(steps))) for k in range(args.steps)]
+    step_ms = [ev[k][0].elapsed_time(ev[k][ncalls]) for k in range(args.steps)]
     ms_per_step = sum(step_ms) / len(step_ms)
     phase_ms = {}
-    for p, name in enumerate(LayerStep.PHASES):
-        phase_ms[name] = sum(ev[k][i][p].elapsed_time(ev[k][i][p + 1]) for k in range(args.steps)
-                             for i in range(len(steps))) / args.steps
+    for i, (name, _) in enumerate(plan.calls):
+        phase_ms[name] = phase_ms.get(name, 0.0) + sum(ev[k][i].elapsed_time(ev[k][i + 1])
+                                                      for k in range(args.steps)) / args.steps
 
     # ---- end to end through the C ABI from pinned host buffers
-    hY = [torch.empty(s.Y.shape, dtype=s.Y.dtype).pin_memory() for s in steps]
-    hdW = [torch.empty(s.dW.shape, dtype=s.dW.dtype).pin_memory() for s in steps]
-    bi = sum(h[0].numel() * 2 + h[1].numel() * 2 + h[2].numel() * 2 for h in host)
+    hY = [torch.empty(l.Y.shape, dtype=l.Y.dtype).pin_memory() for l in plan.lins]
+    hdW = [torch.empty(l.dW.shape, dtype=l.dW.dtype).pin_memory() for l in plan.lins]
+    uniq_hA = {id(h[0]): h[0] for h in host}
+    bi = sum(h.numel() * 2 for h in uniq_hA.values()) + sum(h[1].numel() * 2 + h[2].numel() * 2 for h in host)
     bo = sum(y.numel() * 2 + d.numel() * 4 for y, d in zip(hY, hdW))
     e2e_ms = []
     for k in range(args.warmup + args.steps):
         flush.fill_(float(k))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for i, s in enumerate(steps):
-            s.A.copy_(host[i][0], non_blocking=True)
-            s.W.copy_(host[i][1], non_blocking=True)
-            s.dY.copy_(host[i][2], non_blocking=True)
-            for g in s.graphs:
-                g.replay()
-            hY[i].copy_(s.Y, non_blocking=True)
-            hdW[i].copy_(s.dW, non_blocking=True)
+        copied = set()
+        for i, l in enumerate(plan.lins):
+            if id(host[i][0]) not in copied:
+                l.act.A.copy_(host[i][0], non_blocking=True)
+                copied.add(id(host[i][0]))
+            l.W.copy_(host[i][1], non_blocking=True)
+            l.dY.copy_(host[i][2], non_blocking=True)
+        for g in plan.graphs:
+            g.replay()
+        for i, l in enumerate(plan.lins):
+            hY[i].copy_(l.Y, non_blocking=True)
+            hdW[i].copy_(l.dW, non_blocking=True)
         e1.record()
         e1.synchronize()
         if k >= args.warmup:
@@ -325,11 +361,14 @@ def run_gpu(args):
 
     peaks, peak_src = load_peaks()
     fp4_peak = peaks["bf16_tflops"] * FP4_PER_BF16
-    nnz = sum(int(s.out["nnz"].item()) for s in steps)
+    nnz = sum(int(a.out["nnz"].item()) for a in plan.acts.values())
+    amounts = {ActStep.PHASE: (sum(a.algorithmic_bytes() for a in plan.acts.values()), "B", "hbm")}
+    for l in plan.lins:
+        for name, (amt, unit, bound) in l.algorithmic().items():
+            prev = amounts.get(name, (0.0, unit, bound))
+            amounts[name] = (prev[0] + amt, unit, bound)
     kernels = {}
-    for name in LayerStep.PHASES:
-        amount = sum(s.algorithmic(int(s.out["nnz"].item()))[name][0] for s in steps)
-        unit, bound = steps[0].algorithmic(0)[name][1:]
+    for name, (amount, unit, bound) in amounts.items():
         per_s = amount / (phase_ms[name] * 1e-3)
         if unit == "B":
             ach, u, pk = per_s / 1e9, "GB/s", peaks["hbm_gbs"]
@@ -345,9 +384,9 @@ def run_gpu(args):
     roofline = {"bound": kd["bound"], "kernel": dom, "achieved": kd["achieved"], "peak": kd["peak"],
                 "peak_source": f"{peak_src}" + (" x nominal FP4/BF16 ratio 6" if dom == "fp4_linear_fwd" else ""),
                 "unit": kd["unit"], "frac": kd["frac"], "traffic": tr}
-    quant_bytes = sum(kernels[n]["achieved"] * kernels[n]["ms"] * 1e-3 * 1e9 for n in
-                      ("outlier_clamp_quantile", "fp4_quantize_rows", "fp4_quantize_cols"))
-    quant_ms = sum(kernels[n]["ms"] for n in ("outlier_clamp_quantile", "fp4_quantize_rows", "fp4_quantize_cols"))
+    qnames = (ActStep.PHASE, "fp4_quantize_cols")
+    quant_bytes = sum(amounts[n][0] for n in qnames)
+    quant_ms = sum(kernels[n]["ms"] for n in qnames)
     value = world * flops / (ms_max * 1e-3) / 1e12
     e2e_value = world * flops / (e2e_max * 1e-3) / 1e12
     line = {
@@ -366,7 +405,7 @@ def run_gpu(args):
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "ms_per_step": round(e2e_max, 5)},
-        "gpu_launches": args.steps * len(steps) * sum(LayerStep.LAUNCHES.values()),
+        "gpu_launches": args.steps * plan.launches(),
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:

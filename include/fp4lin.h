@@ -70,6 +70,10 @@ const char* fp4_status_string(fp4_status status);
 /* Version of this ABI (incremented on any signature change). */
 int fp4_abi_version(void);
 
+/* Text of the CUDA error behind the calling thread's most recent FP4_ERR_CUDA
+ * from a kernel launch (static string, never NULL). */
+const char* fp4_last_cuda_error(void);
+
 /*
  * fp4_quantize_rows -- token-wise (row) absmax quantization of A to E2M1, with
  * an optional fused outlier clamp.
@@ -84,7 +88,7 @@ int fp4_abi_version(void);
  * fp32 product x' * s_A[i], saturating at 6, sign kept for values rounding to 0.
  *
  *   A       device, BF16, M x K, row stride lda (elements); 16-byte aligned
- *   M, K    M >= 0; K > 0 and K % 32 == 0
+ *   M, K    M >= 0; 0 < K <= 16384 and K % 32 == 0
  *   lda     >= K, lda % 8 == 0
  *   clamp_t device fp32 scalar (e.g. t_out of outlier_clamp_quantile) or NULL
  *   codes   device, uint8, M x ldc_bytes, row i holds K/2 bytes; 16-byte aligned
@@ -155,8 +159,8 @@ fp4_status fp4_quantize_cols_noalloc(const void* W, int64_t K, int64_t N, int64_
  * with |A| > t; A_clamped = sign(A) min(|A|, t); dA values = A - sign(A) t in
  * fp32.  Rows ascending, column indices ascending within a row.
  *
- *   A        device, BF16, M x K (row stride lda), 16-byte aligned; M*K >= 1
- *   K        K % 8 == 0; lda >= K, lda % 8 == 0
+ *   A        device, BF16, M x K (row stride lda), 16-byte aligned; 1 <= M*K < 2^32
+ *   K        K % 8 == 0, K <= 16384; lda >= K, lda % 8 == 0
  *   q        0 < q <= 1
  *   t_out    device fp32 scalar: t (feed it to fp4_quantize_rows as clamp_t)
  *   row_ptr  device int32, M + 1
@@ -180,6 +184,30 @@ fp4_status outlier_clamp_quantile(const void* A, int64_t M, int64_t K, int64_t l
                                   int64_t nnz_capacity, int64_t* nnz_out, void* A_clamped,
                                   int64_t ldac, void* workspace, size_t ws_bytes,
                                   fp4_stream_t stream);
+
+/*
+ * fp4_quantize_rows_outliers -- outlier_clamp_quantile and
+ * fp4_quantize_rows(clamp_t = t) in one call that reads A twice instead of
+ * three times: the first pass finds the threshold t, the second clamps,
+ * stages the CSR entries of dA and writes the E2M1 codes and row scales of
+ * A_clamped from the same registers.
+ *
+ * Defined by: the passages cited for outlier_clamp_quantile and
+ * fp4_quantize_rows (clamping happens before the row quantization, page
+ * "首个 FP4 ..." (czzqal.com), outlier and quantization passages).  Outputs are
+ * bit-identical to the two separate calls.
+ *
+ *   A, M, K, lda, q, t_out, row_ptr, col_idx, vals, nnz_capacity, nnz_out,
+ *   workspace, ws_bytes   as for outlier_clamp_quantile (no A_clamped output)
+ *   codes, ldc_bytes, scales   as for fp4_quantize_rows; K % 32 == 0
+ * Both calls' limits apply, in particular K <= 16384.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, CAPACITY, WORKSPACE,
+ *         DEVICE_UNSUPPORTED, CUDA.
+ */
+fp4_status fp4_quantize_rows_outliers(const void* A, int64_t M, int64_t K, int64_t lda, double q, uint8_t* codes,
+                                      int64_t ldc_bytes, float* scales, float* t_out, int32_t* row_ptr,
+                                      int32_t* col_idx, float* vals, int64_t nnz_capacity, int64_t* nnz_out,
+                                      void* workspace, size_t ws_bytes, fp4_stream_t stream);
 
 /*
  * fp4_linear_fwd -- FP4 GEMM on tcgen05 (kind::mxf4, unit block scales) with
@@ -230,7 +258,9 @@ fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_bytes, const
  *   W   device BF16 K x ldw, s_w device fp32 N (from fp4_quantize_cols)
  *   M, N, K  M >= 1; N % 8 == 0; K % 8 == 0; all < 2^31
  *   dge_k > 0, dge_clip > 0
- *   dW  device fp32 K x lddw, 16-byte aligned, lddw % 4 == 0
+ *   dW  device fp32 K x lddw, 16-byte aligned, lddw % 4 == 0; the call first
+ *       writes the DGE factors there and then multiplies them by G in place,
+ *       so dW must not alias A, dY, W or s_w
  * Errors: INVALID_ARG, SHAPE, ALIGNMENT, DEVICE_UNSUPPORTED, CUDA;
  *         device-side TIMEOUT flag as for fp4_linear_fwd.
  */

@@ -81,7 +81,18 @@ fp4_status encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const voi
   return r == CUDA_SUCCESS ? FP4_OK : FP4_ERR_CUDA;
 }
 
-fp4_status launch_status() { return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA; }
+namespace {
+thread_local const char* t_last_cuda_error = "no CUDA error";
+}  // namespace
+
+fp4_status launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return FP4_OK;
+  t_last_cuda_error = cudaGetErrorString(e);
+  return FP4_ERR_CUDA;
+}
+
+const char* last_cuda_error() { return t_last_cuda_error; }
 
 namespace {
 // One CTA waits on an mbarrier that is never arrived on; the bounded wait
@@ -120,6 +131,8 @@ FP4_API const char* fp4_status_string(fp4_status s) {
 }
 
 FP4_API int fp4_abi_version(void) { return 1; }
+
+FP4_API const char* fp4_last_cuda_error(void) { return fp4::last_cuda_error(); }
 
 FP4_API fp4_status fp4_device_status(fp4_stream_t stream, uint32_t* flags_out) {
   fp4_status st = fp4::check_device(nullptr);

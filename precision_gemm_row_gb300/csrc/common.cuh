@@ -24,8 +24,9 @@ uint32_t* status_word();
 fp4_status encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0,
                           uint64_t dim1, uint64_t row_stride_bytes, uint32_t box0, uint32_t box1,
                           CUtensorMapSwizzle swizzle);
-// Maps the last launch error to FP4_ERR_CUDA.
+// Maps the last launch error to FP4_ERR_CUDA (and remembers its text for this thread).
 fp4_status launch_status();
+const char* last_cuda_error();
 // Default limit for bounded mbarrier waits, in nanoseconds.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
@@ -211,19 +212,6 @@ __device__ __forceinline__ float scale_from_absmax(float absmax) {
   return (absmax == 0.0f || !isfinite(s)) ? 1.0f : s;
 }
 
-// E2M1 code of y: nearest of {0,.5,1,1.5,2,3,4,6}, ties to the even code,
-// saturating, sign bit copied from y.  Counts the decision boundaries that |y|
-// has passed; a boundary is strict (>) where the tie goes down to the even
-// code and inclusive (>=) where it goes up to it.
-__device__ __forceinline__ uint32_t e2m1_encode(float y) {
-  const float a = fabsf(y);
-  const uint32_t mag = static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
-                       static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
-                       static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) +
-                       static_cast<uint32_t>(a > 5.0f);
-  return mag | ((__float_as_uint(y) >> 28) & 8u);
-}
-
 // Two E2M1 codes in one byte (lo in bits 3..0, hi in bits 7..4) by the hardware
 // conversion (round to nearest even, saturating to +-6).  The sign bits are
 // then set from the inputs, so a value that rounds to zero keeps its sign.
@@ -236,5 +224,64 @@ __device__ __forceinline__ uint32_t e2m1x2_encode(float lo, float hi) {
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// Scales 8 BF16 values by s after clamping |x| to t, and packs their 8 E2M1
+// codes into one 32-bit word (element 0 in the lowest nibble).
+// Packed BF16 helpers: a 32-bit word holds two BF16 values, element 2i in the
+// low half.  Magnitudes compare as unsigned 15-bit integers (sign cleared).
+
+// sign(x) min(|x|, t) for both halves, with tb2 = t's 15-bit pattern in both
+// halves: exact, since t is itself a BF16 value.
+__device__ __forceinline__ uint32_t clamp_pair(uint32_t w, uint32_t tb2) {
+  const uint32_t gt = __vcmpgtu2(w & 0x7FFF7FFFu, tb2);
+  return (w & ~gt) | (((w & 0x80008000u) | tb2) & gt);
+}
+
+// Two E2M1 codes (one byte) of the fp32 products x * s of a BF16 pair.
+__device__ __forceinline__ uint32_t quantize_pair(uint32_t w, float s) {
+  return e2m1x2_encode(__fmul_rn(__uint_as_float(w << 16), s), __fmul_rn(__uint_as_float(w & 0xFFFF0000u), s));
+}
+
+// Eight codes of a 16-byte chunk of BF16 values, element 0 in the lowest nibble;
+// with CLAMP the values are first clamped to t (tb2 as for clamp_pair).
+template <bool CLAMP>
+__device__ __forceinline__ uint32_t quantize8(const uint4 v, float s, uint32_t tb2) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) out |= quantize_pair(CLAMP ? clamp_pair(w[i], tb2) : w[i], s) << (8 * i);
+  return out;
+}
+
+// As quantize8<true> for a clamp threshold t that need not be a BF16 value:
+// the clamp sign(x) min(|x|, t) is taken in fp32.
+__device__ __forceinline__ uint32_t quantize8_clamp_f32(const uint4 v, float s, float t) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+    if (fabsf(lo) > t) lo = copysignf(t, lo);
+    if (fabsf(hi) > t) hi = copysignf(t, hi);
+    out |= e2m1x2_encode(__fmul_rn(lo, s), __fmul_rn(hi, s)) << (8 * i);
+  }
+  return out;
+}
+
+// Running maximum of the 15-bit magnitude patterns of a chunk, per 16-bit half.
+__device__ __forceinline__ uint32_t maxmag8(const uint4 v, uint32_t acc) {
+  acc = __vmaxu2(acc, v.x & 0x7FFF7FFFu);
+  acc = __vmaxu2(acc, v.y & 0x7FFF7FFFu);
+  acc = __vmaxu2(acc, v.z & 0x7FFF7FFFu);
+  return __vmaxu2(acc, v.w & 0x7FFF7FFFu);
+}
+
+// Largest magnitude pattern of a warp's packed maxima, as an fp32 value.
+__device__ __forceinline__ uint32_t warp_max_bits(uint32_t acc2) {
+  uint32_t m = max(acc2 & 0xFFFFu, acc2 >> 16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  return m;
+}
 
 }  // namespace fp4

@@ -26,7 +26,11 @@
 //
 // Roles (10 warps): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
 // warps 2-9 epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (one dW row per
-// thread) and columns (w-2)/4 * 128 .. +127 of the 256-wide tile.  Every
+// thread) and columns (w-2)/4 * 128 .. +127 of the 256-wide tile.  At the
+// start of each tile, while the tensor core runs its first chunks, the
+// epilogue warps write the DGE factors of the tile into dW; after the last
+// chunk they multiply them by the gradient in place (coalesced row chunks
+// through a swizzled staging tile).  Every
 // mbarrier wait is bounded; on expiry the CTA records FP4_FLAG_TIMEOUT,
 // drains its TMA loads and MMAs, frees TMEM and exits.
 #include "common.cuh"
@@ -50,14 +54,13 @@ constexpr int kBoxBytes = kBox * kBT * 2;         // 8 KB
 constexpr int kAStage = (kBM / kBox) * kBoxBytes; // 16 KB
 constexpr int kBStage = (kBN / kBox) * kBoxBytes; // 32 KB
 constexpr int kStageBytes = kAStage + kBStage;
-constexpr int kStages = 3;
-// epilogue staging per warp: dW block 32 x 32 fp32 (128-byte swizzle) and two
-// W blocks 32 x 32 BF16 (64-byte swizzle), all moved by TMA
+constexpr int kStages = 4;
+// epilogue staging per warp: one dW block of 32 x 32 fp32 (128-byte swizzle),
+// written out with coalesced stores (TMA stays free for the main loop's stages)
 constexpr int kOutBytes = kBlk * kBlk * 4;        // 4 KB
-constexpr int kWBytes = kBlk * kBlk * 2;          // 2 KB
-constexpr int kEpiWarpBytes = kOutBytes + 2 * kWBytes;
+constexpr int kEpiWarpBytes = kOutBytes;
 constexpr int kDataBytes = kStages * kStageBytes + kEpiWarps * kEpiWarpBytes;
-constexpr int kNumBars = 2 * kStages + 2 * kNAcc + 1 + 2 * kEpiWarps;
+constexpr int kNumBars = 2 * kStages + 2 * kNAcc + 1;
 constexpr int kSmemBytes = 1024 + kDataBytes + 8 * kNumBars + 16;
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A and B BF16, both
@@ -72,29 +75,28 @@ struct WgradParams {
   float* dW;
   int64_t lddw;
   int M, N, K;
-  float inv_k, expo, clip;
+  float inv_k, expo, clip, pw0;
   uint32_t* status;
   uint64_t wait_ns;
 };
 
 // DGE factor f'(x) for the scaled weight magnitude x.  |u|^e uses the fast
-// power intrinsic (relative error a few fp32 ulps); u = 0 follows the limit of
-// |u|^e: +inf for e < 0 (then clipped), 1 for e = 0, 0 for e > 0.
-__device__ __forceinline__ float dge_factor(float x, float inv_k, float expo, float clip) {
-  if (!(x < 6.0f)) return inv_k;
-  // interval [lo, lo + delta]: delta 0.5 below 2, 1 below 4, 2 below 6; 2/delta is a
-  // power of two, so (x - lo) * (2/delta) equals 2 (x - lo) / delta exactly
-  const bool a = x < 2.0f, b = x < 4.0f;
-  const float lo = a ? floorf(x * 2.0f) * 0.5f : (b ? floorf(x) : 4.0f);
-  const float two_over_delta = a ? 4.0f : (b ? 2.0f : 1.0f);
-  const float u = fabsf(fmaf(x - lo, two_over_delta, -1.0f));
-  const float pw = u > 0.0f ? __powf(u, expo) : (expo < 0.0f ? INFINITY : (expo == 0.0f ? 1.0f : 0.0f));
-  return fminf(clip, inv_k * pw);
+// power intrinsic (relative error a few fp32 ulps); u = 0 takes pw0, the limit
+// of |u|^e there: +inf for e < 0 (then clipped), 1 for e = 0, 0 for e > 0.
+// Written without branches: the interval is found by scaling x with 2/delta
+// (a power of two, so s and its fractional part are exact), and every case is
+// a select, so a warp never diverges over mixed magnitudes.
+__device__ __forceinline__ float dge_factor(float x, float inv_k, float expo, float clip, float pw0) {
+  const float two_over_delta = x < 2.0f ? 2.0f : (x < 4.0f ? 1.0f : 0.5f);
+  const float s = x * two_over_delta;                        // interval [floor(s), floor(s) + 1)
+  const float u = fabsf(fmaf(s - floorf(s), 2.0f, -1.0f));   // |2 (x - lo) / delta - 1|
+  const float pw = u > 0.0f ? __powf(u, expo) : pw0;
+  const float f = fminf(clip, inv_k * pw);
+  return x < 6.0f ? f : inv_k;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     wgrad_dge_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
-                     const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmD,
                      const WgradParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -108,14 +110,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t accf0 = empty0 + 8 * kStages;
   const uint32_t acce0 = accf0 + 8 * kNAcc;
   const uint32_t done_bar = acce0 + 8 * kNAcc;
-  const uint32_t wbar0 = done_bar + 8;  // two per epilogue warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmG);
-    prefetch_tmap(&tmW);
-    prefetch_tmap(&tmD);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -125,7 +124,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(acce0 + 8 * b, kEpiWarps);
     }
     mbar_init(done_bar, 1);
-    for (int b = 0; b < 2 * kEpiWarps; ++b) mbar_init(wbar0 + 8 * b, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -240,15 +238,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c_base = (ew / 4) * kEpiCols;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
     uint8_t* out_s = sEpi + ew * kEpiWarpBytes;          // 32 x 32 fp32, 128-byte swizzle
-    uint8_t* w_s = out_s + kOutBytes;                     // 2 x (32 x 32 BF16), 64-byte swizzle
-    const uint32_t wbar = wbar0 + 16 * ew;
-    uint32_t wuse[2] = {0u, 0u};                          // completed uses of each W buffer
-    uint32_t wissued[2] = {0u, 0u};                       // loads issued into each W buffer
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
+    constexpr int kNBlk = kEpiCols / kBlk;
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       const int rb = tile % num_r, nb = tile / num_r;
+      const int row0 = rb * kBM + q * 32;  // first dW row of this warp's 32-row slab
+      // (1) While the tile's first chunks run on the tensor core, this warp
+      // writes the DGE factors f'(|W s_W|) of its 32 x 128 slab into dW; the
+      // final pass multiplies them by the gradient in place.  Each block goes
+      // through the swizzled staging tile and out as coalesced 128-byte rows;
+      // the final pass reads every element back from the same lane that wrote it.
+      if (row0 < p.K) {
+        const int my_row = row0 + lane;
+        const uint16_t* wrow = p.W + int64_t(my_row < p.K ? my_row : row0) * p.ldw;
+        // all loads of the pass first (one memory latency), then the math
+        uint4 w[kNBlk][4];
+        float swv[kNBlk];
+#pragma unroll
+        for (int j = 0; j < kNBlk; ++j) {
+          const int col0 = nb * kBN + c_base + j * kBlk;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            w[j][c] = (col0 + 8 * c < p.N) ? __ldg(reinterpret_cast<const uint4*>(wrow + col0 + 8 * c))
+                                           : make_uint4(0u, 0u, 0u, 0u);
+          swv[j] = (col0 + lane < p.N) ? __ldg(p.s_w + col0 + lane) : 1.0f;  // column col0 + lane
+        }
+#pragma unroll
+        for (int j = 0; j < kNBlk; ++j) {
+          const int col0 = nb * kBN + c_base + j * kBlk;
+          if (col0 < p.N) {  // same for the whole warp
+            __syncwarp();  // the staging tile is free
+            uint8_t* orow = out_s + lane * 128;  // this lane's row: chunk c at c ^ (lane & 7)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t wv[4] = {w[j][c].x, w[j][c].y, w[j][c].z, w[j][c].w};
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                float f[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                  const int cc = 8 * c + 4 * half + t;
+                  const float sw = __shfl_sync(0xFFFFFFFFu, swv[j], cc);
+                  const float wf = bf16_bits_to_float((wv[(4 * half + t) >> 1] >> (16 * (t & 1))) & 0xFFFFu);
+                  f[t] = dge_factor(fabsf(__fmul_rn(wf, sw)), p.inv_k, p.expo, p.clip, p.pw0);
+                }
+                const int oc = 2 * c + half;
+                *reinterpret_cast<float4*>(orow + ((oc ^ (lane & 7)) << 4)) = make_float4(f[0], f[1], f[2], f[3]);
+              }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {  // lane l: chunk l % 8 of rows l / 8 + 4 i
+              const int r = (lane >> 3) + 4 * i, c = lane & 7;
+              const int grow = row0 + r, gcol = col0 + 4 * c;
+              if (grow < p.K && gcol < p.N)
+                *reinterpret_cast<float4*>(p.dW + int64_t(grow) * p.lddw + gcol) =
+                    *reinterpret_cast<const float4*>(out_s + r * 128 + ((c ^ (r & 7)) << 4));
+            }
+          }
+        }
+      }
       float sum[kEpiCols];
 #pragma unroll
       for (int c = 0; c < kEpiCols; ++c) sum[c] = 0.0f;
@@ -279,70 +330,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // DGE and store, one 32 x 32 block at a time: W block in by TMA (next
-      // block prefetched), factor per element, dW block out by TMA store.
-      const int row0 = rb * kBM + q * 32;
+      // (3) dW = G * f': this lane's sums go through the staging tile so that the
+      // multiply, the read of f' and the store of dW are coalesced row chunks.
       if (row0 >= p.K) continue;
-      constexpr int kNBlk = kEpiCols / kBlk;
-      auto issue_w = [&](int j) {
-        const int buf = j & 1;
-        ++wissued[buf];
-        if (lane == 0) {
-          mbar_arrive_expect_tx(wbar + 8 * buf, kWBytes);
-          tma_load_2d(smem_u32(w_s + buf * kWBytes), &tmW, wbar + 8 * buf, nb * kBN + c_base + j * kBlk, row0);
-        }
-      };
-      if (nb * kBN + c_base < p.N) issue_w(0);
 #pragma unroll
       for (int j = 0; j < kNBlk; ++j) {
         const int col0 = nb * kBN + c_base + j * kBlk;
         if (col0 >= p.N) break;  // same for the whole warp
-        if (j + 1 < kNBlk && col0 + kBlk < p.N) issue_w(j + 1);
-        const int buf = j & 1;
-        if (!mbar_wait(wbar + 8 * buf, wuse[buf] & 1u, p.wait_ns)) {
-          ok = false;
-          break;
-        }
-        ++wuse[buf];
-        // the previous block's TMA store must have read out_s before it is overwritten
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-        // this lane's row of the W block: 4 chunks of 8 BF16, chunk c at physical c ^ ((lane >> 1) & 3);
-        // its row of the dW block: 8 chunks of 4 fp32, chunk c at physical c ^ (lane & 7)
-        const uint8_t* wrow = w_s + buf * kWBytes + lane * 64;
+        __syncwarp();  // the staging tile is free
         uint8_t* orow = out_s + lane * 128;
-        const float sw_lane = (col0 + lane < p.N) ? __ldg(p.s_w + col0 + lane) : 1.0f;  // column col0 + lane
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 w8 = *reinterpret_cast<const uint4*>(wrow + ((c ^ ((lane >> 1) & 3)) << 4));
-          const uint32_t wv[4] = {w8.x, w8.y, w8.z, w8.w};
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(orow + ((c ^ (lane & 7)) << 4)) =
+              make_float4(sum[j * kBlk + 4 * c], sum[j * kBlk + 4 * c + 1], sum[j * kBlk + 4 * c + 2],
+                          sum[j * kBlk + 4 * c + 3]);
+        __syncwarp();
+        // the factors of this block (written by this same lane in the factor pass):
+        // all eight loads before any store, so they are in flight together
+        float4 f[8];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float o[4];
+        for (int i = 0; i < 8; ++i) {  // same lane-to-element map as the factor pass
+          const int r = (lane >> 3) + 4 * i, c = lane & 7;
+          const int grow = row0 + r, gcol = col0 + 4 * c;
+          f[i] = (grow < p.K && gcol < p.N) ? __ldcg(reinterpret_cast<const float4*>(p.dW + int64_t(grow) * p.lddw + gcol))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int cc = 8 * c + 4 * half + t;
-              const float sw = __shfl_sync(0xFFFFFFFFu, sw_lane, cc);
-              const float w = bf16_bits_to_float((wv[(4 * half + t) >> 1] >> (16 * (t & 1))) & 0xFFFFu);
-              o[t] = sum[j * kBlk + cc] * dge_factor(fabsf(__fmul_rn(w, sw)), p.inv_k, p.expo, p.clip);
-            }
-            const int oc = 2 * c + half;
-            *reinterpret_cast<float4*>(orow + ((oc ^ (lane & 7)) << 4)) = make_float4(o[0], o[1], o[2], o[3]);
+        for (int i = 0; i < 8; ++i) {
+          const int r = (lane >> 3) + 4 * i, c = lane & 7;
+          const int grow = row0 + r, gcol = col0 + 4 * c;
+          if (grow < p.K && gcol < p.N) {
+            const float4 g = *reinterpret_cast<const float4*>(out_s + r * 128 + ((c ^ (r & 7)) << 4));
+            *reinterpret_cast<float4*>(p.dW + int64_t(grow) * p.lddw + gcol) =
+                make_float4(g.x * f[i].x, g.y * f[i].y, g.z * f[i].z, g.w * f[i].w);
           }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmD, smem_u32(out_s), col0, row0);
-          bulk_commit_group();
-        }
       }
-      if (!ok) break;
     }
-    // on an early exit a prefetched W block may still be in flight: wait for it
-    for (int b = 0; b < 2; ++b)
-      if (wissued[b] > wuse[b] && !mbar_wait(wbar + 8 * b, wuse[b] & 1u, p.wait_ns)) ok = false;
-    if (lane == 0) bulk_wait_all();
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   }
 
@@ -379,13 +403,6 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   st = encode_tmap_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, uint64_t(N), uint64_t(M), uint64_t(lddy) * 2, kBox,
                       kBT, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != FP4_OK) return st;
-  CUtensorMap tmW, tmD;
-  st = encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, uint64_t(N), uint64_t(K), uint64_t(ldw) * 2, kBlk,
-                      kBlk, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (st != FP4_OK) return st;
-  st = encode_tmap_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dW, uint64_t(N), uint64_t(K), uint64_t(lddw) * 4, kBlk,
-                      kBlk, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != FP4_OK) return st;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -407,10 +424,11 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   p.inv_k = 1.0f / dge_k;
   p.expo = 1.0f / dge_k - 1.0f;
   p.clip = dge_clip;
+  p.pw0 = p.expo < 0.0f ? INFINITY : (p.expo == 0.0f ? 1.0f : 0.0f);
   p.status = status_word();
   p.wait_ns = kWaitLimitNs;
   const int64_t tiles = ((K + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
   const int grid = int(tiles < sms ? tiles : sms);
-  wgrad_dge_kernel<<<grid, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmG, tmW, tmD, p);
+  wgrad_dge_kernel<<<grid, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmG, p);
   return launch_status();
 }

@@ -9,10 +9,12 @@
 //     pattern per CTA in shared memory, merged into a global histogram; the
 //     last CTA to finish (atomic ticket) scans it for the exact k-th order
 //     statistic t.
-//  2. stage: one warp per row counts |A| > t, reserves space in a staging area
-//     with one atomic per row and writes (column, A - sign(A) t) in column
-//     order; optionally writes A_clamped.
-//  3. row_scan: exclusive scan of the per-row counts -> row_ptr (one CTA).
+//  2. rows_outlier: one row per warp (or a few warps for long rows), held in
+//     registers: counts |A| > t per 16-byte chunk, reserves the row's run in a
+//     staging area with one atomic and writes (column, A - sign(A) t) in column
+//     order; optionally writes A_clamped, and in the fused variant also the
+//     row's E2M1 codes and scale (the clamp applied), so A is read once here.
+//  3. row_scan: scan of the per-row counts -> row_ptr (one CTA, coalesced tiles).
 //  4. gather: copies every row's staged entries to its CSR position.
 #include <cmath>
 
@@ -62,21 +64,34 @@ __global__ void __launch_bounds__(kHistThreads, 1)
   const int cpr = K >> 3;  // 16-byte chunks per row
   const int64_t total = M * cpr;
   const bool dense = (lda == K);
-  for (int64_t g = int64_t(blockIdx.x) * kHistThreads + threadIdx.x; g < total;
-       g += int64_t(gridDim.x) * kHistThreads) {
-    const uint4* p;
-    if (dense) {
-      p = reinterpret_cast<const uint4*>(A) + g;
-    } else {
-      const int64_t r = g / cpr;
-      p = reinterpret_cast<const uint4*>(A + r * lda) + (g - r * cpr);
-    }
-    const uint4 v = __ldcs(p);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  const int64_t stride = int64_t(gridDim.x) * kHistThreads;
+  constexpr int kU = 4;  // loads in flight per thread
+  for (int64_t g0 = int64_t(blockIdx.x) * kHistThreads + threadIdx.x; g0 < total; g0 += stride * kU) {
+    uint4 v[kU];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      atomicAdd(&hist[w[i] & 0x7FFFu], 1u);
-      atomicAdd(&hist[(w[i] >> 16) & 0x7FFFu], 1u);
+    for (int u = 0; u < kU; ++u) {
+      const int64_t g = g0 + u * stride;
+      if (g < total) {
+        const uint4* p;
+        if (dense) {
+          p = reinterpret_cast<const uint4*>(A) + g;
+        } else {
+          const int64_t r = g / cpr;
+          p = reinterpret_cast<const uint4*>(A + r * lda) + (g - r * cpr);
+        }
+        v[u] = __ldcs(p);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (g0 + u * stride < total) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          atomicAdd(&hist[w[i] & 0x7FFFu], 1u);
+          atomicAdd(&hist[(w[i] >> 16) & 0x7FFFu], 1u);
+        }
+      }
     }
   }
   __syncthreads();
@@ -129,121 +144,208 @@ __global__ void __launch_bounds__(kHistThreads, 1)
   }
 }
 
-// One warp per row: count entries with magnitude pattern > t_bits, reserve a
-// contiguous run in the staging area, then write them in column order.
-__global__ void __launch_bounds__(256) stage_kernel(const uint16_t* __restrict__ A, int64_t M, int K, int64_t lda,
-                                                   Ctrl* ctrl,
-                                                   const float* __restrict__ t_ptr, int64_t cap,
-                                                   int32_t* __restrict__ row_cnt, int64_t* __restrict__ row_start,
-                                                   int32_t* __restrict__ scol, float* __restrict__ sval,
-                                                   uint16_t* __restrict__ A_c, int64_t ldac,
-                                                   uint32_t* __restrict__ status) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp_global = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+constexpr int kRowWarps = 8;
+
+// 8-bit mask of the elements of a 16-byte BF16 chunk whose magnitude pattern exceeds tb.
+__device__ __forceinline__ uint32_t outlier_mask8(const uint4 v, uint32_t tb) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m |= uint32_t((w[i] & 0x7FFFu) > tb) << (2 * i);
+    m |= uint32_t(((w[i] >> 16) & 0x7FFFu) > tb) << (2 * i + 1);
+  }
+  return m;
+}
+
+// Each row is handled by `wpr` warps; lane l of warp w holds the row's 16-byte
+// chunks ci = l + 32 (w + wpr c), c < CH, in registers.  Column order of the
+// entries is chunk-slot c first, then warp, then lane, which is what the
+// offsets below follow.
+template <int CH, bool CODES>
+__global__ void __launch_bounds__(256, 2) rows_outlier_kernel(
+    const uint16_t* __restrict__ A, int64_t M, int K, int64_t lda, Ctrl* ctrl, const float* __restrict__ t_ptr,
+    int64_t cap, int32_t* __restrict__ row_cnt, int64_t* __restrict__ row_start, int32_t* __restrict__ scol,
+    float* __restrict__ sval, uint16_t* __restrict__ A_c, int64_t ldac, uint8_t* __restrict__ codes, int64_t ldc,
+    float* __restrict__ scales, uint32_t* __restrict__ status, int wpr) {
+  __shared__ uint32_t red[kRowWarps];
+  __shared__ uint32_t tcnt[kRowWarps][CH];
+  __shared__ unsigned long long rbase[kRowWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows_per_cta = kRowWarps / wpr;
+  const int r_in_cta = warp / wpr, w_in_row = warp % wpr;
+  const int wrow0 = r_in_cta * wpr;  // first warp of this row
+  const int nchunk = K >> 3;
   const uint32_t tb = ctrl->t_bits;
+  const uint32_t tb2 = tb | (tb << 16);
   const float t = *t_ptr;
-  const int cpr = K >> 3;
-  for (int64_t row = warp_global; row < M; row += nwarps) {
-    const uint4* src = reinterpret_cast<const uint4*>(A + row * lda);
-    uint32_t cnt = 0;
-    for (int c = lane; c < cpr; c += 32) {
-      const uint4 v = __ldg(src + c);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t cw[4];
+  for (int64_t row0 = int64_t(blockIdx.x) * rows_per_cta; row0 < M; row0 += int64_t(gridDim.x) * rows_per_cta) {
+    const int64_t row = row0 + r_in_cta;
+    const bool active = row < M;
+    const uint4* src = reinterpret_cast<const uint4*>(A + (active ? row : 0) * lda);
+    uint4 v[CH];
+    uint32_t msk[CH], excl[CH];
+    uint32_t mx = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
-        const bool olo = (lo & 0x7FFFu) > tb, ohi = (hi & 0x7FFFu) > tb;
-        cnt += uint32_t(olo) + uint32_t(ohi);
-        cw[i] = (olo ? ((lo & 0x8000u) | tb) : lo) | ((ohi ? ((hi & 0x8000u) | tb) : hi) << 16);
+    for (int c = 0; c < CH; ++c) {
+      const int ci = lane + 32 * (w_in_row + wpr * c);
+      v[c] = (active && ci < nchunk) ? __ldcs(src + ci) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      if (CODES) mx = maxmag8(v[c], mx);
+      const uint32_t g = __vcmpgtu2(v[c].x & 0x7FFF7FFFu, tb2) | __vcmpgtu2(v[c].y & 0x7FFF7FFFu, tb2) |
+                         __vcmpgtu2(v[c].z & 0x7FFF7FFFu, tb2) | __vcmpgtu2(v[c].w & 0x7FFF7FFFu, tb2);
+      msk[c] = 0;
+      excl[c] = 0;
+      uint32_t tot = 0;
+      if (__any_sync(0xFFFFFFFFu, g != 0)) {  // rare: some lane has an outlier in this slot
+        msk[c] = g ? outlier_mask8(v[c], tb) : 0u;
+        const uint32_t n = __popc(msk[c]);
+        uint32_t incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        excl[c] = incl - n;
       }
-      if (A_c) reinterpret_cast<uint4*>(A_c + row * ldac)[c] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      if (lane == 0) tcnt[warp][c] = tot;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
-    unsigned long long base = 0;
-    if (cnt && lane == 0) base = atomicAdd(&ctrl->cursor, (unsigned long long)cnt);
-    base = __shfl_sync(0xFFFFFFFFu, base, 0);
-    if (lane == 0) {
-      row_cnt[row] = int32_t(cnt);
-      row_start[row] = int64_t(base);
+    if (CODES) {
+      const uint32_t mb = warp_max_bits(mx);
+      if (lane == 0) red[warp] = mb;
     }
-    if (cnt == 0) continue;
-    if (int64_t(base + cnt) > cap) {
-      if (lane == 0) atomicOr(status, FP4_FLAG_CAPACITY);
-      continue;
-    }
-    // second pass (row is L1/L2 resident): write entries in column order
-    unsigned long long run = base;
-    for (int c0 = 0; c0 < cpr; c0 += 32) {
-      const int c = c0 + lane;
-      uint32_t mask = 0;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (c < cpr) {
-        v = __ldg(src + c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          mask |= uint32_t((w[i] & 0x7FFFu) > tb) << (2 * i);
-          mask |= uint32_t(((w[i] >> 16) & 0x7FFFu) > tb) << (2 * i + 1);
+    __syncthreads();
+    if (w_in_row == 0 && lane == 0) {
+      unsigned long long total = 0;
+      for (int c = 0; c < CH; ++c)
+        for (int w = 0; w < wpr; ++w) total += tcnt[wrow0 + w][c];
+      unsigned long long base = 0;
+      if (active) {
+        if (total) base = atomicAdd(&ctrl->cursor, total);
+        row_cnt[row] = int32_t(total);
+        row_start[row] = int64_t(base);
+        if (int64_t(base + total) > cap) {
+          atomicOr(status, FP4_FLAG_CAPACITY);
+          base = ~0ull;
         }
       }
-      const uint32_t n = __popc(mask);
-      uint32_t incl = n;
+      rbase[r_in_cta] = base;
+    }
+    __syncthreads();
+    const unsigned long long rb = rbase[r_in_cta];
+    if (active && rb != ~0ull) {
+      unsigned long long off = rb;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      if (n) {
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        unsigned long long pos = run + (incl - n);
-        for (int e = 0; e < 8; ++e) {
-          if (mask & (1u << e)) {
-            const float x = bf16_bits_to_float((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
-            scol[pos] = c * 8 + e;
+      for (int c = 0; c < CH; ++c) {
+        unsigned long long pos = off + excl[c];
+        for (int w = 0; w < w_in_row; ++w) pos += tcnt[wrow0 + w][c];
+        uint32_t m = msk[c];
+        if (m) {
+          const int ci = lane + 32 * (w_in_row + wpr * c);
+          const uint4 vc = v[c];
+          while (m) {  // set bits in ascending column order
+            const int e = __ffs(m) - 1;
+            m &= m - 1;
+            const uint32_t word = e < 4 ? (e < 2 ? vc.x : vc.y) : (e < 6 ? vc.z : vc.w);
+            const float x = bf16_bits_to_float((word >> (16 * (e & 1))) & 0xFFFFu);
+            scol[pos] = ci * 8 + e;
             sval[pos] = __fsub_rn(x, copysignf(t, x));
             ++pos;
           }
         }
+        for (int w = 0; w < wpr; ++w) off += tcnt[wrow0 + w][c];
       }
-      run += total;
     }
+    if (active && A_c) {
+      uint4* dst = reinterpret_cast<uint4*>(A_c + row * ldac);
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int ci = lane + 32 * (w_in_row + wpr * c);
+        if (ci < nchunk) {
+          const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+          uint32_t cw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
+            cw[i] = (((lo & 0x7FFFu) > tb) ? ((lo & 0x8000u) | tb) : lo) |
+                    ((((hi & 0x7FFFu) > tb) ? ((hi & 0x8000u) | tb) : hi) << 16);
+          }
+          dst[ci] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        }
+      }
+    }
+    if (CODES) {
+      uint32_t amax_bits = 0;
+      for (int i = 0; i < wpr; ++i) amax_bits = max(amax_bits, red[wrow0 + i]);
+      // max over min(|x|, t) = min(max |x|, t)
+      const float sc = scale_from_absmax(bf16_bits_to_float(min(amax_bits, tb)));
+      if (active) {
+        if (w_in_row == 0 && lane == 0) scales[row] = sc;
+        uint32_t* dst = reinterpret_cast<uint32_t*>(codes + row * ldc);
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int ci = lane + 32 * (w_in_row + wpr * c);
+          if (ci < nchunk) dst[ci] = msk[c] ? quantize8<true>(v[c], sc, tb2) : quantize8<false>(v[c], sc, tb2);
+        }
+      }
+    }
+    __syncthreads();  // tcnt / rbase / red are reused by the next row group
   }
 }
 
-// row_ptr[0] = 0, row_ptr[i+1] = sum of counts of rows <= i; checks the total
-// against the histogram's count.
+// row_ptr[0] = 0, row_ptr[i+1] = sum of counts of rows <= i, in tiles of 4096
+// rows (coalesced loads); checks the total against the histogram's count.
 __global__ void __launch_bounds__(1024) row_scan_kernel(const int32_t* __restrict__ row_cnt, int64_t M,
                                                        int32_t* __restrict__ row_ptr, int64_t* __restrict__ nnz_out,
                                                        const Ctrl* __restrict__ ctrl, int64_t cap,
                                                        uint32_t* __restrict__ status) {
-  __shared__ long long part[1024];
-  const int64_t per = (M + 1023) / 1024;
-  const int64_t r0 = int64_t(threadIdx.x) * per;
-  const int64_t r1 = r0 + per < M ? r0 + per : M;
-  long long s = 0;
-  for (int64_t r = r0; r < r1; ++r) s += row_cnt[r];
-  part[threadIdx.x] = s;
-  __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {
-    const long long add = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+  __shared__ long long wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  long long carry = 0;
+  if (tid == 0) row_ptr[0] = 0;
+  for (int64_t base = 0; base < M; base += 4096) {
+    const int64_t idx = base + 4 * tid;
+    int c[4];
+    if (idx + 3 < M) {
+      const int4 q = *reinterpret_cast<const int4*>(row_cnt + idx);
+      c[0] = q.x; c[1] = q.y; c[2] = q.z; c[3] = q.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] = (idx + i < M) ? row_cnt[idx + i] : 0;
+    }
+    const long long s0 = c[0], s1 = s0 + c[1], s2 = s1 + c[2], s3 = s2 + c[3];
+    long long x = s3;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
     __syncthreads();
-    part[threadIdx.x] += add;
+    if (warp == 0) {
+      long long w = wsum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+        if (lane >= o) w += y;
+      }
+      wsum[lane] = w;
+    }
+    __syncthreads();
+    const long long excl = carry + (warp ? wsum[warp - 1] : 0) + x - s3;
+    const long long incl4[4] = {s0, s1, s2, s3};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (idx + i < M) row_ptr[idx + i + 1] = int32_t(excl + incl4[i]);
+    carry += wsum[31];
     __syncthreads();
   }
-  long long run = part[threadIdx.x] - s;
-  if (threadIdx.x == 0) row_ptr[0] = 0;
-  for (int64_t r = r0; r < r1; ++r) {
-    run += row_cnt[r];
-    row_ptr[r + 1] = int32_t(run);
-  }
-  if (threadIdx.x == 1023) {
-    const long long total = part[1023];
-    if (nnz_out) *nnz_out = total;
-    if (uint64_t(total) != ctrl->nnz_expect && total <= cap) atomicOr(status, FP4_FLAG_INTERNAL);
+  if (tid == 0) {
+    if (nnz_out) *nnz_out = carry;
+    if (uint64_t(carry) != ctrl->nnz_expect && carry <= cap) atomicOr(status, FP4_FLAG_INTERNAL);
   }
 }
 
@@ -284,28 +386,36 @@ FP4_API size_t outlier_clamp_quantile_workspace(int64_t M, int64_t K, int64_t nn
   return fp4::ws_layout(M, nnz_capacity).total;
 }
 
-FP4_API fp4_status outlier_clamp_quantile(const void* A, int64_t M, int64_t K, int64_t lda, double q, float* t_out,
-                                          int32_t* row_ptr, int32_t* col_idx, float* vals, int64_t nnz_capacity,
-                                          int64_t* nnz_out, void* A_clamped, int64_t ldac, void* workspace,
-                                          size_t ws_bytes, fp4_stream_t stream) {
-  using namespace fp4;
-  if (!A || !t_out || !row_ptr || !workspace) return FP4_ERR_INVALID_ARG;
-  if (!(q > 0.0) || !(q <= 1.0)) return FP4_ERR_INVALID_ARG;
-  if (M <= 0 || K <= 0 || K % 8 != 0 || lda < K || K > (1 << 30) || M >= (int64_t(1) << 31) ||
-      M * K >= (int64_t(1) << 32))
-    return FP4_ERR_SHAPE;
-  if (A_clamped && ldac < K) return FP4_ERR_SHAPE;
-  if (lda % 8 != 0 || !aligned16(A) || !aligned16(workspace) || (A_clamped && (!aligned16(A_clamped) || ldac % 8)))
-    return FP4_ERR_ALIGNMENT;
-  const int64_t need = outlier_max_nnz(M, K, q);
-  if (nnz_capacity < need || nnz_capacity >= (int64_t(1) << 31)) return FP4_ERR_CAPACITY;
-  if (nnz_capacity > 0 && (!col_idx || !vals)) return FP4_ERR_INVALID_ARG;
-  const WsLayout L = ws_layout(M, nnz_capacity);
-  if (ws_bytes < L.total) return FP4_ERR_WORKSPACE;
+namespace fp4 {
+namespace {
+
+template <bool CODES>
+void launch_rows_outlier(int ch, int wpr, unsigned blocks, cudaStream_t s, const uint16_t* A, int64_t M, int K,
+                         int64_t lda, Ctrl* ctrl, const float* t, int64_t cap, int32_t* row_cnt, int64_t* row_start,
+                         int32_t* scol, float* sval, uint16_t* A_c, int64_t ldac, uint8_t* codes, int64_t ldc,
+                         float* scales, uint32_t* status) {
+#define FP4_ROWS_OUTLIER(CHV)                                                                                     \
+  rows_outlier_kernel<CHV, CODES><<<blocks, 256, 0, s>>>(A, M, K, lda, ctrl, t, cap, row_cnt, row_start, scol, \
+                                                         sval, A_c, ldac, codes, ldc, scales, status, wpr)
+  switch (ch) {
+    case 1: FP4_ROWS_OUTLIER(1); break;
+    case 2: FP4_ROWS_OUTLIER(2); break;
+    case 4: FP4_ROWS_OUTLIER(4); break;
+    default: FP4_ROWS_OUTLIER(8); break;
+  }
+#undef FP4_ROWS_OUTLIER
+}
+
+// Histogram + threshold, fused row pass (CSR staging, optional A_clamped, optional
+// codes / scales), row scan and gather.  Arguments are validated by the callers.
+fp4_status run_outlier_pipeline(const void* A, int64_t M, int64_t K, int64_t lda, double q, float* t_out,
+                                int32_t* row_ptr, int32_t* col_idx, float* vals, int64_t nnz_capacity,
+                                int64_t* nnz_out, void* A_clamped, int64_t ldac, uint8_t* codes, int64_t ldc,
+                                float* scales, void* workspace, cudaStream_t s) {
   int sms = 0;
   fp4_status st = check_device(&sms);
   if (st != FP4_OK) return st;
-  auto s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(M, nnz_capacity);
   auto* ws = static_cast<uint8_t*>(workspace);
   auto* ghist = reinterpret_cast<uint32_t*>(ws + L.hist);
   auto* ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
@@ -314,9 +424,10 @@ FP4_API fp4_status outlier_clamp_quantile(const void* A, int64_t M, int64_t K, i
   auto* scol = reinterpret_cast<int32_t*>(ws + L.scol);
   auto* sval = reinterpret_cast<float*>(ws + L.sval);
   uint32_t* status = status_word();
+  const auto* a = static_cast<const uint16_t*>(A);
 
   const int64_t n = M * K;
-  const int64_t k_rank = n - need;
+  const int64_t k_rank = n - outlier_max_nnz(M, K, q);
   if (cudaMemsetAsync(ws, 0, L.cnt, s) != cudaSuccess) return FP4_ERR_CUDA;  // histogram + control block
 
   static bool attr_set[64] = {false};
@@ -333,22 +444,85 @@ FP4_API fp4_status outlier_clamp_quantile(const void* A, int64_t M, int64_t K, i
   int64_t hblocks = (chunks + kHistThreads * 4 - 1) / (kHistThreads * 4);
   if (hblocks > sms) hblocks = sms;
   if (hblocks < 1) hblocks = 1;
-  histogram_select_kernel<<<unsigned(hblocks), kHistThreads, hist_smem, s>>>(
-      static_cast<const uint16_t*>(A), M, int(K), lda, k_rank, ghist, ctrl, t_out);
+  histogram_select_kernel<<<unsigned(hblocks), kHistThreads, hist_smem, s>>>(a, M, int(K), lda, k_rank, ghist, ctrl,
+                                                                             t_out);
   if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
 
-  int64_t sblocks = (M + 7) / 8;
-  if (sblocks > int64_t(sms) * 8) sblocks = int64_t(sms) * 8;
-  stage_kernel<<<unsigned(sblocks), 256, 0, s>>>(static_cast<const uint16_t*>(A), M, int(K), lda, ctrl, t_out,
-                                                  nnz_capacity, row_cnt, row_start, scol, sval,
-                                                  static_cast<uint16_t*>(A_clamped), ldac, status);
+  // fused row pass: rows of <= 8 chunks per lane, 1..8 warps per row (K <= 32768)
+  const int nchunk = int(K / 8);
+  int wpr = 1;
+  while (wpr < 8 && nchunk > 32 * 8 * wpr) wpr *= 2;
+  const int per_lane = (nchunk + 32 * wpr - 1) / (32 * wpr);
+  const int ch = per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : 8;
+  const int rows_per_cta = kRowWarps / wpr;
+  int64_t rblocks = (M + rows_per_cta - 1) / rows_per_cta;
+  if (rblocks > int64_t(sms) * 8) rblocks = int64_t(sms) * 8;
+  if (codes)
+    launch_rows_outlier<true>(ch, wpr, unsigned(rblocks), s, a, M, int(K), lda, ctrl, t_out, nnz_capacity, row_cnt,
+                              row_start, scol, sval, static_cast<uint16_t*>(A_clamped), ldac, codes, ldc, scales,
+                              status);
+  else
+    launch_rows_outlier<false>(ch, wpr, unsigned(rblocks), s, a, M, int(K), lda, ctrl, t_out, nnz_capacity, row_cnt,
+                               row_start, scol, sval, static_cast<uint16_t*>(A_clamped), ldac, nullptr, 0, nullptr,
+                               status);
   if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
   row_scan_kernel<<<1, 1024, 0, s>>>(row_cnt, M, row_ptr, nnz_out, ctrl, nnz_capacity, status);
   if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
   if (nnz_capacity > 0) {
-    gather_kernel<<<unsigned(sblocks), 256, 0, s>>>(row_cnt, row_start, row_ptr, M, scol, sval, col_idx, vals,
+    int64_t gblocks = (M + 7) / 8;
+    if (gblocks > int64_t(sms) * 8) gblocks = int64_t(sms) * 8;
+    gather_kernel<<<unsigned(gblocks), 256, 0, s>>>(row_cnt, row_start, row_ptr, M, scol, sval, col_idx, vals,
                                                     nnz_capacity);
     if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
   }
   return FP4_OK;
+}
+
+fp4_status validate_outlier_args(const void* A, int64_t M, int64_t K, int64_t lda, double q, const float* t_out,
+                                 const int32_t* row_ptr, const int32_t* col_idx, const float* vals,
+                                 int64_t nnz_capacity, const void* workspace, size_t ws_bytes) {
+  if (!A || !t_out || !row_ptr || !workspace) return FP4_ERR_INVALID_ARG;
+  if (!(q > 0.0) || !(q <= 1.0)) return FP4_ERR_INVALID_ARG;
+  if (M <= 0 || K <= 0 || K % 8 != 0 || lda < K || K > 16384 || M >= (int64_t(1) << 31) ||
+      M * K >= (int64_t(1) << 32))
+    return FP4_ERR_SHAPE;
+  if (lda % 8 != 0 || !aligned16(A) || !aligned16(workspace)) return FP4_ERR_ALIGNMENT;
+  const int64_t need = outlier_max_nnz(M, K, q);
+  if (nnz_capacity < need || nnz_capacity >= (int64_t(1) << 31)) return FP4_ERR_CAPACITY;
+  if (nnz_capacity > 0 && (!col_idx || !vals)) return FP4_ERR_INVALID_ARG;
+  if (ws_bytes < ws_layout(M, nnz_capacity).total) return FP4_ERR_WORKSPACE;
+  return FP4_OK;
+}
+
+}  // namespace
+}  // namespace fp4
+
+FP4_API fp4_status outlier_clamp_quantile(const void* A, int64_t M, int64_t K, int64_t lda, double q, float* t_out,
+                                          int32_t* row_ptr, int32_t* col_idx, float* vals, int64_t nnz_capacity,
+                                          int64_t* nnz_out, void* A_clamped, int64_t ldac, void* workspace,
+                                          size_t ws_bytes, fp4_stream_t stream) {
+  using namespace fp4;
+  fp4_status st = validate_outlier_args(A, M, K, lda, q, t_out, row_ptr, col_idx, vals, nnz_capacity, workspace,
+                                        ws_bytes);
+  if (st != FP4_OK) return st;
+  if (A_clamped && ldac < K) return FP4_ERR_SHAPE;
+  if (A_clamped && (!aligned16(A_clamped) || ldac % 8)) return FP4_ERR_ALIGNMENT;
+  return run_outlier_pipeline(A, M, K, lda, q, t_out, row_ptr, col_idx, vals, nnz_capacity, nnz_out, A_clamped, ldac,
+                              nullptr, 0, nullptr, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+FP4_API fp4_status fp4_quantize_rows_outliers(const void* A, int64_t M, int64_t K, int64_t lda, double q,
+                                              uint8_t* codes, int64_t ldc_bytes, float* scales, float* t_out,
+                                              int32_t* row_ptr, int32_t* col_idx, float* vals, int64_t nnz_capacity,
+                                              int64_t* nnz_out, void* workspace, size_t ws_bytes,
+                                              fp4_stream_t stream) {
+  using namespace fp4;
+  fp4_status st = validate_outlier_args(A, M, K, lda, q, t_out, row_ptr, col_idx, vals, nnz_capacity, workspace,
+                                        ws_bytes);
+  if (st != FP4_OK) return st;
+  if (!codes || !scales) return FP4_ERR_INVALID_ARG;
+  if (K % 32 != 0 || ldc_bytes < K / 2) return FP4_ERR_SHAPE;
+  if (ldc_bytes % 16 != 0 || !aligned16(codes) || !aligned16(scales)) return FP4_ERR_ALIGNMENT;
+  return run_outlier_pipeline(A, M, K, lda, q, t_out, row_ptr, col_idx, vals, nnz_capacity, nnz_out, nullptr, 0, codes,
+                              ldc_bytes, scales, workspace, reinterpret_cast<cudaStream_t>(stream));
 }

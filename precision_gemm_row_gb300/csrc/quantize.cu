@@ -14,79 +14,56 @@ namespace {
 
 constexpr int kRowThreads = 256;  // 8 warps
 
-// Scales 8 BF16 values by s after clamping |x| to t, and packs their 8 E2M1
-// codes into one 32-bit word (element 0 in the lowest nibble).
-template <bool CLAMP>
-__device__ __forceinline__ uint32_t quantize8(const uint4 v, float s, float t) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float lo = bf16_bits_to_float(w[i] & 0xFFFFu);
-    float hi = bf16_bits_to_float(w[i] >> 16);
-    if (CLAMP) {
-      if (fabsf(lo) > t) lo = copysignf(t, lo);
-      if (fabsf(hi) > t) hi = copysignf(t, hi);
-    }
-    out |= e2m1x2_encode(__fmul_rn(lo, s), __fmul_rn(hi, s)) << (8 * i);
-  }
-  return out;
-}
-
-__device__ __forceinline__ float absmax8(const uint4 v, float t) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float m = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    m = fmaxf(m, fminf(fabsf(bf16_bits_to_float(w[i] & 0xFFFFu)), t));
-    m = fmaxf(m, fminf(fabsf(bf16_bits_to_float(w[i] >> 16)), t));
-  }
-  return m;
-}
-
 // Each row is handled by `wpr` warps; each lane keeps up to CH 16-byte chunks
 // of the row in registers, so A is read from HBM exactly once.
 template <int CH, bool CLAMP>
-__global__ void __launch_bounds__(kRowThreads) quantize_rows_kernel(const uint16_t* __restrict__ A, int64_t M,
-                                                                    int K, int64_t lda,
-                                                                    const float* __restrict__ clamp_t,
-                                                                    uint8_t* __restrict__ codes, int64_t ldc,
-                                                                    float* __restrict__ scales, int wpr) {
-  __shared__ float red[kRowThreads / 32];
+__global__ void __launch_bounds__(kRowThreads, 2) quantize_rows_kernel(const uint16_t* __restrict__ A, int64_t M,
+                                                                       int K, int64_t lda,
+                                                                       const float* __restrict__ clamp_t,
+                                                                       uint8_t* __restrict__ codes, int64_t ldc,
+                                                                       float* __restrict__ scales, int wpr) {
+  __shared__ uint32_t red[kRowThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows_per_cta = (kRowThreads / 32) / wpr;
   const int r_in_cta = warp / wpr, w_in_row = warp % wpr;
   const int nchunk = K >> 3;
-  const float t = CLAMP ? __ldg(clamp_t) : INFINITY;
+  // A BF16 threshold (the usual case: the quantile threshold is one) is applied
+  // exactly on the bit patterns; any other fp32 threshold in fp32.
+  const float tf = CLAMP ? __ldg(clamp_t) : INFINITY;
+  const bool t_bits_exact = (__float_as_uint(tf) & 0xFFFFu) == 0u;
+  const uint32_t tb = CLAMP ? (__float_as_uint(tf) >> 16) & 0x7FFFu : 0x7FFFu;
+  const uint32_t tb2 = tb | (tb << 16);
 
   for (int64_t row0 = int64_t(blockIdx.x) * rows_per_cta; row0 < M; row0 += int64_t(gridDim.x) * rows_per_cta) {
     const int64_t row = row0 + r_in_cta;
     const bool active = row < M;
     const uint4* src = reinterpret_cast<const uint4*>(A + (active ? row : 0) * lda);
     uint4 v[CH];
-    float amax = 0.0f;
+    uint32_t mx = 0;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int ci = lane + 32 * (w_in_row + wpr * c);
       v[c] = (active && ci < nchunk) ? __ldcs(src + ci) : make_uint4(0u, 0u, 0u, 0u);
-      amax = fmaxf(amax, absmax8(v[c], t));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    for (int c = 0; c < CH; ++c) mx = maxmag8(v[c], mx);
+    uint32_t amax_bits = warp_max_bits(mx);
     if (wpr > 1) {
-      if (lane == 0) red[warp] = amax;
+      if (lane == 0) red[warp] = amax_bits;
       __syncthreads();
-      for (int i = 0; i < wpr; ++i) amax = fmaxf(amax, red[r_in_cta * wpr + i]);
+      for (int i = 0; i < wpr; ++i) amax_bits = max(amax_bits, red[r_in_cta * wpr + i]);
       __syncthreads();
     }
-    const float s = scale_from_absmax(amax);
+    // max over min(|x|, t) = min(max |x|, t)
+    const float s = scale_from_absmax(CLAMP ? fminf(bf16_bits_to_float(amax_bits), tf) : bf16_bits_to_float(amax_bits));
     if (active) {
       if (w_in_row == 0 && lane == 0) scales[row] = s;
       uint32_t* dst = reinterpret_cast<uint32_t*>(codes + row * ldc);
 #pragma unroll
       for (int c = 0; c < CH; ++c) {
         const int ci = lane + 32 * (w_in_row + wpr * c);
-        if (ci < nchunk) dst[ci] = quantize8<CLAMP>(v[c], s, t);
+        if (ci < nchunk)
+          dst[ci] = (!CLAMP || t_bits_exact) ? quantize8<CLAMP>(v[c], s, tb2) : quantize8_clamp_f32(v[c], s, tf);
       }
     }
   }
@@ -107,13 +84,23 @@ __global__ void __launch_bounds__(256) col_absmax_kernel(const uint16_t* __restr
 #pragma unroll
   for (int i = 0; i < 8; ++i) m[i] = 0.0f;
   if (col_ok) {
-    for (int k = k0 + grp; k < k1; k += 8) {
-      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(W + int64_t(k) * ldw) + cchunk);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    constexpr int kU = 4;  // rows in flight per thread
+    for (int kb = k0 + grp; kb < k1; kb += 8 * kU) {
+      uint4 v[kU];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        m[2 * i] = fmaxf(m[2 * i], fabsf(bf16_bits_to_float(w[i] & 0xFFFFu)));
-        m[2 * i + 1] = fmaxf(m[2 * i + 1], fabsf(bf16_bits_to_float(w[i] >> 16)));
+      for (int u = 0; u < kU; ++u) {
+        const int k = kb + 8 * u;
+        v[u] = k < k1 ? __ldcs(reinterpret_cast<const uint4*>(W + int64_t(k) * ldw) + cchunk)
+                      : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          m[2 * i] = fmaxf(m[2 * i], fabsf(bf16_bits_to_float(w[i] & 0xFFFFu)));
+          m[2 * i + 1] = fmaxf(m[2 * i + 1], fabsf(bf16_bits_to_float(w[i] >> 16)));
+        }
       }
     }
   }
@@ -128,61 +115,92 @@ __global__ void __launch_bounds__(256) col_absmax_kernel(const uint16_t* __restr
   if (col < N) atomicMax(colmax + col, __float_as_uint(r));
 }
 
-// Quantizes a 64 (K) x 64 (N) tile of W with the column scales and writes it
-// transposed: codes_t[j][k/2], 32 bytes per column per tile.
-__global__ void __launch_bounds__(256) quantize_cols_kernel(const uint16_t* __restrict__ W, int K, int N,
-                                                           int64_t ldw, const uint32_t* __restrict__ colmax,
-                                                           uint8_t* __restrict__ codes_t, int64_t ldc,
-                                                           float* __restrict__ scales) {
-  __shared__ float s_col[64];
-  __shared__ uint8_t tile[64][64 + 16];  // [column][k] one code per byte
+// Quantizes a 256 (K) x 32 (N) tile of W with the column scales and writes it
+// transposed (codes_t[j][k/2], 128 bytes per column per tile).  The tile comes
+// in by one TMA load (row pitch 64 bytes: a warp reading one k for 32 columns
+// touches 64 contiguous bytes) and leaves by one TMA store from a 128-byte
+// swizzled staging tile (one 128-byte row per column).
+constexpr int kColTileK = 256, kColTileN = 32;
+
+__global__ void __launch_bounds__(256) quantize_cols_tma_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                               const __grid_constant__ CUtensorMap tmC, int K, int N,
+                                                               const uint32_t* __restrict__ colmax,
+                                                               float* __restrict__ scales,
+                                                               uint32_t* __restrict__ status) {
+  __shared__ __align__(1024) uint8_t w_s[kColTileK * kColTileN * 2];
+  __shared__ __align__(1024) uint8_t c_s[kColTileN * 128];
+  __shared__ float s_col[kColTileN];
+  __shared__ __align__(8) uint64_t bar;
   const int tid = threadIdx.x;
-  const int j0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
-  if (tid < 64) {
+  const int j0 = blockIdx.x * kColTileN, k0 = blockIdx.y * kColTileK;
+  const uint32_t b = smem_u32(&bar);
+  if (tid == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(b, kColTileK * kColTileN * 2);
+    tma_load_2d(smem_u32(w_s), &tmW, b, j0, k0);
+  }
+  if (tid < kColTileN) {
     const int j = j0 + tid;
-    float s = 1.0f;
+    float sc = 1.0f;
     if (j < N) {
-      s = scale_from_absmax(__uint_as_float(colmax[j]));
-      if (blockIdx.y == 0) scales[j] = s;
+      sc = scale_from_absmax(__uint_as_float(colmax[j]));
+      if (blockIdx.y == 0) scales[j] = sc;
     }
-    s_col[tid] = s;
+    s_col[tid] = sc;
   }
   __syncthreads();
+  const bool ok = mbar_wait(b, 0, kWaitLimitNs);
+  if (!ok && tid == 0) atomicOr(status, FP4_FLAG_TIMEOUT);
+  const int j = tid & 31, kq = tid >> 5;  // column, group of 32 rows (one warp per group)
+  const float sc = s_col[j];
+  const uint16_t* col = reinterpret_cast<const uint16_t*>(w_s) + j;
+  uint32_t out[4];
 #pragma unroll
-  for (int it = 0; it < 2; ++it) {
-    const int r = (tid >> 3) + 32 * it;  // k within tile
-    const int cc = tid & 7;              // 8-column chunk within tile
-    const int k = k0 + r, j = j0 + cc * 8;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (k < K && j < N) {
-      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(W + int64_t(k) * ldw + j));
-      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-    }
+  for (int q = 0; q < 4; ++q) {
+    uint32_t word = 0;
 #pragma unroll
-    for (int i = 0; i < 8; i += 2) {
-      const float x0 = bf16_bits_to_float(w[i >> 1] & 0xFFFFu);
-      const float x1 = bf16_bits_to_float(w[i >> 1] >> 16);
-      const uint32_t c2 = e2m1x2_encode(__fmul_rn(x0, s_col[cc * 8 + i]), __fmul_rn(x1, s_col[cc * 8 + i + 1]));
-      tile[cc * 8 + i][r] = static_cast<uint8_t>(c2 & 0xFu);
-      tile[cc * 8 + i + 1][r] = static_cast<uint8_t>(c2 >> 4);
+    for (int bb = 0; bb < 4; ++bb) {
+      const int k = 32 * kq + 8 * q + 2 * bb;
+      const float x0 = bf16_bits_to_float(col[k * kColTileN]);
+      const float x1 = bf16_bits_to_float(col[(k + 1) * kColTileN]);
+      word |= e2m1x2_encode(__fmul_rn(x0, sc), __fmul_rn(x1, sc)) << (8 * bb);
     }
+    out[q] = word;
   }
+  *reinterpret_cast<uint4*>(c_s + j * 128 + ((kq ^ (j & 7)) << 4)) = make_uint4(out[0], out[1], out[2], out[3]);
+  fence_proxy_async_smem();
   __syncthreads();
-  if (tid < 128) {
-    const int c = tid >> 1, h = tid & 1;  // column, which 32-k half
-    const int j = j0 + c, k = k0 + 32 * h;
-    if (j < N && k < K) {
-      uint32_t out[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t wv = 0;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) wv |= uint32_t(tile[c][32 * h + 8 * q + b]) << (4 * b);
-        out[q] = wv;
-      }
-      *reinterpret_cast<uint4*>(codes_t + int64_t(j) * ldc + (k >> 1)) = make_uint4(out[0], out[1], out[2], out[3]);
-    }
+  if (tid == 0 && ok) {
+    tma_store_2d(&tmC, smem_u32(c_s), k0 / 2, j0);
+    bulk_commit_group();
+    bulk_wait_all();
   }
+}
+
+// Column maxima (atomic max into colmax) then the TMA tile quantizer.
+fp4_status launch_cols(const uint16_t* w, int64_t K, int64_t N, int64_t ldw, uint8_t* codes_t, int64_t ldc,
+                       float* scales, uint32_t* colmax, int sms, cudaStream_t s) {
+  CUtensorMap tmW, tmC;
+  fp4_status st = encode_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, uint64_t(N), uint64_t(K),
+                                 uint64_t(ldw) * 2, kColTileN, kColTileK, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != FP4_OK) return st;
+  st = encode_tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes_t, uint64_t(K / 2), uint64_t(N), uint64_t(ldc), 128,
+                      kColTileN, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st != FP4_OK) return st;
+  if (cudaMemsetAsync(colmax, 0, size_t(N) * 4, s) != cudaSuccess) return FP4_ERR_CUDA;
+  const int col_blocks = int((N + 255) / 256);
+  int splits = (4 * sms + col_blocks - 1) / col_blocks;
+  const int max_splits = int((K + 63) / 64);
+  if (splits > max_splits) splits = max_splits;
+  if (splits < 1) splits = 1;
+  const int rows_per_split = int((K + splits - 1) / splits);
+  splits = int((K + rows_per_split - 1) / rows_per_split);
+  col_absmax_kernel<<<dim3(col_blocks, splits), 256, 0, s>>>(w, int(K), int(N), ldw, rows_per_split, colmax);
+  if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
+  quantize_cols_tma_kernel<<<dim3(unsigned((N + kColTileN - 1) / kColTileN), unsigned((K + kColTileK - 1) / kColTileK)),
+                             256, 0, s>>>(tmW, tmC, int(K), int(N), colmax, scales, status_word());
+  return launch_status();
 }
 
 template <int CH>
@@ -209,7 +227,7 @@ FP4_API fp4_status fp4_quantize_rows(const void* A, int64_t M, int64_t K, int64_
   using namespace fp4;
   if (M < 0 || K <= 0) return FP4_ERR_SHAPE;
   if (M > 0 && (!A || !codes || !scales)) return FP4_ERR_INVALID_ARG;
-  if (K % 32 != 0 || K > (1 << 30) || lda < K || ldc_bytes < K / 2) return FP4_ERR_SHAPE;
+  if (K % 32 != 0 || K > 16384 || lda < K || ldc_bytes < K / 2) return FP4_ERR_SHAPE;
   if (lda % 8 != 0 || ldc_bytes % 16 != 0 || !aligned16(A) || !aligned16(codes) || !aligned16(scales) ||
       (clamp_t && (reinterpret_cast<uintptr_t>(clamp_t) & 3u)))
     return FP4_ERR_ALIGNMENT;
@@ -218,9 +236,9 @@ FP4_API fp4_status fp4_quantize_rows(const void* A, int64_t M, int64_t K, int64_
   if (st != FP4_OK) return st;
   if (M == 0) return FP4_OK;
   const int nchunk = int(K / 8);
-  // warps per row and chunks per lane: keep <= 16 chunks (64 registers) per lane
+  // warps per row and chunks per lane: keep <= 8 chunks (32 registers) per lane
   int wpr = 1;
-  while (wpr < 8 && nchunk > 32 * 16 * wpr) wpr *= 2;
+  while (wpr < 8 && nchunk > 32 * 8 * wpr) wpr *= 2;
   const int per_lane = (nchunk + 32 * wpr - 1) / (32 * wpr);
   auto s = reinterpret_cast<cudaStream_t>(stream);
   const auto* a = static_cast<const uint16_t*>(A);
@@ -228,8 +246,6 @@ FP4_API fp4_status fp4_quantize_rows(const void* A, int64_t M, int64_t K, int64_
   else if (per_lane <= 2) launch_rows<2>(a, M, int(K), lda, clamp_t, codes, ldc_bytes, scales, wpr, sms, s);
   else if (per_lane <= 4) launch_rows<4>(a, M, int(K), lda, clamp_t, codes, ldc_bytes, scales, wpr, sms, s);
   else if (per_lane <= 8) launch_rows<8>(a, M, int(K), lda, clamp_t, codes, ldc_bytes, scales, wpr, sms, s);
-  else if (per_lane <= 12) launch_rows<12>(a, M, int(K), lda, clamp_t, codes, ldc_bytes, scales, wpr, sms, s);
-  else if (per_lane <= 16) launch_rows<16>(a, M, int(K), lda, clamp_t, codes, ldc_bytes, scales, wpr, sms, s);
   else return FP4_ERR_SHAPE;
   return launch_status();
 }
@@ -254,22 +270,8 @@ FP4_API fp4_status fp4_quantize_cols(const void* W, int64_t K, int64_t N, int64_
   int sms = 0;
   fp4_status st = check_device(&sms);
   if (st != FP4_OK) return st;
-  auto s = reinterpret_cast<cudaStream_t>(stream);
-  auto* colmax = static_cast<uint32_t*>(workspace);
-  if (cudaMemsetAsync(colmax, 0, size_t(N) * 4, s) != cudaSuccess) return FP4_ERR_CUDA;
-  const int col_blocks = int((N + 255) / 256);
-  int splits = (4 * sms + col_blocks - 1) / col_blocks;
-  const int max_splits = int((K + 63) / 64);
-  if (splits > max_splits) splits = max_splits;
-  if (splits < 1) splits = 1;
-  const int rows_per_split = int((K + splits - 1) / splits);
-  splits = int((K + rows_per_split - 1) / rows_per_split);
-  const auto* w = static_cast<const uint16_t*>(W);
-  col_absmax_kernel<<<dim3(col_blocks, splits), 256, 0, s>>>(w, int(K), int(N), ldw, rows_per_split, colmax);
-  if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
-  quantize_cols_kernel<<<dim3(unsigned((N + 63) / 64), unsigned((K + 63) / 64)), 256, 0, s>>>(
-      w, int(K), int(N), ldw, colmax, codes_t, ldc_bytes, scales);
-  return launch_status();
+  return launch_cols(static_cast<const uint16_t*>(W), K, N, ldw, codes_t, ldc_bytes, scales,
+                     static_cast<uint32_t*>(workspace), sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -322,20 +324,7 @@ FP4_API fp4_status fp4_quantize_cols_noalloc(const void* W, int64_t K, int64_t N
   uint32_t* colmax = nullptr;
   st = scratch_address(&colmax);
   if (st != FP4_OK) return st;
-  auto s = reinterpret_cast<cudaStream_t>(stream);
-  // the maxima are merged with atomic max, so the shared array must start at zero on every call
-  if (cudaMemsetAsync(colmax, 0, size_t(N) * 4, s) != cudaSuccess) return FP4_ERR_CUDA;
-  const int col_blocks = int((N + 255) / 256);
-  int splits = (4 * sms + col_blocks - 1) / col_blocks;
-  const int max_splits = int((K + 63) / 64);
-  if (splits > max_splits) splits = max_splits;
-  if (splits < 1) splits = 1;
-  const int rows_per_split = int((K + splits - 1) / splits);
-  splits = int((K + rows_per_split - 1) / rows_per_split);
-  const auto* w = static_cast<const uint16_t*>(W);
-  col_absmax_kernel<<<dim3(col_blocks, splits), 256, 0, s>>>(w, int(K), int(N), ldw, rows_per_split, colmax);
-  if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
-  quantize_cols_kernel<<<dim3(unsigned((N + 63) / 64), unsigned((K + 63) / 64)), 256, 0, s>>>(
-      w, int(K), int(N), ldw, colmax, codes_t, ldc_bytes, scales);
-  return launch_status();
+  // the maxima are merged with atomic max, so launch_cols clears the shared array on every call
+  return launch_cols(static_cast<const uint16_t*>(W), K, N, ldw, codes_t, ldc_bytes, scales, colmax, sms,
+                     reinterpret_cast<cudaStream_t>(stream));
 }

@@ -24,9 +24,9 @@ FLAG_TIMEOUT, FLAG_CAPACITY, FLAG_INTERNAL = 0x1, 0x2, 0x4
 
 # exported symbols, in the order include/fp4lin.h declares them
 EXPORTS = (
-    "fp4_status_string", "fp4_abi_version", "fp4_quantize_rows", "fp4_quantize_cols_workspace",
+    "fp4_status_string", "fp4_abi_version", "fp4_last_cuda_error", "fp4_quantize_rows", "fp4_quantize_cols_workspace",
     "fp4_quantize_cols", "fp4_quantize_cols_noalloc", "outlier_max_nnz", "outlier_clamp_quantile_workspace", "outlier_clamp_quantile",
-    "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_device_status", "fp4_selftest_bounded_wait",
+    "fp4_quantize_rows_outliers", "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_device_status", "fp4_selftest_bounded_wait",
 )
 
 
@@ -48,6 +48,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     sig = {
         "fp4_status_string": (ctypes.c_char_p, [_c_int]),
         "fp4_abi_version": (_c_int, []),
+        "fp4_last_cuda_error": (ctypes.c_char_p, []),
         "fp4_quantize_rows": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp]),
         "fp4_quantize_cols_workspace": (_c_sz, [_c_i64]),
         "fp4_quantize_cols": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_vp, _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]),
@@ -56,6 +57,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "outlier_clamp_quantile_workspace": (_c_sz, [_c_i64, _c_i64, _c_i64]),
         "outlier_clamp_quantile": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_d, _c_vp, _c_vp, _c_vp, _c_vp,
                                             _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_sz, _c_vp]),
+        "fp4_quantize_rows_outliers": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_d, _c_vp, _c_i64, _c_vp, _c_vp,
+                                                _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]),
         "fp4_linear_fwd": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp,
                                     _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_i64, _c_vp]),
         "fp4_linear_wgrad_dge": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64,
@@ -79,7 +82,10 @@ def status_string(status: int) -> str:
 
 def _check(fn: str, status: int) -> None:
     if status != 0:
-        raise FP4Error(fn, status, status_string(status))
+        msg = status_string(status)
+        if msg == "FP4_ERR_CUDA":
+            msg += ": " + _lib.fp4_last_cuda_error().decode()
+        raise FP4Error(fn, status, msg)
 
 
 def _p(t: Optional[torch.Tensor]):
@@ -192,6 +198,32 @@ def outlier_clamp_quantile(A: torch.Tensor, q: float, want_clamped: bool = False
     return o
 
 
+def fp4_quantize_rows_outliers(A: torch.Tensor, q: float, out: Optional[Dict[str, torch.Tensor]] = None,
+                               stream=None) -> Dict[str, torch.Tensor]:
+    """Threshold, clamp, CSR of dA and the row codes / scales of A_clamped in one call.
+    Returns the outlier_clamp_quantile dict plus 'codes' (M x K/2) and 'scales' (M)."""
+    lda = _rowmajor(A, "A", torch.bfloat16)
+    M, K = A.shape
+    cap = outlier_max_nnz(M, K, q)
+    dev = A.device
+    o = dict(out) if out is not None else {}
+    o.setdefault("t", torch.empty((1,), dtype=torch.float32, device=dev))
+    o.setdefault("row_ptr", torch.empty((M + 1,), dtype=torch.int32, device=dev))
+    o.setdefault("col_idx", torch.empty((max(cap, 1),), dtype=torch.int32, device=dev))
+    o.setdefault("vals", torch.empty((max(cap, 1),), dtype=torch.float32, device=dev))
+    o.setdefault("nnz", torch.empty((1,), dtype=torch.int64, device=dev))
+    o.setdefault("codes", torch.empty((M, K // 2), dtype=torch.uint8, device=dev))
+    o.setdefault("scales", torch.empty((M,), dtype=torch.float32, device=dev))
+    ws_bytes = outlier_clamp_quantile_workspace(M, K, o["col_idx"].numel())
+    o.setdefault("workspace", torch.empty((ws_bytes,), dtype=torch.uint8, device=dev))
+    ldc = _rowmajor(o["codes"], "codes", torch.uint8)
+    ws = o["workspace"]
+    _check("fp4_quantize_rows_outliers", _lib.fp4_quantize_rows_outliers(
+        _p(A), M, K, lda, float(q), _p(o["codes"]), ldc, _p(o["scales"]), _p(o["t"]), _p(o["row_ptr"]),
+        _p(o["col_idx"]), _p(o["vals"]), o["col_idx"].numel(), _p(o["nnz"]), _p(ws), ws.numel(), _s(stream)))
+    return o
+
+
 # ---------------------------------------------------------------- GEMMs
 
 def fp4_linear_fwd(a_codes: torch.Tensor, s_a: Optional[torch.Tensor], w_codes_t: torch.Tensor,
@@ -251,11 +283,12 @@ def fp4_selftest_bounded_wait(timeout_us: int, stream=None) -> None:
 # ---------------------------------------------------------------- one layer
 
 def linear_forward(A: torch.Tensor, W: torch.Tensor, q: float, out_type: str = "bf16", stream=None):
-    """The whole forward of the quantized linear layer: quantile clamp + CSR,
-    row quantization of A_clamped (fused clamp), column quantization of W,
-    FP4 GEMM with scales and compensation.  Returns (Y, intermediates)."""
-    o = outlier_clamp_quantile(A, q, stream=stream)
-    a_codes, s_a = fp4_quantize_rows(A, clamp_t=o["t"], stream=stream)
+    """The whole forward of the quantized linear layer: quantile threshold,
+    clamp + CSR of dA + row quantization of A_clamped (one fused pass), column
+    quantization of W, FP4 GEMM with scales and compensation.  Returns
+    (Y, intermediates)."""
+    o = fp4_quantize_rows_outliers(A, q, stream=stream)
     w_codes_t, s_w = fp4_quantize_cols(W, stream=stream)
-    Y = fp4_linear_fwd(a_codes, s_a, w_codes_t, s_w, A.shape[1], csr=o, W=W, out_type=out_type, stream=stream)
-    return Y, dict(outlier=o, a_codes=a_codes, s_a=s_a, w_codes_t=w_codes_t, s_w=s_w)
+    Y = fp4_linear_fwd(o["codes"], o["scales"], w_codes_t, s_w, A.shape[1], csr=o, W=W, out_type=out_type,
+                       stream=stream)
+    return Y, dict(outlier=o, a_codes=o["codes"], s_a=o["scales"], w_codes_t=w_codes_t, s_w=s_w)

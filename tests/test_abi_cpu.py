@@ -44,7 +44,7 @@ def test_binding_names_match_header():
     from precision_gemm_row_gb300 import fp4lin
     assert set(fp4lin.EXPORTS) == set(_declared_functions())
     for n in fp4lin.EXPORTS:
-        if n not in ("fp4_status_string", "fp4_abi_version"):
+        if n not in ("fp4_status_string", "fp4_abi_version", "fp4_last_cuda_error"):
             assert hasattr(fp4lin, n)
 
 

@@ -1,6 +1,6 @@
 """Full-size parity on every workload (the 1.3B / 7B / 13B LLaMA shapes and the
 Student-t stress case), run through the same launches bench.py times
-(bench.LayerStep).  The oracle recomputes sampled outputs one by one:
+(bench.StepPlan).  The oracle recomputes sampled outputs one by one:
 
 * threshold t: exact order statistic over ALL of |A| (full sort);
 * CSR: every row's count against a full count of |A| > t; column indices and
@@ -10,6 +10,8 @@ Student-t stress case), run through the same launches bench.py times
 * raw FP4 accumulators bit-exact, BF16 Y (1 ulp + fp32 sum bound) on sampled rows;
 * DGE weight gradient within 1e-5 relative Frobenius on sampled feature rows.
 """
+import types
+
 import numpy as np
 import pytest
 import torch
@@ -62,10 +64,12 @@ def test_full_size_linear(fp4, workload, linear):
     work = wl.WORKLOADS[workload]
     lin = next(l for l in work.linears if l.name == linear)
     A_bits, W_bits, dY_bits = work.activation(lin), work.weight(lin), work.grad(lin)
-    step = bench.LayerStep(fp4, lin, dev_bf16(A_bits), dev_bf16(W_bits), dev_bf16(dY_bits))
-    step.run()
-    step.run()                       # second pass over the same buffers (workspace reuse)
+    plan = bench.StepPlan(fp4, types.SimpleNamespace(linears=[lin]),
+                          [(dev_bf16(A_bits), dev_bf16(W_bits), dev_bf16(dY_bits))])
+    plan.run()
+    plan.run()                       # second pass over the same buffers (workspace reuse)
     torch.cuda.synchronize()
+    act, step = next(iter(plan.acts.values())), plan.lins[0]
     assert_no_device_flags(fp4)
     M, K, N = lin.M, lin.K, lin.N
     rows = _sample(M, 1)
@@ -74,34 +78,34 @@ def test_full_size_linear(fp4, workload, linear):
 
     # threshold over all of |A|
     t, t_bits, k = orc.quantile_threshold(A_bits, lin.q)
-    assert step.out["t"].cpu().numpy().view(np.uint32)[0] == np.float32(t).view(np.uint32)
+    assert act.out["t"].cpu().numpy().view(np.uint32)[0] == np.float32(t).view(np.uint32)
     # CSR row counts for every row, entries for sampled rows
-    rp = step.out["row_ptr"].cpu().numpy().astype(np.int64)
+    rp = act.out["row_ptr"].cpu().numpy().astype(np.int64)
     counts = np.count_nonzero((A_bits & np.uint16(0x7FFF)) > np.uint16(t_bits), axis=1)
     assert np.array_equal(np.diff(rp), counts) and rp[0] == 0
-    assert int(step.out["nnz"].item()) == rp[-1] <= orc.clamp_rank(M * K, 1.0) - k
+    assert int(act.out["nnz"].item()) == rp[-1] <= orc.clamp_rank(M * K, 1.0) - k
     A_c_s, rp_s, ci_s, cv_s = orc.clamp_and_compensation(A_bits[rows], t)
-    ci_g = step.out["col_idx"].cpu().numpy()
-    cv_g = step.out["vals"].cpu().numpy()
+    ci_g = act.out["col_idx"].cpu().numpy()
+    cv_g = act.out["vals"].cpu().numpy()
     for r, i in enumerate(rows):
         seg = slice(rp[i], rp[i + 1])
         assert np.array_equal(ci_g[seg], ci_s[rp_s[r]:rp_s[r + 1]])
         assert np.array_equal(cv_g[seg].view(np.uint32), cv_s[rp_s[r]:rp_s[r + 1]].view(np.uint32))
     # row quantization of A_clamped on sampled rows
     ref_a, ref_sa = orc.quantize_rows(A_c_s)
-    assert np.array_equal(step.a_codes[torch.from_numpy(rows).cuda()].cpu().numpy(), ref_a)
-    assert np.array_equal(step.s_a.cpu().numpy()[rows].view(np.uint32), ref_sa.view(np.uint32))
+    assert np.array_equal(act.out["codes"][torch.from_numpy(rows).cuda()].cpu().numpy(), ref_a)
+    assert np.array_equal(act.out["scales"].cpu().numpy()[rows].view(np.uint32), ref_sa.view(np.uint32))
     # column quantization of W on sampled columns
     Wf = orc.bf16_to_f32(W_bits)
     ref_w, ref_sw = orc.quantize_cols(Wf[:, cols])
     assert np.array_equal(step.w_codes[torch.from_numpy(cols).cuda()].cpu().numpy(), ref_w)
     assert np.array_equal(step.s_w.cpu().numpy()[cols].view(np.uint32), ref_sw.view(np.uint32))
     # GEMM: raw accumulator (bit-exact) and compensated BF16 Y on sampled rows, from the GPU's own codes
-    a_codes = step.a_codes.cpu().numpy()
+    a_codes = act.out["codes"].cpu().numpy()
     w_codes = step.w_codes.cpu().numpy()
-    s_a = step.s_a.cpu().numpy()
+    s_a = act.out["scales"].cpu().numpy()
     s_w = step.s_w.cpu().numpy()
-    raw = fp4.fp4_linear_fwd(step.a_codes, None, step.w_codes, None, K, out_type="raw")
+    raw = fp4.fp4_linear_fwd(act.out["codes"], None, step.w_codes, None, K, out_type="raw")
     ref_raw = orc.gemm_raw(a_codes, w_codes, rows=rows).astype(np.float32)
     assert np.array_equal(raw[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint32), ref_raw.view(np.uint32))
     rp32 = rp.astype(np.int32)

@@ -96,6 +96,19 @@ def test_quantize_rows_with_fused_clamp_bit_exact(fp4):
     assert np.array_equal(codes.cpu().numpy(), ref_codes)
 
 
+@pytest.mark.parametrize("t", [2.7182817, 0.3, 1e30])
+def test_quantize_rows_with_arbitrary_fp32_clamp(fp4, t):
+    # a clamp threshold that is not a BF16 value is applied in fp32: x' = sign(x) min(|x|, t)
+    A_bits = _t3_bits(7, (64, 512), 2.0)
+    A = orc.bf16_to_f32(A_bits)
+    tf = np.float32(t)
+    A_c = np.where(np.abs(A) > tf, np.copysign(tf, A), A).astype(np.float32)
+    ref_codes, ref_s = orc.quantize_rows(A_c)
+    codes, s = fp4.fp4_quantize_rows(dev_bf16(A_bits), clamp_t=torch.tensor([t], dtype=torch.float32, device="cuda"))
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
+
+
 def test_quantize_rows_strided_input(fp4):
     A_bits = _normal_bits(3, (20, 200))
     big = dev_bf16(A_bits)
@@ -165,6 +178,30 @@ def test_outlier_clamp_repeated_calls_reuse_workspace(fp4):
     o2 = fp4.outlier_clamp_quantile(dev_bf16(A2), 0.99, out={"workspace": o["workspace"]})
     t, _, _ = orc.quantile_threshold(A2, 0.99)
     assert float(o2["t"].item()) == float(t)
+
+
+@pytest.mark.parametrize("shape,q", [((256, 512), 0.99), ((300, 1056), 0.97), ((37, 13824), 0.999), ((5, 4096), 0.5),
+                                     ((129, 96), 1.0)])
+def test_fused_rows_outliers_matches_oracle_and_separate_calls(fp4, shape, q):
+    A_bits = _t3_bits(shape[0] * 3 + shape[1], shape, 2.0)
+    A = dev_bf16(A_bits)
+    o = fp4.fp4_quantize_rows_outliers(A, q)
+    torch.cuda.synchronize()
+    t, _, _ = orc.quantile_threshold(A_bits, q)
+    A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
+    ref_codes, ref_s = orc.quantize_rows(A_c)
+    nnz = int(o["nnz"].item())
+    assert o["t"].cpu().numpy().view(np.uint32)[0] == np.float32(t).view(np.uint32)
+    assert np.array_equal(o["row_ptr"].cpu().numpy(), rp)
+    assert np.array_equal(o["col_idx"][:nnz].cpu().numpy(), ci)
+    assert np.array_equal(o["vals"][:nnz].cpu().numpy().view(np.uint32), cv.view(np.uint32))
+    assert np.array_equal(o["codes"].cpu().numpy(), ref_codes)
+    assert np.array_equal(o["scales"].cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    # same bytes as the two separate entry points
+    o2 = fp4.outlier_clamp_quantile(A, q)
+    codes2, s2 = fp4.fp4_quantize_rows(A, clamp_t=o2["t"])
+    assert torch.equal(codes2, o["codes"]) and torch.equal(s2.view(torch.int32), o["scales"].view(torch.int32))
+    assert_no_device_flags(fp4)
 
 
 # ---------------------------------------------------------------- DGE weight gradient
