@@ -272,23 +272,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       float comp[EC];
 #pragma unroll
       for (int c = 0; c < EC; ++c) comp[c] = 0.0f;
-      for (int e = e0; e < e1; ++e) {
-        const int k = __ldg(p.ci + e);
-        const float v = __ldg(p.cv + e);
-        const uint4* wr = reinterpret_cast<const uint4*>(p.W + int64_t(k) * p.ldw + col_base);
-        uint4 w[EC / 8];
+      // the (column, value) pairs of the row's first kRegEnt entries are fetched
+      // together; W is read in groups of 5 pieces (40 columns) per entry
+      constexpr int kRegEnt = 4;
+      int kk[kRegEnt];
+      float vv[kRegEnt];
 #pragma unroll
-        for (int g = 0; g < EC / 8; ++g) w[g] = (8 * g < nvalid) ? __ldg(wr + g) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int g = 0; g < EC / 8; ++g) {
-          const uint32_t wv[4] = {w[g].x, w[g].y, w[g].z, w[g].w};
-#pragma unroll
-          for (int t = 0; t < 8; ++t)
-            comp[8 * g + t] =
-                fmaf(v, bf16_bits_to_float((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu), comp[8 * g + t]);
+      for (int j = 0; j < kRegEnt; ++j) {
+        kk[j] = 0;
+        vv[j] = 0.0f;
+        if (e0 + j < e1) {
+          kk[j] = __ldg(p.ci + e0 + j);
+          vv[j] = __ldg(p.cv + e0 + j);
         }
       }
-      if (!mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns)) {
+      for (int e = e0; e < e1; ++e) {
+        const int j = e - e0;
+        int k;
+        float v;
+        if (j < kRegEnt) {
+          k = kk[0];
+          v = vv[0];
+#pragma unroll
+          for (int i = 1; i < kRegEnt; ++i)
+            if (j == i) {
+              k = kk[i];
+              v = vv[i];
+            }
+        } else {
+          k = __ldg(p.ci + e);
+          v = __ldg(p.cv + e);
+        }
+        const uint4* wr = reinterpret_cast<const uint4*>(p.W + int64_t(k) * p.ldw + col_base);
+#pragma unroll
+        for (int g0 = 0; g0 < EC / 8; g0 += 5) {
+          uint4 w[5];
+#pragma unroll
+          for (int g = 0; g < 5; ++g)
+            w[g] = (8 * (g0 + g) < nvalid) ? __ldg(wr + g0 + g) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int g = 0; g < 5; ++g) {
+            const uint32_t wv[4] = {w[g].x, w[g].y, w[g].z, w[g].w};
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+              comp[8 * (g0 + g) + t] =
+                  fmaf(v, bf16_bits_to_float((wv[t >> 1] >> (16 * (t & 1))) & 0xFFFFu), comp[8 * (g0 + g) + t]);
+          }
+        }
+      }
+      // the warp leaves the wait converged and with one verdict (tcgen05.ld is warp-wide)
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns))) {
         ok = false;
         break;
       }
@@ -302,40 +335,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int pc = 0; pc < EC; pc += 40) {
         if (col_base + pc < p.N) {   // warp-uniform
-          float y[40];
-#pragma unroll
-          for (int g = 0; g < 5; ++g) {
-            uint32_t r[8];
-            tmem_ld8(tmem + lane_base + uint32_t(acc * BN + c_base + pc + 8 * g), r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const int c = pc + 8 * g + t;
-              y[8 * g + t] = raw ? __uint_as_float(r[t]) : __uint_as_float(r[t]) * inv_sa * inv_sw_w[c] + comp[c];
-            }
-          }
 #pragma unroll
           for (int part = 0; part < 2; ++part) {
             if (bf16_out && part == 1) break;
             if (lane == 0) bulk_wait_read_all();   // the previous store has read the buffer
             __syncwarp();
-            if (bf16_out) {
+            // 8 columns at a time: read, scale, add, convert and stage
 #pragma unroll
-              for (int g = 0; g < 5; ++g) {
+            for (int gg = 0; gg < 5; ++gg) {
+              // fp32: only the groups that overlap columns 20*part .. +19 of the pass
+              if (!bf16_out && !(8 * gg < 20 * part + 20 && 8 * gg + 8 > 20 * part)) continue;
+              uint32_t r[8];
+              tmem_ld8(tmem + lane_base + uint32_t(acc * BN + c_base + pc + 8 * gg), r);
+              tmem_wait_ld();
+              float y[8];
+#pragma unroll
+              for (int t = 0; t < 8; ++t) {
+                const int c = pc + 8 * gg + t;
+                y[t] = raw ? __uint_as_float(r[t]) : __uint_as_float(r[t]) * inv_sa * inv_sw_w[c] + comp[c];
+              }
+              if (bf16_out) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                  const __nv_bfloat162 h = __floats2bfloat162_rn(y[8 * g + 2 * t], y[8 * g + 2 * t + 1]);
+                  const __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * t], y[2 * t + 1]);
                   pk[t] = *reinterpret_cast<const uint32_t*>(&h);
                 }
-                *reinterpret_cast<uint4*>(orow + 16 * g) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              }
-            } else {
+                *reinterpret_cast<uint4*>(orow + 16 * gg) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              } else {
+                // fp32: columns 20*part .. +19 of this pass go to the staging row
 #pragma unroll
-              for (int g = 0; g < 5; ++g)
-                *reinterpret_cast<float4*>(orow + 16 * g) =
-                    make_float4(y[20 * part + 4 * g], y[20 * part + 4 * g + 1], y[20 * part + 4 * g + 2],
-                                y[20 * part + 4 * g + 3]);
+                for (int t = 0; t < 8; ++t) {
+                  const int cc = 8 * gg + t - 20 * part;
+                  if (cc >= 0 && cc < 20) reinterpret_cast<float*>(orow)[cc] = y[t];
+                }
+              }
             }
             fence_proxy_async_smem();
             __syncwarp();

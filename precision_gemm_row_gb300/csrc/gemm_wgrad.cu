@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kEpiCols; ++c) sum[c] = 0.0f;
       for (int tb0 = 0; tb0 < tblocks; tb0 += kChunkStages) {
-        if (!mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns)) {
+        // the warp leaves the wait converged and with one verdict (tcgen05.ld is warp-wide)
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns))) {
           ok = false;
           break;
         }
