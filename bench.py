@@ -146,7 +146,8 @@ class LinStep:
     """One linear: column quantization of W, FP4 GEMM, DGE weight gradient."""
 
     PHASES = ("fp4_quantize_cols", "fp4_linear_fwd", "fp4_linear_wgrad_dge")
-    LAUNCHES = {"fp4_quantize_cols": 2, "fp4_linear_fwd": 1, "fp4_linear_wgrad_dge": 1}
+    # fwd: 2 compensation prep kernels (after a memset) and the GEMM
+    LAUNCHES = {"fp4_quantize_cols": 2, "fp4_linear_fwd": 3, "fp4_linear_wgrad_dge": 1}
 
     def __init__(self, fp4, lin, act: ActStep, W, dY):
         import torch
@@ -158,6 +159,7 @@ class LinStep:
         self.s_w = torch.empty(N, dtype=torch.float32, device=dev)
         self.ws_cols = torch.empty(max(fp4.fp4_quantize_cols_workspace(N), 16), dtype=torch.uint8, device=dev)
         self.Y = torch.empty((lin.M, N), dtype=torch.bfloat16, device=dev)
+        self.ws_fwd = torch.empty(fp4.fp4_linear_fwd_workspace(lin.M, N, K), dtype=torch.uint8, device=dev)
         self.dW = torch.empty((K, N), dtype=torch.float32, device=dev)
 
     def fns(self):
@@ -165,7 +167,7 @@ class LinStep:
         return [
             lambda: fp4.fp4_quantize_cols(self.W, codes_t=self.w_codes, scales=self.s_w, workspace=self.ws_cols),
             lambda: fp4.fp4_linear_fwd(a.out["codes"], a.out["scales"], self.w_codes, self.s_w, lin.K, csr=a.out,
-                                       W=self.W, out_type="bf16", Y=self.Y),
+                                       W=self.W, out_type="bf16", Y=self.Y, workspace=self.ws_fwd),
             lambda: fp4.fp4_linear_wgrad_dge(a.A, self.dY, self.W, self.s_w, DGE_K, DGE_CLIP, dW=self.dW),
         ]
 

@@ -210,8 +210,17 @@ fp4_status fp4_quantize_rows_outliers(const void* A, int64_t M, int64_t K, int64
                                       void* workspace, size_t ws_bytes, fp4_stream_t stream);
 
 /*
+ * fp4_linear_fwd_workspace -- bytes of device workspace that fp4_linear_fwd
+ * uses to run the compensation on the tensor cores for an M x K by K x N
+ * product (grows as 1 KB per row of M and of N).  0 for invalid shapes.
+ * Host-only.  This workspace has no counterpart on the pages: it holds the
+ * scaled, split operands of the compensation product described below.
+ */
+size_t fp4_linear_fwd_workspace(int64_t M, int64_t N, int64_t K);
+
+/*
  * fp4_linear_fwd -- FP4 GEMM on tcgen05 (kind::mxf4, unit block scales) with
- * the row x column scales and the sparse dA*W compensation in the epilogue.
+ * the row x column scales and the sparse dA*W compensation.
  *
  * Defined by: page "首个 FP4 ..." (czzqal.com), GeMM passage (custom FP4 GEMM
  * kernel, tiled multiply in FP4) and granularity passage (the row / column
@@ -220,24 +229,39 @@ fp4_status fp4_quantize_rows_outliers(const void* A, int64_t M, int64_t K, int64
  *   acc[i,j] = sum_k decode(a_codes[i,k]) * decode(w_codes_t[j,k])   (exact in fp32)
  *   Y[i,j]   = acc[i,j] / (s_A[i] s_W[j]) + sum_{e in row i of dA} val[e] * W[col[e], j]
  *
+ * How the compensation runs (results agree to fp32 rounding either way):
+ *   - workspace given and dA has at most 128 distinct nonzero columns (outlier
+ *     channels): the product over those columns runs on the tensor cores as
+ *     TF32 MMAs into the same accumulator, with dA s_A and W s_W each split
+ *     into two TF32 parts (relative error of each term about 2^-22);
+ *   - otherwise (no workspace, or more distinct columns): the epilogue threads
+ *     add the sum in fp32, entry by entry in CSR order.
+ *
  *   a_codes   device uint8 M x lda_codes_bytes (K-major), 16-byte aligned, lda_codes_bytes % 16 == 0
  *   s_a       device fp32 M
  *   w_codes_t device uint8 N x ldw_codes_bytes (K-major), 16-byte aligned, % 16 == 0
  *   s_w       device fp32 N
- *   M, N, K   M, N >= 1; K >= 32, K % 32 == 0; M, N, K < 2^31; N % 8 == 0
+ *   M, N, K   M, N >= 1; 32 <= K <= 16384, K % 32 == 0; M, N < 2^31; N % 8 == 0
  *   dA_row_ptr, dA_col, dA_val  device CSR of dA (as from outlier_clamp_quantile),
- *             all three NULL for no compensation
+ *             all three NULL for no compensation; the columns of a row must be
+ *             distinct (the epilogue path is fastest when they ascend)
  *   W         device BF16 K x ldw (the unquantized weight), required iff compensation
  *   Y         device, M x ldy elements of the output type; 16-byte aligned, ldy % 8 == 0
  *   y_type    fp4_out_type
- * Errors: INVALID_ARG, SHAPE, ALIGNMENT, DEVICE_UNSUPPORTED, CUDA;
- *         device-side TIMEOUT flag if a pipeline wait runs out (about 1 s).
+ *   workspace device, 256-byte aligned, ws_bytes >= fp4_linear_fwd_workspace(M, N, K),
+ *             or NULL; used only with compensation; must not be shared by calls
+ *             that may run at the same time; owned by the caller
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE (non-NULL and too small),
+ *         DEVICE_UNSUPPORTED, CUDA; device-side TIMEOUT flag if a pipeline wait
+ *         runs out (about 1 s); device-side INTERNAL flag for a dA column
+ *         outside [0, K) (the entry is skipped).
  */
 fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_bytes, const float* s_a,
                           const uint8_t* w_codes_t, int64_t ldw_codes_bytes, const float* s_w,
                           int64_t M, int64_t N, int64_t K, const int32_t* dA_row_ptr,
                           const int32_t* dA_col, const float* dA_val, const void* W, int64_t ldw,
-                          void* Y, int y_type, int64_t ldy, fp4_stream_t stream);
+                          void* Y, int y_type, int64_t ldy, void* workspace, size_t ws_bytes,
+                          fp4_stream_t stream);
 
 /*
  * fp4_linear_wgrad_dge -- BF16 weight-gradient GEMM on tcgen05 (kind::f16)

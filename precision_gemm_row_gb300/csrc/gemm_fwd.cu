@@ -26,6 +26,18 @@
 // reads the accumulator in groups of 8 columns, scales, adds and stores.
 // Every mbarrier wait is bounded; on expiry the CTA records FP4_FLAG_TIMEOUT,
 // drains its TMA loads and MMAs, frees TMEM and exits.
+//
+// Compensation on the tensor cores.  Outliers gather in a few channels, so dA
+// has few distinct nonzero columns H.  When the caller passes a workspace and
+// |H| <= kHotMax, small prep kernels build, for the columns in H,
+//   P  = fl32(dA[:,H] * s_A)   (M x |H|)    and   Q^T = fl32(W[H,:] * s_W)^T  (N x |H|),
+// each split exactly into two TF32 parts (x = hi + lo + O(2^-23 |x|)), and the
+// GEMM kernel runs, after the FP4 K loop of a tile, three more pipeline stages
+// per 32 columns of H: kind::tf32 MMAs of hi*hi, hi*lo and lo*hi into the same
+// accumulator (the dropped lo*lo term is below 2^-22 relative).  The epilogue
+// then scales acc + P Q^T by 1/(s_A s_W), which equals acc/(s_A s_W) + dA W up to
+// fp32 rounding, and does no compensation work of its own.  Without a
+// workspace, or with more distinct columns, the epilogue forms the sum itself.
 #include "common.cuh"
 
 namespace fp4 {
@@ -67,6 +79,173 @@ __host__ __device__ constexpr uint32_t idesc_mxf4() {
   return (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (1u << 23) | (uint32_t(kBM >> 4) << 24);
 }
 
+constexpr int kHotMax = 128;    // distinct dA columns handled on the tensor cores
+constexpr int kHotChunk = 32;   // TF32 values per 128-byte row: one pipeline stage of K
+
+// Filled on the device by the prep kernels, read by every CTA of the GEMM.
+struct HotInfo {
+  int hc;     // distinct nonzero columns of dA
+  int hp;     // hc rounded up to a multiple of kHotChunk
+  int mode;   // 1: compensation on the tensor cores
+  int pad;
+};
+
+// Instruction descriptor, kind::tf32: fp32 accumulator, A and B TF32, both K-major.
+template <int BN>
+__host__ __device__ constexpr uint32_t idesc_tf32() {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+}
+
+// Round an fp32 value to TF32 (10 explicit mantissa bits), nearest, ties to even.
+__device__ __forceinline__ float round_tf32(float x) {
+  uint32_t u = __float_as_uint(x);
+  u += 0xFFFu + ((u >> 13) & 1u);
+  return __uint_as_float(u & 0xFFFFE000u);
+}
+
+// x = hi + lo + r with hi, lo TF32 values and |r| <= 2^-23 |x| (lo is the
+// rounded remainder x - hi, which fp32 holds exactly).
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+  hi = round_tf32(x);
+  lo = round_tf32(x - hi);
+}
+
+// Numbers the marked columns in ascending order (word prefix counts), lists
+// them, and decides whether the tensor-core path applies.  Run by one CTA of
+// 512 threads; reads the bitmap from L2.
+__device__ void hot_scan(const uint32_t* bitmap, uint32_t* word_prefix, int32_t* hlist, HotInfo* info, int nwords,
+                         uint32_t* wsum) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const uint32_t bits = t < nwords ? __ldcg(bitmap + t) : 0u;
+  const uint32_t c = __popc(bits);
+  uint32_t incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[w] = incl;
+  __syncthreads();
+  uint32_t base = 0, total = 0;
+  for (int i = 0; i < 16; ++i) {
+    total += wsum[i];
+    if (i < w) base += wsum[i];
+  }
+  const uint32_t excl = base + incl - c;
+  if (t < nwords) word_prefix[t] = excl;
+  const bool on = total > 0 && total <= uint32_t(kHotMax);
+  if (on) {
+    uint32_t m = bits, h = excl;
+    while (m) {
+      const int b = __ffs(m) - 1;
+      m &= m - 1u;
+      hlist[h++] = t * 32 + b;
+    }
+  }
+  if (t == 0) {
+    HotInfo hi;
+    hi.hc = int(total);
+    hi.hp = int((total + kHotChunk - 1) / kHotChunk) * kHotChunk;
+    hi.mode = on ? 1 : 0;
+    hi.pad = 0;
+    *info = hi;
+  }
+}
+
+// Marks the columns of every dA entry in a K-bit bitmap (cleared beforehand,
+// together with `done`).  Outlier columns repeat across rows, so each CTA marks
+// a bitmap of its own in shared memory and ORs only its nonzero words into the
+// global one; the last CTA to finish numbers the columns (hot_scan) and resets
+// `done` for the next call.  512 threads per CTA.
+__global__ void __launch_bounds__(512) hot_mark_kernel(const int32_t* __restrict__ rp, const int32_t* __restrict__ ci,
+                                                       int M, int K, uint32_t* bitmap, uint32_t* done,
+                                                       uint32_t* word_prefix, int32_t* hlist, HotInfo* info,
+                                                       uint32_t* status) {
+  __shared__ uint32_t local[16384 / 32];
+  __shared__ uint32_t wsum[16];
+  __shared__ bool last;
+  const int nwords = K >> 5;
+  for (int w = threadIdx.x; w < nwords; w += blockDim.x) local[w] = 0u;
+  __syncthreads();
+  const int nnz = __ldg(rp + M);
+  bool bad = false;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < nnz; e += gridDim.x * blockDim.x) {
+    const int k = __ldg(ci + e);
+    if (uint32_t(k) < uint32_t(K)) atomicOr(local + (k >> 5), 1u << (k & 31));
+    else bad = true;
+  }
+  if (bad) atomicOr(status, FP4_FLAG_INTERNAL);
+  __syncthreads();
+  for (int w = threadIdx.x; w < nwords; w += blockDim.x)
+    if (local[w]) atomicOr(bitmap + w, local[w]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  hot_scan(bitmap, word_prefix, hlist, info, nwords, wsum);
+  if (threadIdx.x == 0) *done = 0u;
+}
+
+// Builds both operands of the compensation product, 256 threads per CTA:
+//   CTAs [0, p_ctas): one warp per row i: P[i, 0..hp) = 0, then the row's
+//     entries, scaled by s_A[i] and split, at their column numbers (the row's
+//     columns are distinct);
+//   the rest: one thread per output column j and 4 columns h of H:
+//     Q^T[j, h] = fl32(W[H[h], j] * s_W[j]), split; zero for h in [hc, hp).
+__global__ void __launch_bounds__(256) hot_build_kernel(
+    const int32_t* __restrict__ rp, const int32_t* __restrict__ ci, const float* __restrict__ cv,
+    const float* __restrict__ s_a, const uint16_t* __restrict__ W, int64_t ldw, const float* __restrict__ s_w,
+    const uint32_t* __restrict__ bitmap, const uint32_t* __restrict__ word_prefix, const int32_t* __restrict__ hlist,
+    const HotInfo* __restrict__ info, float* p_hi, float* p_lo, float* q_hi, float* q_lo, int M, int N, int K,
+    int p_ctas) {
+  const HotInfo hi = *info;
+  if (!hi.mode) return;
+  if (int(blockIdx.x) < p_ctas) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= M) return;
+    float4* ph = reinterpret_cast<float4*>(p_hi + int64_t(row) * kHotMax);
+    float4* pl = reinterpret_cast<float4*>(p_lo + int64_t(row) * kHotMax);
+    for (int i = lane; i < hi.hp / 4; i += 32) {
+      ph[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      pl[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncwarp();
+    const int e0 = __ldg(rp + row), e1 = __ldg(rp + row + 1);
+    const float sa = __ldg(s_a + row);
+    for (int e = e0 + lane; e < e1; e += 32) {
+      const int k = __ldg(ci + e);
+      if (uint32_t(k) >= uint32_t(K)) continue;   // flagged by the marking pass
+      const uint32_t wd = __ldg(bitmap + (k >> 5));
+      const int h = int(__ldg(word_prefix + (k >> 5)) + __popc(wd & ((1u << (k & 31)) - 1u)));
+      float a, b;
+      split_tf32(__fmul_rn(__ldg(cv + e), sa), a, b);
+      p_hi[int64_t(row) * kHotMax + h] = a;
+      p_lo[int64_t(row) * kHotMax + h] = b;
+    }
+    return;
+  }
+  const int nj = (N + 255) / 256;
+  const int qb = int(blockIdx.x) - p_ctas;
+  const int h0 = 4 * (qb / nj);
+  if (h0 >= hi.hp) return;
+  const int j = (qb % nj) * 256 + threadIdx.x;
+  if (j >= N) return;
+  const float sw = __ldg(s_w + j);
+  float a[4], b[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int h = h0 + t;
+    const float x = h < hi.hc ? __fmul_rn(bf16_bits_to_float(__ldg(W + int64_t(__ldg(hlist + h)) * ldw + j)), sw)
+                              : 0.0f;
+    split_tf32(x, a[t], b[t]);
+  }
+  reinterpret_cast<float4*>(q_hi + int64_t(j) * kHotMax)[h0 / 4] = make_float4(a[0], a[1], a[2], a[3]);
+  reinterpret_cast<float4*>(q_lo + int64_t(j) * kHotMax)[h0 / 4] = make_float4(b[0], b[1], b[2], b[3]);
+}
+
 struct FwdParams {
   const float* s_a;
   const float* s_w;
@@ -79,6 +258,7 @@ struct FwdParams {
   int64_t ldy;
   int y_type;
   int M, N, K;
+  const HotInfo* hot;   // null: no tensor-core compensation
   uint32_t* status;
   uint64_t wait_ns;
 };
@@ -86,7 +266,9 @@ struct FwdParams {
 template <int BN, int NACC>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmY, const FwdParams p) {
+                   const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmPh,
+                   const __grid_constant__ CUtensorMap tmPl, const __grid_constant__ CUtensorMap tmQh,
+                   const __grid_constant__ CUtensorMap tmQl, const FwdParams p) {
   using C = FwdCfg<BN, NACC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -107,6 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmY);
+    if (p.hot) {
+      prefetch_tmap(&tmPh);
+      prefetch_tmap(&tmPl);
+      prefetch_tmap(&tmQh);
+      prefetch_tmap(&tmQl);
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
@@ -143,6 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_n = (p.N + BN - 1) / BN;
   const int tiles = num_m * num_n;
   const int kblocks = (p.K / 2 + kBKBytes - 1) / kBKBytes;
+  // tensor-core compensation: 3 stages (hi*hi, hi*lo, lo*hi) per 32 columns of H
+  const bool hot = p.hot != nullptr && p.hot->mode != 0;
+  const int hot_stages = hot ? 3 * (p.hot->hp / kHotChunk) : 0;
+  const int nstages = kblocks + hot_stages;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -152,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       const int mb = tile % num_m, nb = tile / num_m;
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = 0; kb < nstages; ++kb) {
         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
           ok = false;
           break;
@@ -160,8 +352,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           const uint32_t fb = full0 + 8 * stage;
           mbar_arrive_expect_tx(fb, C::kStageBytes);
-          tma_load_2d(smem_u32(sA + stage * C::kAStage), &tmA, fb, kb * kBKBytes, mb * kBM);
-          tma_load_2d(smem_u32(sB + stage * C::kBStage), &tmB, fb, kb * kBKBytes, nb * BN);
+          if (kb < kblocks) {
+            tma_load_2d(smem_u32(sA + stage * C::kAStage), &tmA, fb, kb * kBKBytes, mb * kBM);
+            tma_load_2d(smem_u32(sB + stage * C::kBStage), &tmB, fb, kb * kBKBytes, nb * BN);
+          } else {
+            // 32 columns of H: P part x Q part, pairs (hi, hi), (hi, lo), (lo, hi);
+            // every load names its tensor map directly
+            const int hs = kb - kblocks, chunk = hs / 3, pair = hs - 3 * chunk;
+            const uint32_t da = smem_u32(sA + stage * C::kAStage), db = smem_u32(sB + stage * C::kBStage);
+            const int x = chunk * kHotChunk;
+            if (pair == 2) tma_load_2d(da, &tmPl, fb, x, mb * kBM);
+            else tma_load_2d(da, &tmPh, fb, x, mb * kBM);
+            if (pair == 1) tma_load_2d(db, &tmQl, fb, x, nb * BN);
+            else tma_load_2d(db, &tmQh, fb, x, nb * BN);
+          }
         }
         __syncwarp();
         ++issued;
@@ -195,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem + uint32_t(acc * BN);
-      for (int kb = 0; kb < kblocks; ++kb) {
+      for (int kb = 0; kb < nstages; ++kb) {
         if (!mbar_wait(full0 + 8 * stage, phase, p.wait_ns)) {
           ok = false;
           break;
@@ -203,11 +407,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a0 = a_base + stage * C::kAStage, b0 = b_base + stage * C::kBStage;
+          // 32 bytes of K per MMA in both kinds: 64 E2M1 values or 8 TF32 values
+          if (kb < kblocks) {
 #pragma unroll
-          for (int k = 0; k < kBKBytes / kMmaKBytes; ++k) {
-            const uint64_t ad = smem_desc_sw128(a0 + k * kMmaKBytes, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(b0 + k * kMmaKBytes, 16, 1024);
-            mma_mxf4(d_tmem, ad, bd, idesc, sfa, sfb, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kBKBytes / kMmaKBytes; ++k) {
+              const uint64_t ad = smem_desc_sw128(a0 + k * kMmaKBytes, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(b0 + k * kMmaKBytes, 16, 1024);
+              mma_mxf4(d_tmem, ad, bd, idesc, sfa, sfb, (kb | k) != 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kBKBytes / kMmaKBytes; ++k) {
+              const uint64_t ad = smem_desc_sw128(a0 + k * kMmaKBytes, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(b0 + k * kMmaKBytes, 16, 1024);
+              mma_tf32(d_tmem, ad, bd, idesc_tf32<BN>(), 1u);
+            }
           }
           tc_commit(empty0 + 8 * stage);
         }
@@ -259,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int e0 = 0, e1 = 0;
       if (row_ok && !raw) {
         inv_sa = 1.0f / __ldg(p.s_a + row);
-        if (p.rp) {
+        if (p.rp && !hot) {
           e0 = __ldg(p.rp + row);
           e1 = __ldg(p.rp + row + 1);
         }
@@ -406,11 +620,51 @@ constexpr int kFwdAcc = 2;
 }  // namespace
 }  // namespace fp4
 
+namespace fp4 {
+namespace {
+// Workspace of the tensor-core compensation (offsets in bytes).
+struct HotLayout {
+  size_t info, bitmap, prefix, hlist, p_hi, p_lo, q_hi, q_lo, total;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+HotLayout hot_layout(int64_t M, int64_t N, int64_t K) {
+  HotLayout L;
+  size_t off = 0;
+  L.info = off;
+  off += 256;
+  L.bitmap = off;   // K/32 bitmap words, then the CTA-done counter (one memset clears both)
+  off = align_up(off + size_t(K / 32) * 4 + 4, 256);
+  L.prefix = off;
+  off = align_up(off + size_t(K / 32) * 4, 256);
+  L.hlist = off;
+  off = align_up(off + size_t(kHotMax) * 4, 1024);
+  L.p_hi = off;
+  off = align_up(off + size_t(M) * kHotMax * 4, 1024);
+  L.p_lo = off;
+  off = align_up(off + size_t(M) * kHotMax * 4, 1024);
+  L.q_hi = off;
+  off = align_up(off + size_t(N) * kHotMax * 4, 1024);
+  L.q_lo = off;
+  off = align_up(off + size_t(N) * kHotMax * 4, 1024);
+  L.total = off;
+  return L;
+}
+}  // namespace
+}  // namespace fp4
+
+FP4_API size_t fp4_linear_fwd_workspace(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || K > 16384 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31))
+    return 0;
+  return fp4::hot_layout(M, N, K).total;
+}
+
 FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_bytes, const float* s_a,
                                   const uint8_t* w_codes_t, int64_t ldw_codes_bytes, const float* s_w, int64_t M,
                                   int64_t N, int64_t K, const int32_t* dA_row_ptr, const int32_t* dA_col,
                                   const float* dA_val, const void* W, int64_t ldw, void* Y, int y_type, int64_t ldy,
-                                  fp4_stream_t stream) {
+                                  void* workspace, size_t ws_bytes, fp4_stream_t stream) {
   using namespace fp4;
   using C = FwdCfg<kFwdBN, kFwdAcc>;
   if (!a_codes || !w_codes_t || !Y) return FP4_ERR_INVALID_ARG;
@@ -428,9 +682,14 @@ FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_byte
   if (lda_codes_bytes % 16 || ldw_codes_bytes % 16 || !aligned16(a_codes) || !aligned16(w_codes_t) || !aligned16(Y) ||
       ldy % 8 || (comp && (!aligned16(W) || ldw % 8)))
     return FP4_ERR_ALIGNMENT;
+  const HotLayout L = hot_layout(M, N, K);
+  const bool use_hot = comp && workspace != nullptr;
+  if (use_hot && ws_bytes < L.total) return FP4_ERR_WORKSPACE;
+  if (use_hot && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FP4_ERR_ALIGNMENT;
   int sms = 0;
   fp4_status st = check_device(&sms);
   if (st != FP4_OK) return st;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
 
   CUtensorMap tmA, tmB;
   st = encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, uint64_t(K / 2), uint64_t(M),
@@ -446,6 +705,46 @@ FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_byte
                       uint64_t(N), uint64_t(M), uint64_t(ldy) * (bf16_out ? 2 : 4), bf16_out ? 40 : 20, 32,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != FP4_OK) return st;
+
+  // tensor-core compensation: prep kernels fill the workspace; the GEMM reads
+  // HotInfo to learn whether (and over how many columns) to run the TF32 stages
+  CUtensorMap tmPh = tmA, tmPl = tmA, tmQh = tmA, tmQl = tmA;   // unused unless use_hot
+  const HotInfo* hot_info = nullptr;
+  if (use_hot) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    HotInfo* info = reinterpret_cast<HotInfo*>(ws + L.info);
+    uint32_t* bitmap = reinterpret_cast<uint32_t*>(ws + L.bitmap);
+    uint32_t* prefix = reinterpret_cast<uint32_t*>(ws + L.prefix);
+    int32_t* hlist = reinterpret_cast<int32_t*>(ws + L.hlist);
+    float* p_hi = reinterpret_cast<float*>(ws + L.p_hi);
+    float* p_lo = reinterpret_cast<float*>(ws + L.p_lo);
+    float* q_hi = reinterpret_cast<float*>(ws + L.q_hi);
+    float* q_lo = reinterpret_cast<float*>(ws + L.q_lo);
+    const int nwords = int(K / 32);
+    uint32_t* done = bitmap + nwords;
+    if (cudaMemsetAsync(bitmap, 0, size_t(nwords) * 4 + 4, cs) != cudaSuccess) return launch_status();
+    hot_mark_kernel<<<sms / 2, 512, 0, cs>>>(dA_row_ptr, dA_col, int(M), int(K), bitmap, done, prefix, hlist, info,
+                                             status_word());
+    const int p_ctas = int((M + 7) / 8);
+    const int q_ctas = int((N + 255) / 256) * (kHotMax / 4);
+    hot_build_kernel<<<p_ctas + q_ctas, 256, 0, cs>>>(dA_row_ptr, dA_col, dA_val, s_a, static_cast<const uint16_t*>(W),
+                                                     ldw, s_w, bitmap, prefix, hlist, info, p_hi, p_lo, q_hi, q_lo,
+                                                     int(M), int(N), int(K), p_ctas);
+    st = launch_status();
+    if (st != FP4_OK) return st;
+    const uint32_t row_bytes = kHotMax * 4;
+    if ((st = encode_tmap_2d(&tmPh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p_hi, kHotMax, uint64_t(M), row_bytes, kHotChunk,
+                             kBM, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
+        (st = encode_tmap_2d(&tmPl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p_lo, kHotMax, uint64_t(M), row_bytes, kHotChunk,
+                             kBM, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
+        (st = encode_tmap_2d(&tmQh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q_hi, kHotMax, uint64_t(N), row_bytes, kHotChunk,
+                             kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
+        (st = encode_tmap_2d(&tmQl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q_lo, kHotMax, uint64_t(N), row_bytes, kHotChunk,
+                             kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK)
+      return st;
+    hot_info = info;
+  }
+
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -469,10 +768,11 @@ FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_byte
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
+  p.hot = hot_info;
   p.status = status_word();
   p.wait_ns = kWaitLimitNs;
   const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kFwdBN - 1) / kFwdBN);
   const int grid = int(tiles < sms ? tiles : sms);
-  kern<<<grid, kThreads, C::kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmB, tmY, p);
+  kern<<<grid, kThreads, C::kSmemBytes, cs>>>(tmA, tmB, tmY, tmPh, tmPl, tmQh, tmQl, p);
   return launch_status();
 }

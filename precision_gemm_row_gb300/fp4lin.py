@@ -26,7 +26,8 @@ FLAG_TIMEOUT, FLAG_CAPACITY, FLAG_INTERNAL = 0x1, 0x2, 0x4
 EXPORTS = (
     "fp4_status_string", "fp4_abi_version", "fp4_last_cuda_error", "fp4_quantize_rows", "fp4_quantize_cols_workspace",
     "fp4_quantize_cols", "fp4_quantize_cols_noalloc", "outlier_max_nnz", "outlier_clamp_quantile_workspace", "outlier_clamp_quantile",
-    "fp4_quantize_rows_outliers", "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_device_status", "fp4_selftest_bounded_wait",
+    "fp4_quantize_rows_outliers", "fp4_linear_fwd_workspace", "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_device_status",
+    "fp4_selftest_bounded_wait",
 )
 
 
@@ -59,8 +60,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                             _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_sz, _c_vp]),
         "fp4_quantize_rows_outliers": (_c_int, [_c_vp, _c_i64, _c_i64, _c_i64, _c_d, _c_vp, _c_i64, _c_vp, _c_vp,
                                                 _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_sz, _c_vp]),
+        "fp4_linear_fwd_workspace": (_c_sz, [_c_i64, _c_i64, _c_i64]),
         "fp4_linear_fwd": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp,
-                                    _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_i64, _c_vp]),
+                                    _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_sz, _c_vp]),
         "fp4_linear_wgrad_dge": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64,
                                           _c_i64, _c_f, _c_f, _c_vp, _c_i64, _c_vp]),
         "fp4_device_status": (_c_int, [_c_vp, ctypes.POINTER(_c_u32)]),
@@ -226,11 +228,21 @@ def fp4_quantize_rows_outliers(A: torch.Tensor, q: float, out: Optional[Dict[str
 
 # ---------------------------------------------------------------- GEMMs
 
+def fp4_linear_fwd_workspace(M: int, N: int, K: int) -> int:
+    """Bytes of workspace fp4_linear_fwd uses to run the compensation on the tensor cores."""
+    return int(_lib.fp4_linear_fwd_workspace(M, N, K))
+
+
 def fp4_linear_fwd(a_codes: torch.Tensor, s_a: Optional[torch.Tensor], w_codes_t: torch.Tensor,
                    s_w: Optional[torch.Tensor], K: int, csr: Optional[Dict[str, torch.Tensor]] = None,
                    W: Optional[torch.Tensor] = None, out_type: str = "bf16", Y: Optional[torch.Tensor] = None,
-                   stream=None) -> torch.Tensor:
-    """Y = (qA qW^T) / (s_A s_W^T) [+ dA W]; out_type 'bf16', 'fp32' or 'raw' (unscaled accumulator)."""
+                   workspace="auto", stream=None) -> torch.Tensor:
+    """Y = (qA qW^T) / (s_A s_W^T) [+ dA W]; out_type 'bf16', 'fp32' or 'raw' (unscaled accumulator).
+
+    workspace: "auto" allocates one when csr is given (compensation on the tensor
+    cores when dA has few distinct columns); None forces the epilogue path; or a
+    caller-owned CUDA uint8 tensor of at least fp4_linear_fwd_workspace(M, N, K) bytes.
+    """
     lda_c = _rowmajor(a_codes, "a_codes", torch.uint8)
     ldw_c = _rowmajor(w_codes_t, "w_codes_t", torch.uint8)
     M, N = a_codes.shape[0], w_codes_t.shape[0]
@@ -240,12 +252,19 @@ def fp4_linear_fwd(a_codes: torch.Tensor, s_a: Optional[torch.Tensor], w_codes_t
     ldy = _rowmajor(Y, "Y", torch.bfloat16 if yt == FP4_OUT_BF16 else torch.float32)
     rp = ci = cv = None
     ldw = 0
+    ws, ws_bytes = None, 0
     if csr is not None:
         rp, ci, cv = csr["row_ptr"], csr["col_idx"], csr["vals"]
         ldw = _rowmajor(W, "W", torch.bfloat16)
+        if isinstance(workspace, str):
+            if workspace != "auto":
+                raise ValueError("workspace must be 'auto', None or a CUDA uint8 tensor")
+            workspace = torch.empty(fp4_linear_fwd_workspace(M, N, K), dtype=torch.uint8, device=a_codes.device)
+        if workspace is not None:
+            ws, ws_bytes = workspace, workspace.numel() * workspace.element_size()
     _check("fp4_linear_fwd", _lib.fp4_linear_fwd(
         _p(a_codes), lda_c, _p(s_a), _p(w_codes_t), ldw_c, _p(s_w), M, N, K, _p(rp), _p(ci), _p(cv), _p(W), ldw,
-        _p(Y), yt, ldy, _s(stream)))
+        _p(Y), yt, ldy, _p(ws), ws_bytes, _s(stream)))
     return Y
 
 

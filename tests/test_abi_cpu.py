@@ -77,6 +77,18 @@ def test_workspace_sizes(lib):
     assert ws >= 32768 * 4 + 8192 * 12 + 16778 * 8
 
 
+def test_fwd_workspace_size(lib):
+    lib.fp4_linear_fwd_workspace.restype = ctypes.c_size_t
+    lib.fp4_linear_fwd_workspace.argtypes = [ctypes.c_int64] * 3
+    small = lib.fp4_linear_fwd_workspace(256, 512, 512)
+    big = lib.fp4_linear_fwd_workspace(8192, 5504, 2048)
+    # two 512-byte TF32 planes per row of M and per row of N, plus small tables
+    assert big >= 2 * 512 * (8192 + 5504)
+    assert 0 < small < big
+    assert lib.fp4_linear_fwd_workspace(256, 512, 48) == 0      # K not a multiple of 32
+    assert lib.fp4_linear_fwd_workspace(0, 512, 512) == 0
+
+
 def test_host_validation_rejects_bad_arguments_without_launching(lib):
     from precision_gemm_row_gb300 import fp4lin  # noqa: F401  (declares argtypes)
     L = fp4lin._lib
@@ -98,12 +110,15 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
                                     None) == 4
     # bad output type / bad K for the GEMM
     assert L.fp4_linear_fwd(fake, 32, fake, fake, 32, fake, 4, 8, 64, None, None, None, None, 0, fake, 7, 8,
-                            None) == 1
+                            None, 0, None) == 1
     assert L.fp4_linear_fwd(fake, 32, fake, fake, 32, fake, 4, 8, 48, None, None, None, None, 0, fake, 0, 8,
-                            None) == 2
+                            None, 0, None) == 2
     # partial CSR
     assert L.fp4_linear_fwd(fake, 32, fake, fake, 32, fake, 4, 8, 64, fake, None, None, None, 0, fake, 0, 8,
-                            None) == 1
+                            None, 0, None) == 1
+    # compensation workspace given but too small
+    assert L.fp4_linear_fwd(fake, 32, fake, fake, 32, fake, 4, 8, 64, fake, fake, fake, fake, 8, fake, 0, 8,
+                            fake, 16, None) == 4
     # DGE parameters
     assert L.fp4_linear_wgrad_dge(fake, 64, fake, 8, fake, 8, fake, 4, 8, 64, 0.0, 3.0, fake, 8, None) == 1
     assert L.fp4_quantize_cols(fake, 64, 12, 16, fake, 32, fake, fake, 1 << 10, None) == 2

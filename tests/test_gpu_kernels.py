@@ -255,8 +255,9 @@ def test_gemm_raw_exact_at_maximum_K(fp4, sign_pattern):
         assert float(Y[0, 0]) == 36.0 * K
 
 
+@pytest.mark.parametrize("workspace", ["auto", None])
 @pytest.mark.parametrize("M,N,K,q", [(256, 512, 512, 0.99), (300, 520, 1056, 0.97), (129, 264, 96, 0.9)])
-def test_linear_fwd_scaled_and_compensated(fp4, M, N, K, q):
+def test_linear_fwd_scaled_and_compensated(fp4, M, N, K, q, workspace):
     A_bits = _t3_bits(M, (M, K), 2.0)
     W_bits = _normal_bits(N, (K, N), 0.02)
     t, _, _ = orc.quantile_threshold(A_bits, q)
@@ -271,7 +272,7 @@ def test_linear_fwd_scaled_and_compensated(fp4, M, N, K, q):
     y_comp = orc.linear_fwd(a_codes, s_a, w_codes, s_w, rp, ci, cv, W_bits)
     y_plain = orc.linear_fwd(a_codes, s_a, w_codes, s_w)
     # BF16, compensated: 1 ulp plus the fp32 bound of the epilogue sum (cancellation)
-    yb = fp4.fp4_linear_fwd(*args, csr=csr, W=W, out_type="bf16")
+    yb = fp4.fp4_linear_fwd(*args, csr=csr, W=W, out_type="bf16", workspace=workspace)
     mag = orc.linear_fwd_magnitude(a_codes, s_a, w_codes, s_w, rp, ci, cv, W_bits)
     n_over = assert_bf16_compensated_close(host_bits(yb), y_comp, mag)
     assert n_over <= max(2, y_comp.size // 10000)
@@ -279,8 +280,49 @@ def test_linear_fwd_scaled_and_compensated(fp4, M, N, K, q):
     yb0 = fp4.fp4_linear_fwd(*args, out_type="bf16")
     assert bf16_ulp_distance(host_bits(yb0), orc.f64_to_bf16(y_plain)).max() <= BF16_ULP_TOL
     # fp32, compensated: relative Frobenius
-    yf = fp4.fp4_linear_fwd(*args, csr=csr, W=W, out_type="fp32")
+    yf = fp4.fp4_linear_fwd(*args, csr=csr, W=W, out_type="fp32", workspace=workspace)
     assert rel_frobenius(yf.cpu().numpy(), y_comp) <= FROB_TOL
+    assert_no_device_flags(fp4)
+
+
+def _hot_channel_bits(seed, M, K, n_hot, scale=20.0):
+    """N(0,1) activations with n_hot seeded channels multiplied by `scale` (outliers gather there)."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    hot = rng.choice(K, size=n_hot, replace=False)
+    x[:, hot] *= scale
+    return wl.f32_to_bf16_bits(x), np.sort(hot)
+
+
+@pytest.mark.parametrize("M,N,K,n_hot", [(256, 512, 512, 10), (300, 520, 1056, 100), (129, 264, 2048, 128),
+                                         (200, 240, 512, 129), (64, 16, 64, 1)])
+def test_linear_fwd_compensation_paths_agree(fp4, M, N, K, n_hot):
+    """dA confined to n_hot channels: up to 128 distinct columns run on the tensor
+    cores (TF32 parts, several 32-column chunks), 129 fall back to the epilogue;
+    both paths meet the compensated bound against the oracle."""
+    A_bits, hot = _hot_channel_bits(M + n_hot, M, K, n_hot)
+    W_bits = _normal_bits(N + K, (K, N), 0.02)
+    # every entry of a hot channel above the threshold, none elsewhere: keep 30% of the hot entries
+    q = 1.0 - 0.3 * n_hot / K
+    t, _, _ = orc.quantile_threshold(A_bits, q)
+    A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
+    assert set(np.unique(ci)) <= set(hot.tolist())
+    distinct = np.unique(ci).size
+    a_codes, s_a = orc.quantize_rows(A_c)
+    w_codes, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    csr = {"row_ptr": d(rp), "col_idx": d(ci), "vals": d(cv)}
+    W = dev_bf16(W_bits)
+    args = (d(a_codes), d(s_a), d(w_codes), d(s_w), K)
+    y_comp = orc.linear_fwd(a_codes, s_a, w_codes, s_w, rp, ci, cv, W_bits)
+    mag = orc.linear_fwd_magnitude(a_codes, s_a, w_codes, s_w, rp, ci, cv, W_bits)
+    for ws in ("auto", None):
+        yb = fp4.fp4_linear_fwd(*args, csr=csr, W=W, out_type="bf16", workspace=ws)
+        n_over = assert_bf16_compensated_close(host_bits(yb), y_comp, mag)
+        assert n_over <= max(2, y_comp.size // 10000)
+        yf = fp4.fp4_linear_fwd(*args, csr=csr, W=W, out_type="fp32", workspace=ws)
+        assert rel_frobenius(yf.cpu().numpy(), y_comp) <= FROB_TOL
+    assert distinct == n_hot or n_hot == 1
     assert_no_device_flags(fp4)
 
 
