@@ -411,7 +411,7 @@ def run_gpu(args):
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(args.workload, 4 * args.cpu_budget)   # about 10 s of one core
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
