@@ -50,12 +50,20 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
 
-template <int BN, int NACC>
+// PAIR: tiles of 256 x BN per CTA pair (a cluster of two CTAs on two SMs): each
+// CTA loads its 128 rows of A and half of the tile's BN rows of B per stage, the
+// leader CTA issues M = 256 tcgen05 MMAs (cta_group::2), and each CTA's TMEM
+// holds its 128 rows x BN columns of the accumulator.  Per SM a stage then
+// carries 31 KB instead of 46 KB for the same MMA work, which pays once the K
+// loop is long; short K loops run single-CTA 128 x BN tiles.
+template <int BN, int NACC, bool PAIR>
 struct FwdCfg {
+  static constexpr int kCtas = PAIR ? 2 : 1;
+  static constexpr int kBRows = BN / kCtas;             // rows of B per CTA
   static constexpr int kAStage = kBM * kBKBytes;
-  static constexpr int kBStage = BN * kBKBytes;
-  static constexpr int kStageBytes = kAStage + kBStage;
-  static constexpr int kStages = (196 * 1024) / kStageBytes;
+  static constexpr int kBStage = kBRows * kBKBytes;
+  static constexpr int kStageBytes = kAStage + kBStage;  // per CTA; the leader's barrier counts the pair's
+  static constexpr int kStages = PAIR ? 6 : 4;
   // scale-factor columns (all bytes 0x7F = 2^0) after the accumulators
   static constexpr uint32_t kSfaCol = ((NACC * BN + 15) / 16) * 16;
   static constexpr uint32_t kSfbCol = kSfaCol + 16;
@@ -70,13 +78,15 @@ struct FwdCfg {
   static_assert(kSfbCol + 16 <= kTmemCols, "accumulators and scale factors exceed TMEM");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "invalid N tile");
   static_assert(kStages >= 2, "too few pipeline stages");
+  static_assert(kBRows % 8 == 0, "B tile rows must be whole 8-row swizzle atoms");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget exceeded");
 };
 
 // Instruction descriptor, kind::mxf4: A and B E2M1 (format 1), both K-major,
-// UE8M0 scale type, M = 128, N = BN, dense K = 64, scale-factor ids 0.
-template <int BN>
+// UE8M0 scale type, M = 128 per CTA (256 for a pair), N = BN, dense K = 64, scale-factor ids 0.
+template <int BN, bool PAIR>
 __host__ __device__ constexpr uint32_t idesc_mxf4() {
-  return (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (1u << 23) | (uint32_t(kBM >> 4) << 24);
+  return (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (1u << 23) | (uint32_t((kBM * (PAIR ? 2 : 1)) >> 4) << 24);
 }
 
 constexpr int kHotMax = 128;    // distinct dA columns handled on the tensor cores
@@ -90,10 +100,10 @@ struct HotInfo {
   int pad;
 };
 
-// Instruction descriptor, kind::tf32: fp32 accumulator, A and B TF32, both K-major.
-template <int BN>
+// Instruction descriptor, kind::tf32: fp32 accumulator, A and B TF32, both K-major, M as for mxf4.
+template <int BN, bool PAIR>
 __host__ __device__ constexpr uint32_t idesc_tf32() {
-  return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+  return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t((kBM * (PAIR ? 2 : 1)) >> 4) << 24);
 }
 
 // Round an fp32 value to TF32 (10 explicit mantissa bits), nearest, ties to even.
@@ -246,6 +256,23 @@ __global__ void __launch_bounds__(256) hot_build_kernel(
   reinterpret_cast<float4*>(q_lo + int64_t(j) * kHotMax)[h0 / 4] = make_float4(b[0], b[1], b[2], b[3]);
 }
 
+// Single-CTA and CTA-pair forms of the pipeline operations.
+template <bool PAIR>
+__device__ __forceinline__ void fwd_tma(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x, int32_t y) {
+  if constexpr (PAIR) tma_load_2d_pair(dst, map, mapa_shared(bar, 0), x, y);   // counted on the leader's barrier
+  else tma_load_2d(dst, map, bar, x, y);
+}
+template <bool PAIR>
+__device__ __forceinline__ void fwd_commit(uint32_t bar, uint16_t mask) {
+  if constexpr (PAIR) tc_commit_pair(bar, mask);
+  else tc_commit(bar);
+}
+template <bool PAIR>
+__device__ __forceinline__ void fwd_sync() {
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
+}
+
 struct FwdParams {
   const float* s_a;
   const float* s_w;
@@ -263,13 +290,13 @@ struct FwdParams {
   uint64_t wait_ns;
 };
 
-template <int BN, int NACC>
+template <int BN, int NACC, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     fp4_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmPh,
                    const __grid_constant__ CUtensorMap tmPl, const __grid_constant__ CUtensorMap tmQh,
                    const __grid_constant__ CUtensorMap tmQl, const FwdParams p) {
-  using C = FwdCfg<BN, NACC>;
+  using C = FwdCfg<BN, NACC, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -284,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t acce0 = accf0 + 8 * NACC;
   const uint32_t done_bar = acce0 + 8 * NACC;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // 0: the CTA that issues the MMAs
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
@@ -295,23 +323,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmQh);
       prefetch_tmap(&tmQl);
     }
+    // full: the leader's counts both CTAs' bytes; empty / acc-full: one multicast
+    // commit each; acc-empty (the leader's): the epilogue warps of both CTAs
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int b = 0; b < NACC; ++b) {
       mbar_init(accf0 + 8 * b, 1);
-      mbar_init(acce0 + 8 * b, kEpiWarps);
+      mbar_init(acce0 + 8 * b, C::kCtas * kEpiWarps);
     }
     mbar_init(done_bar, 1);
-    fence_mbar_init();
+    if constexpr (PAIR) fence_mbar_init_cluster();
+    else fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  fwd_sync<PAIR>();   // (pair) both CTAs' barriers exist before either CTA signals the other
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -324,12 +360,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_wait_st();
   }
   tc_fence_before();
-  __syncthreads();
+  fwd_sync<PAIR>();   // (pair) the leader's first MMA reads both CTAs' scale-factor columns
   tc_fence_after();
 
-  const int num_m = (p.M + kBM - 1) / kBM;
+  constexpr int kTileM = kBM * C::kCtas;   // rows of A per tile (per pair)
+  const int num_m = (p.M + kTileM - 1) / kTileM;
   const int num_n = (p.N + BN - 1) / BN;
   const int tiles = num_m * num_n;
+  const int pair_id = int(blockIdx.x) / C::kCtas, npairs = int(gridDim.x) / C::kCtas;
   const int kblocks = (p.K / 2 + kBKBytes - 1) / kBKBytes;
   // tensor-core compensation: 3 stages (hi*hi, hi*lo, lo*hi) per 32 columns of H
   const bool hot = p.hot != nullptr && p.hot->mode != 0;
@@ -342,29 +380,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     uint32_t issued = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+    for (int tile = pair_id; tile < tiles && ok; tile += npairs) {
       const int mb = tile % num_m, nb = tile / num_m;
+      const int arow = mb * kTileM + int(rank) * kBM;           // this CTA's 128 rows of A
+      const int brow = nb * BN + int(rank) * C::kBRows;         // this CTA's part of the tile's B rows
       for (int kb = 0; kb < nstages; ++kb) {
         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
           ok = false;
           break;
         }
         if (lane == 0) {
+          // completion is counted on the MMA-issuing CTA's full barrier
           const uint32_t fb = full0 + 8 * stage;
-          mbar_arrive_expect_tx(fb, C::kStageBytes);
+          if (rank == 0) mbar_arrive_expect_tx(fb, C::kCtas * C::kStageBytes);
+          const uint32_t da = smem_u32(sA + stage * C::kAStage), db = smem_u32(sB + stage * C::kBStage);
           if (kb < kblocks) {
-            tma_load_2d(smem_u32(sA + stage * C::kAStage), &tmA, fb, kb * kBKBytes, mb * kBM);
-            tma_load_2d(smem_u32(sB + stage * C::kBStage), &tmB, fb, kb * kBKBytes, nb * BN);
+            fwd_tma<PAIR>(da, &tmA, fb, kb * kBKBytes, arow);
+            fwd_tma<PAIR>(db, &tmB, fb, kb * kBKBytes, brow);
           } else {
             // 32 columns of H: P part x Q part, pairs (hi, hi), (hi, lo), (lo, hi);
             // every load names its tensor map directly
             const int hs = kb - kblocks, chunk = hs / 3, pair = hs - 3 * chunk;
-            const uint32_t da = smem_u32(sA + stage * C::kAStage), db = smem_u32(sB + stage * C::kBStage);
             const int x = chunk * kHotChunk;
-            if (pair == 2) tma_load_2d(da, &tmPl, fb, x, mb * kBM);
-            else tma_load_2d(da, &tmPh, fb, x, mb * kBM);
-            if (pair == 1) tma_load_2d(db, &tmQl, fb, x, nb * BN);
-            else tma_load_2d(db, &tmQh, fb, x, nb * BN);
+            if (pair == 2) fwd_tma<PAIR>(da, &tmPl, fb, x, arow);
+            else fwd_tma<PAIR>(da, &tmPh, fb, x, arow);
+            if (pair == 1) fwd_tma<PAIR>(db, &tmQl, fb, x, brow);
+            else fwd_tma<PAIR>(db, &tmQh, fb, x, brow);
           }
         }
         __syncwarp();
@@ -376,23 +417,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
-    // wait for the last load armed on every stage before the CTA may exit
+    // every stage this CTA filled has been released by the pair's MMAs (so its
+    // loads have landed and no commit is still on its way) before the CTA may exit
     for (int s = 0; s < C::kStages; ++s) {
       const uint32_t n_s = issued / C::kStages + (uint32_t(s) < issued % C::kStages ? 1u : 0u);
-      if (n_s > 0 && !mbar_wait(full0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
+      if (n_s > 0 && !mbar_wait(empty0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
         atomicOr(p.status, FP4_FLAG_TIMEOUT);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
+  } else if (warp == 1 && rank == 0) {
+    // ------------------------------------------------ MMA issuer (leader CTA)
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    constexpr uint32_t idesc = idesc_mxf4<BN>();
+    constexpr uint32_t idesc = idesc_mxf4<BN, PAIR>();
     const uint32_t sfa = tmem + C::kSfaCol, sfb = tmem + C::kSfbCol;
     const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+    for (int tile = pair_id; tile < tiles && ok; tile += npairs) {
       if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
         ok = false;
         break;
@@ -413,17 +455,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < kBKBytes / kMmaKBytes; ++k) {
               const uint64_t ad = smem_desc_sw128(a0 + k * kMmaKBytes, 16, 1024);
               const uint64_t bd = smem_desc_sw128(b0 + k * kMmaKBytes, 16, 1024);
-              mma_mxf4(d_tmem, ad, bd, idesc, sfa, sfb, (kb | k) != 0 ? 1u : 0u);
+              if constexpr (PAIR) mma_mxf4_pair(d_tmem, ad, bd, idesc, sfa, sfb, (kb | k) != 0 ? 1u : 0u);
+              else mma_mxf4(d_tmem, ad, bd, idesc, sfa, sfb, (kb | k) != 0 ? 1u : 0u);
             }
           } else {
 #pragma unroll
             for (int k = 0; k < kBKBytes / kMmaKBytes; ++k) {
               const uint64_t ad = smem_desc_sw128(a0 + k * kMmaKBytes, 16, 1024);
               const uint64_t bd = smem_desc_sw128(b0 + k * kMmaKBytes, 16, 1024);
-              mma_tf32(d_tmem, ad, bd, idesc_tf32<BN>(), 1u);
+              if constexpr (PAIR) mma_tf32_pair(d_tmem, ad, bd, idesc_tf32<BN, PAIR>(), 1u);
+              else mma_tf32(d_tmem, ad, bd, idesc_tf32<BN, PAIR>(), 1u);
             }
           }
-          tc_commit(empty0 + 8 * stage);
+          fwd_commit<PAIR>(empty0 + 8 * stage, 0x3);   // the stage is free (in both CTAs of a pair)
         }
         __syncwarp();
         if (++stage == C::kStages) {
@@ -432,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(accf0 + 8 * acc);
+      if (lane == 0) fwd_commit<PAIR>(accf0 + 8 * acc, 0x3);   // the accumulator(s) are ready
       __syncwarp();
       if (++acc == NACC) {
         acc = 0;
@@ -441,11 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
     // every MMA issued by this thread must finish before TMEM is released
-    if (lane == 0) tc_commit(done_bar);
+    if (lane == 0) fwd_commit<PAIR>(done_bar, 0x1);
     __syncwarp();
     if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
-  } else {
-    // ------------------------------------------------ epilogue
+  } else if (warp >= 2) {
+    // ------------------------------------------------ epilogue (both CTAs, own 128 rows)
     constexpr int EC = C::kEpiCols;
     const int q = warp & 3;
     const int c_base = ((warp - 2) / 4) * EC;
@@ -457,8 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     const bool raw = (p.y_type == FP4_OUT_RAW_ACC_FP32);
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    for (int tile = pair_id; tile < tiles; tile += npairs) {
       const int mb = tile % num_m, nb = tile / num_m;
+      const int mrow0 = mb * kTileM + int(rank) * kBM;   // first row of this CTA's rows of the tile
       // this warp's column scales 1/s_W in its own shared-memory slice (no
       // cross-warp barrier, so a warp that gives up on a wait cannot strand others)
       __syncwarp();
@@ -467,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         inv_sw_w[c] = (!raw && col < p.N) ? 1.0f / __ldg(p.s_w + col) : 1.0f;
       }
       __syncwarp();
-      const int row = mb * kBM + r_local;
+      const int row = mrow0 + r_local;
       const bool row_ok = row < p.M;
       float inv_sa = 1.0f;
       int e0 = 0, e1 = 0;
@@ -544,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // store, which writes whole rows and drops what falls outside M x N:
       // 40 columns per pass, as one BF16 store or two fp32 stores of 20 columns.
       const bool bf16_out = (p.y_type == FP4_OUT_BF16);
-      const int row0 = mb * kBM + q * 32;
+      const int row0 = mrow0 + q * 32;
       uint8_t* orow = out_s + lane * C::kOutRowBytes;
 #pragma unroll
       for (int pc = 0; pc < EC; pc += 40) {
@@ -597,7 +642,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce0 + 8 * acc);   // TMEM buffer free for the next tile
+      if (lane == 0) {   // TMEM buffer free for the next tile (the issuing CTA's barrier)
+        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(acce0 + 8 * acc, 0));
+        else mbar_arrive(acce0 + 8 * acc);
+      }
       if (++acc == NACC) {
         acc = 0;
         acc_phase ^= 1u;
@@ -607,10 +655,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   }
 
-  __syncthreads();
+  // (pair) neither CTA leaves or frees TMEM while its partner may still signal it
+  __syncwarp();
+  tc_fence_before();
+  fwd_sync<PAIR>();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, kTmemCols);
+    else tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -660,13 +712,68 @@ FP4_API size_t fp4_linear_fwd_workspace(int64_t M, int64_t N, int64_t K) {
   return fp4::hot_layout(M, N, K).total;
 }
 
+namespace fp4 {
+namespace {
+// Encodes the B-side tensor maps for the tile shape of PAIR and launches the GEMM
+// (as clusters of two CTAs for PAIR), persistent over the tiles.
+template <bool PAIR>
+fp4_status launch_fwd(const CUtensorMap& tmA, const CUtensorMap& tmY, const uint8_t* w_codes_t, int64_t ldw_codes_bytes,
+                      const float* q_hi, const float* q_lo, const float* p_hi, const float* p_lo, FwdParams p, int sms,
+                      cudaStream_t cs) {
+  using C = FwdCfg<kFwdBN, kFwdAcc, PAIR>;
+  fp4_status st;
+  CUtensorMap tmB, tmPh = tmA, tmPl = tmA, tmQh = tmA, tmQl = tmA;   // compensation maps unused without p.hot
+  if ((st = encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_codes_t, uint64_t(p.K / 2), uint64_t(p.N),
+                           uint64_t(ldw_codes_bytes), kBKBytes, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK)
+    return st;
+  if (p.hot) {
+    const uint32_t row_bytes = kHotMax * 4;
+    if ((st = encode_tmap_2d(&tmPh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p_hi, kHotMax, uint64_t(p.M), row_bytes,
+                             kHotChunk, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
+        (st = encode_tmap_2d(&tmPl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p_lo, kHotMax, uint64_t(p.M), row_bytes,
+                             kHotChunk, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
+        (st = encode_tmap_2d(&tmQh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q_hi, kHotMax, uint64_t(p.N), row_bytes,
+                             kHotChunk, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
+        (st = encode_tmap_2d(&tmQl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q_lo, kHotMax, uint64_t(p.N), row_bytes,
+                             kHotChunk, C::kBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK)
+      return st;
+  }
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto kern = fp4_fwd_kernel<kFwdBN, kFwdAcc, PAIR>;
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+      return FP4_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  const int64_t tiles = ((p.M + kBM * C::kCtas - 1) / (kBM * C::kCtas)) * ((p.N + kFwdBN - 1) / kFwdBN);
+  const int64_t units = sms / C::kCtas;
+  const int grid = int(C::kCtas * (tiles < units ? tiles : units));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = cs;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(C::kCtas);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmY, tmPh, tmPl, tmQh, tmQl, p) != cudaSuccess) return launch_status();
+  return launch_status();
+}
+}  // namespace
+}  // namespace fp4
+
 FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_bytes, const float* s_a,
                                   const uint8_t* w_codes_t, int64_t ldw_codes_bytes, const float* s_w, int64_t M,
                                   int64_t N, int64_t K, const int32_t* dA_row_ptr, const int32_t* dA_col,
                                   const float* dA_val, const void* W, int64_t ldw, void* Y, int y_type, int64_t ldy,
                                   void* workspace, size_t ws_bytes, fp4_stream_t stream) {
   using namespace fp4;
-  using C = FwdCfg<kFwdBN, kFwdAcc>;
   if (!a_codes || !w_codes_t || !Y) return FP4_ERR_INVALID_ARG;
   if (y_type != FP4_OUT_BF16 && y_type != FP4_OUT_FP32 && y_type != FP4_OUT_RAW_ACC_FP32) return FP4_ERR_INVALID_ARG;
   const bool raw = (y_type == FP4_OUT_RAW_ACC_FP32);
@@ -691,12 +798,9 @@ FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_byte
   if (st != FP4_OK) return st;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
 
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA;
   st = encode_tmap_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, uint64_t(K / 2), uint64_t(M),
                       uint64_t(lda_codes_bytes), kBKBytes, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != FP4_OK) return st;
-  st = encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_codes_t, uint64_t(K / 2), uint64_t(N),
-                      uint64_t(ldw_codes_bytes), kBKBytes, kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != FP4_OK) return st;
 
   CUtensorMap tmY;
@@ -708,18 +812,18 @@ FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_byte
 
   // tensor-core compensation: prep kernels fill the workspace; the GEMM reads
   // HotInfo to learn whether (and over how many columns) to run the TF32 stages
-  CUtensorMap tmPh = tmA, tmPl = tmA, tmQh = tmA, tmQl = tmA;   // unused unless use_hot
   const HotInfo* hot_info = nullptr;
+  float *p_hi = nullptr, *p_lo = nullptr, *q_hi = nullptr, *q_lo = nullptr;
   if (use_hot) {
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     HotInfo* info = reinterpret_cast<HotInfo*>(ws + L.info);
     uint32_t* bitmap = reinterpret_cast<uint32_t*>(ws + L.bitmap);
     uint32_t* prefix = reinterpret_cast<uint32_t*>(ws + L.prefix);
     int32_t* hlist = reinterpret_cast<int32_t*>(ws + L.hlist);
-    float* p_hi = reinterpret_cast<float*>(ws + L.p_hi);
-    float* p_lo = reinterpret_cast<float*>(ws + L.p_lo);
-    float* q_hi = reinterpret_cast<float*>(ws + L.q_hi);
-    float* q_lo = reinterpret_cast<float*>(ws + L.q_lo);
+    p_hi = reinterpret_cast<float*>(ws + L.p_hi);
+    p_lo = reinterpret_cast<float*>(ws + L.p_lo);
+    q_hi = reinterpret_cast<float*>(ws + L.q_hi);
+    q_lo = reinterpret_cast<float*>(ws + L.q_lo);
     const int nwords = int(K / 32);
     uint32_t* done = bitmap + nwords;
     if (cudaMemsetAsync(bitmap, 0, size_t(nwords) * 4 + 4, cs) != cudaSuccess) return launch_status();
@@ -732,28 +836,9 @@ FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_byte
                                                      int(M), int(N), int(K), p_ctas);
     st = launch_status();
     if (st != FP4_OK) return st;
-    const uint32_t row_bytes = kHotMax * 4;
-    if ((st = encode_tmap_2d(&tmPh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p_hi, kHotMax, uint64_t(M), row_bytes, kHotChunk,
-                             kBM, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
-        (st = encode_tmap_2d(&tmPl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p_lo, kHotMax, uint64_t(M), row_bytes, kHotChunk,
-                             kBM, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
-        (st = encode_tmap_2d(&tmQh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q_hi, kHotMax, uint64_t(N), row_bytes, kHotChunk,
-                             kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
-        (st = encode_tmap_2d(&tmQl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q_lo, kHotMax, uint64_t(N), row_bytes, kHotChunk,
-                             kFwdBN, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK)
-      return st;
     hot_info = info;
   }
 
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  auto kern = fp4_fwd_kernel<kFwdBN, kFwdAcc>;
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
-      return FP4_ERR_CUDA;
-    attr_set[dev] = true;
-  }
   FwdParams p;
   p.s_a = s_a;
   p.s_w = s_w;
@@ -771,8 +856,8 @@ FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_byte
   p.hot = hot_info;
   p.status = status_word();
   p.wait_ns = kWaitLimitNs;
-  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kFwdBN - 1) / kFwdBN);
-  const int grid = int(tiles < sms ? tiles : sms);
-  kern<<<grid, kThreads, C::kSmemBytes, cs>>>(tmA, tmB, tmY, tmPh, tmPl, tmQh, tmQl, p);
-  return launch_status();
+  // CTA pairs once the K loop is long enough (16 FP4 stages, K >= 4096) for the
+  // pair's lighter stages to outweigh its shared accumulator hand-off
+  if (K >= 4096) return launch_fwd<true>(tmA, tmY, w_codes_t, ldw_codes_bytes, q_hi, q_lo, p_hi, p_lo, p, sms, cs);
+  return launch_fwd<false>(tmA, tmY, w_codes_t, ldw_codes_bytes, q_hi, q_lo, p_hi, p_lo, p, sms, cs);
 }

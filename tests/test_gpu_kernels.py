@@ -295,11 +295,13 @@ def _hot_channel_bits(seed, M, K, n_hot, scale=20.0):
 
 
 @pytest.mark.parametrize("M,N,K,n_hot", [(256, 512, 512, 10), (300, 520, 1056, 100), (129, 264, 2048, 128),
-                                         (200, 240, 512, 129), (64, 16, 64, 1)])
+                                         (200, 240, 512, 129), (64, 16, 64, 1), (300, 520, 4096, 100),
+                                         (100, 248, 4096, 7)])
 def test_linear_fwd_compensation_paths_agree(fp4, M, N, K, n_hot):
     """dA confined to n_hot channels: up to 128 distinct columns run on the tensor
     cores (TF32 parts, several 32-column chunks), 129 fall back to the epilogue;
-    both paths meet the compensated bound against the oracle."""
+    both paths meet the compensated bound against the oracle.  K >= 4096 runs the
+    GEMM as CTA pairs (256-row tiles; M = 100 and 300 leave partial pair tiles)."""
     A_bits, hot = _hot_channel_bits(M + n_hot, M, K, n_hot)
     W_bits = _normal_bits(N + K, (K, N), 0.02)
     # every entry of a hot channel above the threshold, none elsewhere: keep 30% of the hot entries
