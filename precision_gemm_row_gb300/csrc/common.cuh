@@ -259,6 +259,58 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t cta_mask) 
       : "memory");
 }
 
+__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Single-CTA (PAIR = false) and CTA-pair forms of the pipeline operations.
+// TMA load whose completion is counted on `bar` of the MMA-issuing CTA (rank 0).
+template <bool PAIR>
+__device__ __forceinline__ void tma_load_2d_to(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                                               int32_t y) {
+  if constexpr (PAIR) tma_load_2d_pair(dst, map, mapa_shared(bar, 0), x, y);
+  else tma_load_2d(dst, map, bar, x, y);
+}
+// Commit of the issued MMAs to `bar` (in the CTAs of `mask`, for a pair).
+template <bool PAIR>
+__device__ __forceinline__ void commit_to(uint32_t bar, uint16_t mask) {
+  if constexpr (PAIR) tc_commit_pair(bar, mask);
+  else tc_commit(bar);
+}
+// Arrive on `bar` of the MMA-issuing CTA (rank 0).
+template <bool PAIR>
+__device__ __forceinline__ void arrive_on_issuer(uint32_t bar) {
+  if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(bar, 0));
+  else mbar_arrive(bar);
+}
+// Block barrier, or cluster barrier for a pair.
+template <bool PAIR>
+__device__ __forceinline__ void cta_sync() {
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
+}
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc_for(uint32_t dst_smem, uint32_t ncols) {
+  if constexpr (PAIR) {
+    tmem_alloc_pair(dst_smem, ncols);
+    tmem_relinquish_pair();
+  } else {
+    tmem_alloc(dst_smem, ncols);
+    tmem_relinquish();
+  }
+}
+template <bool PAIR>
+__device__ __forceinline__ void tmem_dealloc_for(uint32_t taddr, uint32_t ncols) {
+  if constexpr (PAIR) tmem_dealloc_pair(taddr, ncols);
+  else tmem_dealloc(taddr, ncols);
+}
+
 // Each thread of the warp reads 16 consecutive 32-bit columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(

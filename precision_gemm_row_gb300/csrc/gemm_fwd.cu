@@ -256,23 +256,6 @@ __global__ void __launch_bounds__(256) hot_build_kernel(
   reinterpret_cast<float4*>(q_lo + int64_t(j) * kHotMax)[h0 / 4] = make_float4(b[0], b[1], b[2], b[3]);
 }
 
-// Single-CTA and CTA-pair forms of the pipeline operations.
-template <bool PAIR>
-__device__ __forceinline__ void fwd_tma(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x, int32_t y) {
-  if constexpr (PAIR) tma_load_2d_pair(dst, map, mapa_shared(bar, 0), x, y);   // counted on the leader's barrier
-  else tma_load_2d(dst, map, bar, x, y);
-}
-template <bool PAIR>
-__device__ __forceinline__ void fwd_commit(uint32_t bar, uint16_t mask) {
-  if constexpr (PAIR) tc_commit_pair(bar, mask);
-  else tc_commit(bar);
-}
-template <bool PAIR>
-__device__ __forceinline__ void fwd_sync() {
-  if constexpr (PAIR) cluster_sync();
-  else __syncthreads();
-}
-
 struct FwdParams {
   const float* s_a;
   const float* s_w;
@@ -337,17 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (PAIR) fence_mbar_init_cluster();
     else fence_mbar_init();
   }
-  if (warp == 1) {
-    if constexpr (PAIR) {
-      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-      tmem_relinquish();
-    }
-  }
+  if (warp == 1) tmem_alloc_for<PAIR>(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
-  fwd_sync<PAIR>();   // (pair) both CTAs' barriers exist before either CTA signals the other
+  cta_sync<PAIR>();   // (pair) both CTAs' barriers exist before either CTA signals the other
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -360,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_wait_st();
   }
   tc_fence_before();
-  fwd_sync<PAIR>();   // (pair) the leader's first MMA reads both CTAs' scale-factor columns
+  cta_sync<PAIR>();   // (pair) the leader's first MMA reads both CTAs' scale-factor columns
   tc_fence_after();
 
   constexpr int kTileM = kBM * C::kCtas;   // rows of A per tile (per pair)
@@ -395,17 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rank == 0) mbar_arrive_expect_tx(fb, C::kCtas * C::kStageBytes);
           const uint32_t da = smem_u32(sA + stage * C::kAStage), db = smem_u32(sB + stage * C::kBStage);
           if (kb < kblocks) {
-            fwd_tma<PAIR>(da, &tmA, fb, kb * kBKBytes, arow);
-            fwd_tma<PAIR>(db, &tmB, fb, kb * kBKBytes, brow);
+            tma_load_2d_to<PAIR>(da, &tmA, fb, kb * kBKBytes, arow);
+            tma_load_2d_to<PAIR>(db, &tmB, fb, kb * kBKBytes, brow);
           } else {
             // 32 columns of H: P part x Q part, pairs (hi, hi), (hi, lo), (lo, hi);
             // every load names its tensor map directly
             const int hs = kb - kblocks, chunk = hs / 3, pair = hs - 3 * chunk;
             const int x = chunk * kHotChunk;
-            if (pair == 2) fwd_tma<PAIR>(da, &tmPl, fb, x, arow);
-            else fwd_tma<PAIR>(da, &tmPh, fb, x, arow);
-            if (pair == 1) fwd_tma<PAIR>(db, &tmQl, fb, x, brow);
-            else fwd_tma<PAIR>(db, &tmQh, fb, x, brow);
+            if (pair == 2) tma_load_2d_to<PAIR>(da, &tmPl, fb, x, arow);
+            else tma_load_2d_to<PAIR>(da, &tmPh, fb, x, arow);
+            if (pair == 1) tma_load_2d_to<PAIR>(db, &tmQl, fb, x, brow);
+            else tma_load_2d_to<PAIR>(db, &tmQh, fb, x, brow);
           }
         }
         __syncwarp();
@@ -467,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               else mma_tf32(d_tmem, ad, bd, idesc_tf32<BN, PAIR>(), 1u);
             }
           }
-          fwd_commit<PAIR>(empty0 + 8 * stage, 0x3);   // the stage is free (in both CTAs of a pair)
+          commit_to<PAIR>(empty0 + 8 * stage, 0x3);   // the stage is free (in both CTAs of a pair)
         }
         __syncwarp();
         if (++stage == C::kStages) {
@@ -476,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) fwd_commit<PAIR>(accf0 + 8 * acc, 0x3);   // the accumulator(s) are ready
+      if (lane == 0) commit_to<PAIR>(accf0 + 8 * acc, 0x3);   // the accumulator(s) are ready
       __syncwarp();
       if (++acc == NACC) {
         acc = 0;
@@ -485,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
     // every MMA issued by this thread must finish before TMEM is released
-    if (lane == 0) fwd_commit<PAIR>(done_bar, 0x1);
+    if (lane == 0) commit_to<PAIR>(done_bar, 0x1);
     __syncwarp();
     if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   } else if (warp >= 2) {
@@ -642,10 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {   // TMEM buffer free for the next tile (the issuing CTA's barrier)
-        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(acce0 + 8 * acc, 0));
-        else mbar_arrive(acce0 + 8 * acc);
-      }
+      if (lane == 0) arrive_on_issuer<PAIR>(acce0 + 8 * acc);   // TMEM buffer free for the next tile
       if (++acc == NACC) {
         acc = 0;
         acc_phase ^= 1u;
@@ -658,11 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (pair) neither CTA leaves or frees TMEM while its partner may still signal it
   __syncwarp();
   tc_fence_before();
-  fwd_sync<PAIR>();
+  cta_sync<PAIR>();
   if (warp == 1) {
     tc_fence_after();
-    if constexpr (PAIR) tmem_dealloc_pair(tmem, kTmemCols);
-    else tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_for<PAIR>(tmem, kTmemCols);
   }
 }
 

@@ -51,22 +51,33 @@ constexpr int kBlk = 32;                         // epilogue block: 32 rows x 32
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 64;                          // features per TMA box (128 bytes of BF16)
 constexpr int kBoxBytes = kBox * kBT * 2;         // 8 KB
-constexpr int kAStage = (kBM / kBox) * kBoxBytes; // 16 KB
-constexpr int kBStage = (kBN / kBox) * kBoxBytes; // 32 KB
-constexpr int kStageBytes = kAStage + kBStage;
-constexpr int kStages = 4;
 // epilogue staging per warp: one dW block of 32 x 32 fp32 (128-byte swizzle),
 // written out with coalesced stores (TMA stays free for the main loop's stages)
 constexpr int kOutBytes = kBlk * kBlk * 4;        // 4 KB
 constexpr int kEpiWarpBytes = kOutBytes;
-constexpr int kDataBytes = kStages * kStageBytes + kEpiWarps * kEpiWarpBytes;
-constexpr int kNumBars = 2 * kStages + 2 * kNAcc + 1;
-constexpr int kSmemBytes = 1024 + kDataBytes + 8 * kNumBars + 16;
 
-// Instruction descriptor, kind::f16: fp32 accumulator, A and B BF16, both
-// MN-major, N = 256, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
-                            (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+// PAIR: tiles of 256 x 256 per CTA pair (a cluster of two CTAs on two SMs): each
+// CTA loads its 128 dW rows of A and 128 of the tile's 256 dY columns per stage
+// (32 KB instead of 48 KB for the same MMA work), the leader issues M = 256
+// tcgen05 MMAs (cta_group::2), and each CTA's TMEM holds its 128 rows x 256
+// columns.  Short token loops run single-CTA 128 x 256 tiles.
+template <bool PAIR>
+struct WgCfg {
+  static constexpr int kCtas = PAIR ? 2 : 1;
+  static constexpr int kBCols = kBN / kCtas;                  // dY columns per CTA
+  static constexpr int kAStage = (kBM / kBox) * kBoxBytes;    // 16 KB
+  static constexpr int kBStage = (kBCols / kBox) * kBoxBytes; // 16 or 32 KB
+  static constexpr int kStageBytes = kAStage + kBStage;
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kDataBytes = kStages * kStageBytes + kEpiWarps * kEpiWarpBytes;
+  static constexpr int kNumBars = 2 * kStages + 2 * kNAcc + 1;
+  static constexpr int kSmemBytes = 1024 + kDataBytes + 8 * kNumBars + 16;
+  // Instruction descriptor, kind::f16: fp32 accumulator, A and B BF16, both
+  // MN-major, N = 256, M = 128 per CTA.
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
+                                     (uint32_t(kBN >> 3) << 17) | (uint32_t((kBM * kCtas) >> 4) << 24);
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget exceeded");
+};
 
 struct WgradParams {
   const uint16_t* W;
@@ -95,22 +106,26 @@ __device__ __forceinline__ float dge_factor(float x, float inv_k, float expo, fl
   return x < 6.0f ? f : inv_k;
 }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     wgrad_dge_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
                      const WgradParams p) {
+  using C = WgCfg<PAIR>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kAStage;
-  uint8_t* sEpi = smem + kStages * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDataBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  uint8_t* sB = smem + kStages * C::kAStage;
+  uint8_t* sEpi = smem + kStages * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kDataBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kStages;
   const uint32_t accf0 = empty0 + 8 * kStages;
   const uint32_t acce0 = accf0 + 8 * kNAcc;
   const uint32_t done_bar = acce0 + 8 * kNAcc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;   // 0: the CTA that issues the MMAs
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
@@ -121,24 +136,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < kNAcc; ++b) {
       mbar_init(accf0 + 8 * b, 1);
-      mbar_init(acce0 + 8 * b, kEpiWarps);
+      mbar_init(acce0 + 8 * b, C::kCtas * kEpiWarps);
     }
     mbar_init(done_bar, 1);
-    fence_mbar_init();
+    if constexpr (PAIR) fence_mbar_init_cluster();
+    else fence_mbar_init();
   }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
-  }
+  if (warp == 1) tmem_alloc_for<PAIR>(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
-  __syncthreads();
+  cta_sync<PAIR>();   // (pair) both CTAs' barriers exist before either CTA signals the other
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int num_r = (p.K + kBM - 1) / kBM;
+  constexpr int kTileR = kBM * C::kCtas;   // dW rows per tile (per pair)
+  const int num_r = (p.K + kTileR - 1) / kTileR;
   const int num_n = (p.N + kBN - 1) / kBN;
   const int tiles = num_r * num_n;
   const int tblocks = (p.M + kBT - 1) / kBT;
+  const int pair_id = int(blockIdx.x) / C::kCtas, npairs = int(gridDim.x) / C::kCtas;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -146,22 +161,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     uint32_t issued = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+    for (int tile = pair_id; tile < tiles && ok; tile += npairs) {
       const int rb = tile % num_r, nb = tile / num_r;
+      const int arow = rb * kTileR + int(rank) * kBM;          // this CTA's 128 dW rows (A features)
+      const int bcol = nb * kBN + int(rank) * C::kBCols;       // this CTA's dY columns of the tile
       for (int tb = 0; tb < tblocks; ++tb) {
         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
           ok = false;
           break;
         }
         if (lane == 0) {
+          // completion is counted on the MMA-issuing CTA's full barrier
           const uint32_t fb = full0 + 8 * stage;
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          const uint32_t a_dst = smem_u32(sA + stage * kAStage);
-          const uint32_t b_dst = smem_u32(sB + stage * kBStage);
+          if (rank == 0) mbar_arrive_expect_tx(fb, C::kCtas * C::kStageBytes);
+          const uint32_t a_dst = smem_u32(sA + stage * C::kAStage);
+          const uint32_t b_dst = smem_u32(sB + stage * C::kBStage);
 #pragma unroll
-          for (int h = 0; h < kBM / kBox; ++h) tma_load_2d(a_dst + h * kBoxBytes, &tmA, fb, rb * kBM + h * kBox, tb * kBT);
+          for (int h = 0; h < kBM / kBox; ++h) tma_load_2d_to<PAIR>(a_dst + h * kBoxBytes, &tmA, fb, arow + h * kBox, tb * kBT);
 #pragma unroll
-          for (int h = 0; h < kBN / kBox; ++h) tma_load_2d(b_dst + h * kBoxBytes, &tmG, fb, nb * kBN + h * kBox, tb * kBT);
+          for (int h = 0; h < C::kBCols / kBox; ++h) tma_load_2d_to<PAIR>(b_dst + h * kBoxBytes, &tmG, fb, bcol + h * kBox, tb * kBT);
         }
         __syncwarp();
         ++issued;
@@ -172,20 +190,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    // every stage this CTA filled has been released by the MMAs (so its loads
+    // have landed and no commit is still on its way) before the CTA may exit
     for (int s = 0; s < kStages; ++s) {
       const uint32_t n_s = issued / kStages + (uint32_t(s) < issued % kStages ? 1u : 0u);
-      if (n_s > 0 && !mbar_wait(full0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
+      if (n_s > 0 && !mbar_wait(empty0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
         atomicOr(p.status, FP4_FLAG_TIMEOUT);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
+  } else if (warp == 1 && rank == 0) {
+    // ------------------------------------------------ MMA issuer (the pair's leader)
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+    for (int tile = pair_id; tile < tiles && ok; tile += npairs) {
       for (int tb0 = 0; tb0 < tblocks && ok; tb0 += kChunkStages) {
         const int tb1 = tb0 + kChunkStages < tblocks ? tb0 + kChunkStages : tblocks;
         if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
@@ -201,16 +221,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t a0 = a_base + stage * kAStage, b0 = b_base + stage * kBStage;
+            const uint32_t a0 = a_base + stage * C::kAStage, b0 = b_base + stage * C::kBStage;
 #pragma unroll
             for (int k = 0; k < kBT / kMmaT; ++k) {
               // MN-major, 128-byte swizzle: 64-feature atoms kBoxBytes apart (LBO),
               // 8-token groups 1024 bytes apart (SBO); 16 tokens = 2048 bytes per MMA.
               const uint64_t ad = smem_desc_sw128(a0 + k * (kMmaT * 128), kBoxBytes, 1024);
               const uint64_t bd = smem_desc_sw128(b0 + k * (kMmaT * 128), kBoxBytes, 1024);
-              mma_f16(d_tmem, ad, bd, kIdesc, (tb != tb0 || k != 0) ? 1u : 0u);
+              if constexpr (PAIR) mma_f16_pair(d_tmem, ad, bd, C::kIdesc, (tb != tb0 || k != 0) ? 1u : 0u);
+              else mma_f16(d_tmem, ad, bd, C::kIdesc, (tb != tb0 || k != 0) ? 1u : 0u);
             }
-            tc_commit(empty0 + 8 * stage);
+            commit_to<PAIR>(empty0 + 8 * stage, 0x3);   // the stage is free (in both CTAs of a pair)
           }
           __syncwarp();
           if (++stage == kStages) {
@@ -219,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        if (lane == 0) tc_commit(accf0 + 8 * acc);
+        if (lane == 0) commit_to<PAIR>(accf0 + 8 * acc, 0x3);   // the chunk's accumulator(s) are ready
         __syncwarp();
         if (++acc == kNAcc) {
           acc = 0;
@@ -228,11 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
-    if (lane == 0) tc_commit(done_bar);
+    if (lane == 0) commit_to<PAIR>(done_bar, 0x1);
     __syncwarp();
     if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
-  } else {
-    // ------------------------------------------------ chunk promotion + DGE epilogue
+  } else if (warp >= 2) {
+    // ------------------------------------------------ chunk promotion + DGE epilogue (own 128 rows)
     const int ew = warp - 2;
     const int q = warp & 3;
     const int c_base = (ew / 4) * kEpiCols;
@@ -242,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     constexpr int kNBlk = kEpiCols / kBlk;
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+    for (int tile = pair_id; tile < tiles && ok; tile += npairs) {
       const int rb = tile % num_r, nb = tile / num_r;
-      const int row0 = rb * kBM + q * 32;  // first dW row of this warp's 32-row slab
+      const int row0 = rb * kTileR + int(rank) * kBM + q * 32;  // first dW row of this warp's 32-row slab
       // (1) While the tile's first chunks run on the tensor core, this warp
       // writes the DGE factors f'(|W s_W|) of its 32 x 128 slab into dW; the
       // final pass multiplies them by the gradient in place.  Each block goes
@@ -324,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+        if (lane == 0) arrive_on_issuer<PAIR>(acce0 + 8 * acc);
         if (++acc == kNAcc) {
           acc = 0;
           acc_phase ^= 1u;
@@ -371,13 +392,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   }
 
-  __syncthreads();
+  // (pair) neither CTA leaves or frees TMEM while its partner may still signal it
+  __syncwarp();
+  tc_fence_before();
+  cta_sync<PAIR>();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_for<PAIR>(tmem, kTmemCols);
   }
 }
 
+}  // namespace
+}  // namespace fp4
+
+namespace fp4 {
+namespace {
+template <bool PAIR>
+fp4_status launch_wgrad(const CUtensorMap& tmA, const CUtensorMap& tmG, const WgradParams& p, int sms,
+                        cudaStream_t cs) {
+  using C = WgCfg<PAIR>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto kern = wgrad_dge_kernel<PAIR>;
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+      return FP4_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  const int64_t tiles = ((int64_t(p.K) + kBM * C::kCtas - 1) / (kBM * C::kCtas)) * ((int64_t(p.N) + kBN - 1) / kBN);
+  const int64_t units = sms / C::kCtas;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(unsigned(C::kCtas * (tiles < units ? tiles : units)));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = cs;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(C::kCtas);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmG, p) != cudaSuccess) return launch_status();
+  return launch_status();
+}
 }  // namespace
 }  // namespace fp4
 
@@ -404,15 +463,6 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   st = encode_tmap_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, uint64_t(N), uint64_t(M), uint64_t(lddy) * 2, kBox,
                       kBT, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != FP4_OK) return st;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(wgrad_dge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess)
-      return FP4_ERR_CUDA;
-    attr_set[dev] = true;
-  }
   WgradParams p;
   p.W = static_cast<const uint16_t*>(W);
   p.ldw = ldw;
@@ -428,8 +478,9 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   p.pw0 = p.expo < 0.0f ? INFINITY : (p.expo == 0.0f ? 1.0f : 0.0f);
   p.status = status_word();
   p.wait_ns = kWaitLimitNs;
-  const int64_t tiles = ((K + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-  const int grid = int(tiles < sms ? tiles : sms);
-  wgrad_dge_kernel<<<grid, kThreads, kSmemBytes, reinterpret_cast<cudaStream_t>(stream)>>>(tmA, tmG, p);
-  return launch_status();
+  // CTA pairs once the token loop is long (32 or more stages of 64 tokens); short
+  // loops keep single-CTA tiles
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (M >= 2048) return launch_wgrad<true>(tmA, tmG, p, sms, cs);
+  return launch_wgrad<false>(tmA, tmG, p, sms, cs);
 }

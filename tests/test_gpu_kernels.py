@@ -206,9 +206,12 @@ def test_fused_rows_outliers_matches_oracle_and_separate_calls(fp4, shape, q):
 
 # ---------------------------------------------------------------- DGE weight gradient
 
-@pytest.mark.parametrize("M,K,N", [(64, 128, 256), (256, 512, 512), (200, 136, 264), (1000, 384, 520)])
+@pytest.mark.parametrize("M,K,N", [(64, 128, 256), (256, 512, 512), (200, 136, 264), (1000, 384, 520),
+                                   (2048, 200, 264), (2304, 520, 520), (4100, 384, 136)])
 @pytest.mark.parametrize("k,clip", [(5.0, 3.0), (1.0, 3.0)])
 def test_wgrad_dge(fp4, M, K, N, k, clip):
+    """M >= 2048 tokens runs the GEMM as CTA pairs (256-row dW tiles; K = 200, 520
+    and 384 leave partial pair tiles, N = 264 / 136 partial column tiles)."""
     A_bits = _normal_bits(M + 1, (M, K))
     dY_bits = _normal_bits(N + 2, (M, N), 1e-3)
     W_bits = _normal_bits(K + 3, (K, N), 0.02)
