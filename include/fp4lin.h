@@ -282,9 +282,9 @@ fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_bytes, const
  *   W   device BF16 K x ldw, s_w device fp32 N (from fp4_quantize_cols)
  *   M, N, K  M >= 1; N % 8 == 0; K % 8 == 0; all < 2^31
  *   dge_k > 0, dge_clip > 0
- *   dW  device fp32 K x lddw, 16-byte aligned, lddw % 4 == 0; the call first
- *       writes the DGE factors there and then multiplies them by G in place,
- *       so dW must not alias A, dY, W or s_w
+ *   dW  device fp32 K x lddw, 16-byte aligned, lddw % 4 == 0; written once per
+ *       element while other tiles still read W and s_w, so dW must not alias
+ *       A, dY, W or s_w
  * Errors: INVALID_ARG, SHAPE, ALIGNMENT, DEVICE_UNSUPPORTED, CUDA;
  *         device-side TIMEOUT flag as for fp4_linear_fwd.
  */

@@ -26,13 +26,13 @@
 //
 // Roles (10 warps): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
 // warps 2-9 epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (one dW row per
-// thread) and columns (w-2)/4 * 128 .. +127 of the 256-wide tile.  At the
-// start of each tile, while the tensor core runs its first chunks, the
-// epilogue warps write the DGE factors of the tile into dW; after the last
-// chunk they multiply them by the gradient in place (coalesced row chunks
-// through a swizzled staging tile).  Every
-// mbarrier wait is bounded; on expiry the CTA records FP4_FLAG_TIMEOUT,
-// drains its TMA loads and MMAs, frees TMEM and exits.
+// thread) and columns (w-2)/4 * 128 .. +127 of the 256-wide tile, adding each
+// chunk into fp32 registers.  After the last chunk of a tile the warp computes
+// the DGE factors from W and s_W and writes dW = G * f' once, through a swizzled
+// staging tile as coalesced row chunks, while the tensor core already fills
+// both TMEM buffers with the next tile.  Every mbarrier wait is bounded; on
+// expiry the CTA records FP4_FLAG_TIMEOUT, drains its TMA loads and MMAs, frees
+// TMEM and exits.
 #include "common.cuh"
 
 namespace fp4 {
@@ -266,61 +266,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = pair_id; tile < tiles && ok; tile += npairs) {
       const int rb = tile % num_r, nb = tile / num_r;
       const int row0 = rb * kTileR + int(rank) * kBM + q * 32;  // first dW row of this warp's 32-row slab
-      // (1) While the tile's first chunks run on the tensor core, this warp
-      // writes the DGE factors f'(|W s_W|) of its 32 x 128 slab into dW; the
-      // final pass multiplies them by the gradient in place.  Each block goes
-      // through the swizzled staging tile and out as coalesced 128-byte rows;
-      // the final pass reads every element back from the same lane that wrote it.
-      if (row0 < p.K) {
-        const int my_row = row0 + lane;
-        const uint16_t* wrow = p.W + int64_t(my_row < p.K ? my_row : row0) * p.ldw;
-        // all loads of the pass first (one memory latency), then the math
-        uint4 w[kNBlk][4];
-        float swv[kNBlk];
-#pragma unroll
-        for (int j = 0; j < kNBlk; ++j) {
-          const int col0 = nb * kBN + c_base + j * kBlk;
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            w[j][c] = (col0 + 8 * c < p.N) ? __ldg(reinterpret_cast<const uint4*>(wrow + col0 + 8 * c))
-                                           : make_uint4(0u, 0u, 0u, 0u);
-          swv[j] = (col0 + lane < p.N) ? __ldg(p.s_w + col0 + lane) : 1.0f;  // column col0 + lane
-        }
-#pragma unroll
-        for (int j = 0; j < kNBlk; ++j) {
-          const int col0 = nb * kBN + c_base + j * kBlk;
-          if (col0 < p.N) {  // same for the whole warp
-            __syncwarp();  // the staging tile is free
-            uint8_t* orow = out_s + lane * 128;  // this lane's row: chunk c at c ^ (lane & 7)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint32_t wv[4] = {w[j][c].x, w[j][c].y, w[j][c].z, w[j][c].w};
-#pragma unroll
-              for (int half = 0; half < 2; ++half) {
-                float f[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                  const int cc = 8 * c + 4 * half + t;
-                  const float sw = __shfl_sync(0xFFFFFFFFu, swv[j], cc);
-                  const float wf = bf16_bits_to_float((wv[(4 * half + t) >> 1] >> (16 * (t & 1))) & 0xFFFFu);
-                  f[t] = dge_factor(fabsf(__fmul_rn(wf, sw)), p.inv_k, p.expo, p.clip, p.pw0);
-                }
-                const int oc = 2 * c + half;
-                *reinterpret_cast<float4*>(orow + ((oc ^ (lane & 7)) << 4)) = make_float4(f[0], f[1], f[2], f[3]);
-              }
-            }
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {  // lane l: chunk l % 8 of rows l / 8 + 4 i
-              const int r = (lane >> 3) + 4 * i, c = lane & 7;
-              const int grow = row0 + r, gcol = col0 + 4 * c;
-              if (grow < p.K && gcol < p.N)
-                *reinterpret_cast<float4*>(p.dW + int64_t(grow) * p.lddw + gcol) =
-                    *reinterpret_cast<const float4*>(out_s + r * 128 + ((c ^ (r & 7)) << 4));
-            }
-          }
-        }
-      }
       float sum[kEpiCols];
 #pragma unroll
       for (int c = 0; c < kEpiCols; ++c) sum[c] = 0.0f;
@@ -352,39 +297,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // (3) dW = G * f': this lane's sums go through the staging tile so that the
-      // multiply, the read of f' and the store of dW are coalesced row chunks.
+      // (2) dW = G * f'(|W s_W|): this lane's sums go through the staging tile so
+      // that the read of W, the factor, the multiply and the store of dW run on
+      // coalesced row chunks: lane l takes 4 columns (chunk l % 8) of rows l / 8 + 4 i.
+      // This runs while the tensor core starts the next tile in both TMEM buffers.
       if (row0 >= p.K) continue;
 #pragma unroll
       for (int j = 0; j < kNBlk; ++j) {
         const int col0 = nb * kBN + c_base + j * kBlk;
         if (col0 >= p.N) break;  // same for the whole warp
-        __syncwarp();  // the staging tile is free
-        uint8_t* orow = out_s + lane * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<float4*>(orow + ((c ^ (lane & 7)) << 4)) =
-              make_float4(sum[j * kBlk + 4 * c], sum[j * kBlk + 4 * c + 1], sum[j * kBlk + 4 * c + 2],
-                          sum[j * kBlk + 4 * c + 3]);
-        __syncwarp();
-        // the factors of this block (written by this same lane in the factor pass):
-        // all eight loads before any store, so they are in flight together
-        float4 f[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {  // same lane-to-element map as the factor pass
-          const int r = (lane >> 3) + 4 * i, c = lane & 7;
-          const int grow = row0 + r, gcol = col0 + 4 * c;
-          f[i] = (grow < p.K && gcol < p.N) ? __ldcg(reinterpret_cast<const float4*>(p.dW + int64_t(grow) * p.lddw + gcol))
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        const int c = lane & 7, gcol = col0 + 4 * c;
+        const bool col_ok = gcol < p.N;   // N % 8 == 0: the 4 columns are all in or all out
+        // every load of the block first (one memory latency), then the math
+        float4 sw = make_float4(1.f, 1.f, 1.f, 1.f);
+        if (col_ok) sw = make_float4(__ldg(p.s_w + gcol), __ldg(p.s_w + gcol + 1), __ldg(p.s_w + gcol + 2), __ldg(p.s_w + gcol + 3));
+        uint2 w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int r = (lane >> 3) + 4 * i, c = lane & 7;
-          const int grow = row0 + r, gcol = col0 + 4 * c;
-          if (grow < p.K && gcol < p.N) {
+          const int grow = row0 + (lane >> 3) + 4 * i;
+          w[i] = (col_ok && grow < p.K) ? __ldg(reinterpret_cast<const uint2*>(p.W + int64_t(grow) * p.ldw + gcol))
+                                        : make_uint2(0u, 0u);
+        }
+        __syncwarp();  // the staging tile is free
+        uint8_t* orow = out_s + lane * 128;   // this lane's row: chunk k at k ^ (lane & 7)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<float4*>(orow + ((k ^ (lane & 7)) << 4)) =
+              make_float4(sum[j * kBlk + 4 * k], sum[j * kBlk + 4 * k + 1], sum[j * kBlk + 4 * k + 2],
+                          sum[j * kBlk + 4 * k + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = (lane >> 3) + 4 * i;
+          const int grow = row0 + r;
+          if (grow < p.K && col_ok) {
             const float4 g = *reinterpret_cast<const float4*>(out_s + r * 128 + ((c ^ (r & 7)) << 4));
+            const float f0 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(w[i].x & 0xFFFFu), sw.x)), p.inv_k, p.expo, p.clip, p.pw0);
+            const float f1 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(w[i].x >> 16), sw.y)), p.inv_k, p.expo, p.clip, p.pw0);
+            const float f2 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(w[i].y & 0xFFFFu), sw.z)), p.inv_k, p.expo, p.clip, p.pw0);
+            const float f3 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(w[i].y >> 16), sw.w)), p.inv_k, p.expo, p.clip, p.pw0);
             *reinterpret_cast<float4*>(p.dW + int64_t(grow) * p.lddw + gcol) =
-                make_float4(g.x * f[i].x, g.y * f[i].y, g.z * f[i].z, g.w * f[i].w);
+                make_float4(g.x * f0, g.y * f1, g.z * f2, g.w * f3);
           }
         }
       }
