@@ -10,12 +10,14 @@
 //     last CTA to finish (atomic ticket) scans it for the exact k-th order
 //     statistic t.
 //  2. rows_outlier: one row per warp (or a few warps for long rows), held in
-//     registers: counts |A| > t per 16-byte chunk, reserves the row's run in a
-//     staging area with one atomic and writes (column, A - sign(A) t) in column
-//     order; optionally writes A_clamped, and in the fused variant also the
-//     row's E2M1 codes and scale (the clamp applied), so A is read once here.
+//     registers: counts |A| > t per 16-byte chunk and writes the row's count
+//     and its first kRowSlots entries (column, A - sign(A) t), in column order,
+//     into fixed per-row slots (no atomics); optionally writes A_clamped, and
+//     in the fused variant also the row's E2M1 codes and scale (the clamp
+//     applied), so A is read once here.
 //  3. row_scan: scan of the per-row counts -> row_ptr (one CTA, coalesced tiles).
-//  4. gather: copies every row's staged entries to its CSR position.
+//  4. gather: copies every row's slots to its CSR position; a row with more
+//     than kRowSlots entries is read again from A and emitted in full.
 #include <cmath>
 
 #include "common.cuh"
@@ -26,28 +28,28 @@ namespace {
 constexpr int kBins = 32768;
 constexpr int kHistThreads = 1024;
 
+constexpr int kRowSlots = 8;   // entries per row kept by the row pass (more are re-read from A)
+
 struct Ctrl {
   uint32_t done;          // CTAs finished with the histogram
   uint32_t t_bits;        // 15-bit magnitude pattern of t
-  unsigned long long cursor;     // next free staging slot
   unsigned long long nnz_expect; // number of |A| > t from the histogram
 };
 
 struct WsLayout {
-  size_t hist, ctrl, cnt, start, scol, sval, total;
+  size_t hist, ctrl, cnt, scol, sval, total;
 };
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-WsLayout ws_layout(int64_t M, int64_t cap) {
+WsLayout ws_layout(int64_t M) {
   WsLayout L;
   size_t off = 0;
   L.hist = off; off += round256(size_t(kBins) * 4);
   L.ctrl = off; off += round256(sizeof(Ctrl));
   L.cnt = off; off += round256(size_t(M) * 4);
-  L.start = off; off += round256(size_t(M) * 8);
-  L.scol = off; off += round256(size_t(cap) * 4);
-  L.sval = off; off += round256(size_t(cap) * 4);
+  L.scol = off; off += round256(size_t(M) * kRowSlots * 4);
+  L.sval = off; off += round256(size_t(M) * kRowSlots * 4);
   L.total = off;
   return L;
 }
@@ -65,7 +67,7 @@ __global__ void __launch_bounds__(kHistThreads, 1)
   const int64_t total = M * cpr;
   const bool dense = (lda == K);
   const int64_t stride = int64_t(gridDim.x) * kHistThreads;
-  constexpr int kU = 4;  // loads in flight per thread
+  constexpr int kU = 8;  // loads in flight per thread
   for (int64_t g0 = int64_t(blockIdx.x) * kHistThreads + threadIdx.x; g0 < total; g0 += stride * kU) {
     uint4 v[kU];
 #pragma unroll
@@ -116,16 +118,28 @@ __global__ void __launch_bounds__(kHistThreads, 1)
     local[i] = __ldcg(ghist + b0 + i);
     sum += local[i];
   }
-  part[threadIdx.x] = sum;
-  __syncthreads();
-  // inclusive scan over the 1024 partial sums (Hillis-Steele in shared memory, 64-bit safe via two halves)
-  for (int off = 1; off < kHistThreads; off <<= 1) {
-    const uint32_t add = threadIdx.x >= off ? part[threadIdx.x - off] : 0u;
-    __syncthreads();
-    part[threadIdx.x] += add;
-    __syncthreads();
+  // inclusive scan of the 1024 partial sums: within each warp by shuffles, then
+  // over the 32 warp totals (counts fit 32 bits: n < 2^32)
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t x = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
   }
-  const uint64_t incl = part[threadIdx.x];
+  if (lane == 31) part[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t wv = part[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, wv, o);
+      if (lane >= o) wv += y;
+    }
+    part[lane] = wv;
+  }
+  __syncthreads();
+  const uint64_t incl = uint64_t(x) + (wid ? part[wid - 1] : 0u);
   const uint64_t excl = incl - sum;
   if (excl < uint64_t(k_rank) && uint64_t(k_rank) <= incl) {
     uint64_t run = excl;
@@ -165,12 +179,10 @@ __device__ __forceinline__ uint32_t outlier_mask8(const uint4 v, uint32_t tb) {
 template <int CH, bool CODES>
 __global__ void __launch_bounds__(256, 2) rows_outlier_kernel(
     const uint16_t* __restrict__ A, int64_t M, int K, int64_t lda, Ctrl* ctrl, const float* __restrict__ t_ptr,
-    int64_t cap, int32_t* __restrict__ row_cnt, int64_t* __restrict__ row_start, int32_t* __restrict__ scol,
-    float* __restrict__ sval, uint16_t* __restrict__ A_c, int64_t ldac, uint8_t* __restrict__ codes, int64_t ldc,
-    float* __restrict__ scales, uint32_t* __restrict__ status, int wpr) {
+    int32_t* __restrict__ row_cnt, int32_t* __restrict__ scol, float* __restrict__ sval, uint16_t* __restrict__ A_c,
+    int64_t ldac, uint8_t* __restrict__ codes, int64_t ldc, float* __restrict__ scales, int wpr) {
   __shared__ uint32_t red[kRowWarps];
   __shared__ uint32_t tcnt[kRowWarps][CH];
-  __shared__ unsigned long long rbase[kRowWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows_per_cta = kRowWarps / wpr;
   const int r_in_cta = warp / wpr, w_in_row = warp % wpr;
@@ -179,18 +191,34 @@ __global__ void __launch_bounds__(256, 2) rows_outlier_kernel(
   const uint32_t tb = ctrl->t_bits;
   const uint32_t tb2 = tb | (tb << 16);
   const float t = *t_ptr;
-  for (int64_t row0 = int64_t(blockIdx.x) * rows_per_cta; row0 < M; row0 += int64_t(gridDim.x) * rows_per_cta) {
-    const int64_t row = row0 + r_in_cta;
-    const bool active = row < M;
-    const uint4* src = reinterpret_cast<const uint4*>(A + (active ? row : 0) * lda);
-    uint4 v[CH];
-    uint32_t msk[CH], excl[CH];
-    uint32_t mx = 0;
+  // persistent over row groups; the next group's chunks are loaded before the
+  // current group is processed, so every warp keeps one row's loads in flight
+  const int64_t gstride = int64_t(gridDim.x) * rows_per_cta;
+  uint4 v[CH];
+  {
+    const int64_t row = int64_t(blockIdx.x) * rows_per_cta + r_in_cta;
+    const uint4* src = reinterpret_cast<const uint4*>(A + (row < M ? row : 0) * lda);
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       const int ci = lane + 32 * (w_in_row + wpr * c);
-      v[c] = (active && ci < nchunk) ? __ldcs(src + ci) : make_uint4(0u, 0u, 0u, 0u);
+      v[c] = (row < M && ci < nchunk) ? __ldcs(src + ci) : make_uint4(0u, 0u, 0u, 0u);
     }
+  }
+  for (int64_t row0 = int64_t(blockIdx.x) * rows_per_cta; row0 < M; row0 += gstride) {
+    const int64_t row = row0 + r_in_cta;
+    const bool active = row < M;
+    uint4 vn[CH];
+    {
+      const int64_t nrow = row + gstride;
+      const uint4* nsrc = reinterpret_cast<const uint4*>(A + (nrow < M ? nrow : 0) * lda);
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const int ci = lane + 32 * (w_in_row + wpr * c);
+        vn[c] = (nrow < M && ci < nchunk) ? __ldcs(nsrc + ci) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    uint32_t msk[CH], excl[CH];
+    uint32_t mx = 0;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       if (CODES) mx = maxmag8(v[c], mx);
@@ -218,41 +246,31 @@ __global__ void __launch_bounds__(256, 2) rows_outlier_kernel(
       if (lane == 0) red[warp] = mb;
     }
     __syncthreads();
-    if (w_in_row == 0 && lane == 0) {
-      unsigned long long total = 0;
+    if (active && w_in_row == 0 && lane == 0) {
+      uint32_t total = 0;
       for (int c = 0; c < CH; ++c)
         for (int w = 0; w < wpr; ++w) total += tcnt[wrow0 + w][c];
-      unsigned long long base = 0;
-      if (active) {
-        if (total) base = atomicAdd(&ctrl->cursor, total);
-        row_cnt[row] = int32_t(total);
-        row_start[row] = int64_t(base);
-        if (int64_t(base + total) > cap) {
-          atomicOr(status, FP4_FLAG_CAPACITY);
-          base = ~0ull;
-        }
-      }
-      rbase[r_in_cta] = base;
+      row_cnt[row] = int32_t(total);
     }
-    __syncthreads();
-    const unsigned long long rb = rbase[r_in_cta];
-    if (active && rb != ~0ull) {
-      unsigned long long off = rb;
+    if (active) {
+      // the row's first kRowSlots entries go to its slots; a longer row is
+      // emitted again from A by the gather pass
+      uint32_t off = 0;
 #pragma unroll
       for (int c = 0; c < CH; ++c) {
-        unsigned long long pos = off + excl[c];
+        uint32_t pos = off + excl[c];
         for (int w = 0; w < w_in_row; ++w) pos += tcnt[wrow0 + w][c];
         uint32_t m = msk[c];
-        if (m) {
+        if (m && pos < uint32_t(kRowSlots)) {
           const int ci = lane + 32 * (w_in_row + wpr * c);
           const uint4 vc = v[c];
-          while (m) {  // set bits in ascending column order
+          while (m && pos < uint32_t(kRowSlots)) {  // set bits in ascending column order
             const int e = __ffs(m) - 1;
             m &= m - 1;
             const uint32_t word = e < 4 ? (e < 2 ? vc.x : vc.y) : (e < 6 ? vc.z : vc.w);
             const float x = bf16_bits_to_float((word >> (16 * (e & 1))) & 0xFFFFu);
-            scol[pos] = ci * 8 + e;
-            sval[pos] = __fsub_rn(x, copysignf(t, x));
+            scol[row * kRowSlots + pos] = ci * 8 + e;
+            sval[row * kRowSlots + pos] = __fsub_rn(x, copysignf(t, x));
             ++pos;
           }
         }
@@ -292,7 +310,9 @@ __global__ void __launch_bounds__(256, 2) rows_outlier_kernel(
         }
       }
     }
-    __syncthreads();  // tcnt / rbase / red are reused by the next row group
+    __syncthreads();  // tcnt / red are reused by the next row group
+#pragma unroll
+    for (int c = 0; c < CH; ++c) v[c] = vn[c];
   }
 }
 
@@ -345,27 +365,62 @@ __global__ void __launch_bounds__(1024) row_scan_kernel(const int32_t* __restric
   }
   if (tid == 0) {
     if (nnz_out) *nnz_out = carry;
-    if (uint64_t(carry) != ctrl->nnz_expect && carry <= cap) atomicOr(status, FP4_FLAG_INTERNAL);
+    if (carry > cap) atomicOr(status, FP4_FLAG_CAPACITY);
+    else if (uint64_t(carry) != ctrl->nnz_expect) atomicOr(status, FP4_FLAG_INTERNAL);
   }
 }
 
+// One warp per row: the row's slots to its CSR position, or, for a row with
+// more than kRowSlots entries, the row read again from A and emitted in column
+// order (a warp prefix over the lanes' 16-byte chunks).
 __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__ row_cnt,
-                                                    const int64_t* __restrict__ row_start,
                                                     const int32_t* __restrict__ row_ptr, int64_t M,
                                                     const int32_t* __restrict__ scol, const float* __restrict__ sval,
+                                                    const uint16_t* __restrict__ A, int K, int64_t lda,
+                                                    const Ctrl* __restrict__ ctrl, const float* __restrict__ t_ptr,
                                                     int32_t* __restrict__ col_idx, float* __restrict__ vals,
                                                     int64_t cap) {
   const int lane = threadIdx.x & 31;
   const int64_t warp_global = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const uint32_t tb = ctrl->t_bits;
+  const float t = *t_ptr;
+  const int nchunk = K >> 3;
   for (int64_t row = warp_global; row < M; row += nwarps) {
     const int32_t n = row_cnt[row];
-    const int64_t src = row_start[row];
     const int64_t dst = row_ptr[row];
-    if (src + n > cap || dst + n > cap) continue;
-    for (int e = lane; e < n; e += 32) {
-      col_idx[dst + e] = scol[src + e];
-      vals[dst + e] = sval[src + e];
+    if (dst + n > cap) continue;   // flagged by the scan
+    if (n <= kRowSlots) {
+      if (lane < n) {
+        col_idx[dst + lane] = scol[row * kRowSlots + lane];
+        vals[dst + lane] = sval[row * kRowSlots + lane];
+      }
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(A + row * lda);
+    int64_t base = dst;
+    for (int c0 = 0; c0 < nchunk; c0 += 32) {
+      const int ci = c0 + lane;
+      const uint4 v = ci < nchunk ? __ldg(src + ci) : make_uint4(0u, 0u, 0u, 0u);
+      uint32_t m = ci < nchunk ? outlier_mask8(v, tb) : 0u;
+      const uint32_t cnt = __popc(m);
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int64_t pos = base + (incl - cnt);
+      while (m) {
+        const int e = __ffs(m) - 1;
+        m &= m - 1;
+        const uint32_t word = e < 4 ? (e < 2 ? v.x : v.y) : (e < 6 ? v.z : v.w);
+        const float x = bf16_bits_to_float((word >> (16 * (e & 1))) & 0xFFFFu);
+        col_idx[pos] = ci * 8 + e;
+        vals[pos] = __fsub_rn(x, copysignf(t, x));
+        ++pos;
+      }
+      base += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
   }
 }
@@ -383,7 +438,7 @@ FP4_API int64_t outlier_max_nnz(int64_t M, int64_t K, double q) {
 
 FP4_API size_t outlier_clamp_quantile_workspace(int64_t M, int64_t K, int64_t nnz_capacity) {
   if (M <= 0 || K <= 0 || nnz_capacity < 0) return 0;
-  return fp4::ws_layout(M, nnz_capacity).total;
+  return fp4::ws_layout(M).total;
 }
 
 namespace fp4 {
@@ -391,12 +446,12 @@ namespace {
 
 template <bool CODES>
 void launch_rows_outlier(int ch, int wpr, unsigned blocks, cudaStream_t s, const uint16_t* A, int64_t M, int K,
-                         int64_t lda, Ctrl* ctrl, const float* t, int64_t cap, int32_t* row_cnt, int64_t* row_start,
+                         int64_t lda, Ctrl* ctrl, const float* t, int32_t* row_cnt,
                          int32_t* scol, float* sval, uint16_t* A_c, int64_t ldac, uint8_t* codes, int64_t ldc,
-                         float* scales, uint32_t* status) {
-#define FP4_ROWS_OUTLIER(CHV)                                                                                     \
-  rows_outlier_kernel<CHV, CODES><<<blocks, 256, 0, s>>>(A, M, K, lda, ctrl, t, cap, row_cnt, row_start, scol, \
-                                                         sval, A_c, ldac, codes, ldc, scales, status, wpr)
+                         float* scales) {
+#define FP4_ROWS_OUTLIER(CHV)                                                                                 \
+  rows_outlier_kernel<CHV, CODES><<<blocks, 256, 0, s>>>(A, M, K, lda, ctrl, t, row_cnt, scol, sval, A_c, ldac, \
+                                                         codes, ldc, scales, wpr)
   switch (ch) {
     case 1: FP4_ROWS_OUTLIER(1); break;
     case 2: FP4_ROWS_OUTLIER(2); break;
@@ -415,12 +470,11 @@ fp4_status run_outlier_pipeline(const void* A, int64_t M, int64_t K, int64_t lda
   int sms = 0;
   fp4_status st = check_device(&sms);
   if (st != FP4_OK) return st;
-  const WsLayout L = ws_layout(M, nnz_capacity);
+  const WsLayout L = ws_layout(M);
   auto* ws = static_cast<uint8_t*>(workspace);
   auto* ghist = reinterpret_cast<uint32_t*>(ws + L.hist);
   auto* ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
   auto* row_cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
-  auto* row_start = reinterpret_cast<int64_t*>(ws + L.start);
   auto* scol = reinterpret_cast<int32_t*>(ws + L.scol);
   auto* sval = reinterpret_cast<float*>(ws + L.sval);
   uint32_t* status = status_word();
@@ -441,38 +495,37 @@ fp4_status run_outlier_pipeline(const void* A, int64_t M, int64_t K, int64_t lda
     attr_set[dev] = true;
   }
   const int64_t chunks = n / 8;
-  int64_t hblocks = (chunks + kHistThreads * 4 - 1) / (kHistThreads * 4);
+  int64_t hblocks = (chunks + kHistThreads * 8 - 1) / (kHistThreads * 8);
   if (hblocks > sms) hblocks = sms;
   if (hblocks < 1) hblocks = 1;
   histogram_select_kernel<<<unsigned(hblocks), kHistThreads, hist_smem, s>>>(a, M, int(K), lda, k_rank, ghist, ctrl,
                                                                              t_out);
   if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
 
-  // fused row pass: rows of <= 8 chunks per lane, 1..8 warps per row (K <= 32768)
+  // fused row pass: up to 4 chunks per lane (8 for rows longer than 8 warps x 4
+  // chunks), 1..8 warps per row (K <= 32768); persistent, 2 CTAs per SM
   const int nchunk = int(K / 8);
   int wpr = 1;
-  while (wpr < 8 && nchunk > 32 * 8 * wpr) wpr *= 2;
+  while (wpr < 8 && nchunk > 32 * 4 * wpr) wpr *= 2;
   const int per_lane = (nchunk + 32 * wpr - 1) / (32 * wpr);
   const int ch = per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : 8;
   const int rows_per_cta = kRowWarps / wpr;
   int64_t rblocks = (M + rows_per_cta - 1) / rows_per_cta;
-  if (rblocks > int64_t(sms) * 8) rblocks = int64_t(sms) * 8;
+  if (rblocks > int64_t(sms) * 2) rblocks = int64_t(sms) * 2;
   if (codes)
-    launch_rows_outlier<true>(ch, wpr, unsigned(rblocks), s, a, M, int(K), lda, ctrl, t_out, nnz_capacity, row_cnt,
-                              row_start, scol, sval, static_cast<uint16_t*>(A_clamped), ldac, codes, ldc, scales,
-                              status);
+    launch_rows_outlier<true>(ch, wpr, unsigned(rblocks), s, a, M, int(K), lda, ctrl, t_out, row_cnt, scol, sval,
+                              static_cast<uint16_t*>(A_clamped), ldac, codes, ldc, scales);
   else
-    launch_rows_outlier<false>(ch, wpr, unsigned(rblocks), s, a, M, int(K), lda, ctrl, t_out, nnz_capacity, row_cnt,
-                               row_start, scol, sval, static_cast<uint16_t*>(A_clamped), ldac, nullptr, 0, nullptr,
-                               status);
+    launch_rows_outlier<false>(ch, wpr, unsigned(rblocks), s, a, M, int(K), lda, ctrl, t_out, row_cnt, scol, sval,
+                               static_cast<uint16_t*>(A_clamped), ldac, nullptr, 0, nullptr);
   if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
   row_scan_kernel<<<1, 1024, 0, s>>>(row_cnt, M, row_ptr, nnz_out, ctrl, nnz_capacity, status);
   if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
   if (nnz_capacity > 0) {
     int64_t gblocks = (M + 7) / 8;
     if (gblocks > int64_t(sms) * 8) gblocks = int64_t(sms) * 8;
-    gather_kernel<<<unsigned(gblocks), 256, 0, s>>>(row_cnt, row_start, row_ptr, M, scol, sval, col_idx, vals,
-                                                    nnz_capacity);
+    gather_kernel<<<unsigned(gblocks), 256, 0, s>>>(row_cnt, row_ptr, M, scol, sval, a, int(K), lda, ctrl, t_out,
+                                                    col_idx, vals, nnz_capacity);
     if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
   }
   return FP4_OK;
@@ -490,7 +543,7 @@ fp4_status validate_outlier_args(const void* A, int64_t M, int64_t K, int64_t ld
   const int64_t need = outlier_max_nnz(M, K, q);
   if (nnz_capacity < need || nnz_capacity >= (int64_t(1) << 31)) return FP4_ERR_CAPACITY;
   if (nnz_capacity > 0 && (!col_idx || !vals)) return FP4_ERR_INVALID_ARG;
-  if (ws_bytes < ws_layout(M, nnz_capacity).total) return FP4_ERR_WORKSPACE;
+  if (ws_bytes < ws_layout(M).total) return FP4_ERR_WORKSPACE;
   return FP4_OK;
 }
 
