@@ -109,15 +109,20 @@ __global__ void __launch_bounds__(kHistThreads, 1)
   __threadfence();
 
   // Exact order statistic: the smallest bin b with cumulative count >= k_rank.
+  // The merged histogram comes into this CTA's shared memory with coalesced
+  // 16-byte loads; thread t then owns bins 32 t .. 32 t + 31 (summed in a
+  // lane-skewed order, so a warp's 32 reads fall in 32 different banks).
   constexpr int kPer = kBins / kHistThreads;  // 32 bins per thread
+#pragma unroll
+  for (int j = 0; j < kBins / 4 / kHistThreads; ++j) {
+    const int i4 = threadIdx.x + j * kHistThreads;
+    reinterpret_cast<uint4*>(hist)[i4] = __ldcg(reinterpret_cast<const uint4*>(ghist) + i4);
+  }
+  __syncthreads();
   const int b0 = threadIdx.x * kPer;
-  uint32_t local[kPer];
   uint32_t sum = 0;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    local[i] = __ldcg(ghist + b0 + i);
-    sum += local[i];
-  }
+  for (int i = 0; i < kPer; ++i) sum += hist[b0 + ((i + threadIdx.x) & (kPer - 1))];
   // inclusive scan of the 1024 partial sums: within each warp by shuffles, then
   // over the 32 warp totals (counts fit 32 bits: n < 2^32)
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(kHistThreads, 1)
     uint64_t run = excl;
     int sel = b0 + kPer - 1;
     for (int i = 0; i < kPer; ++i) {
-      run += local[i];
+      run += hist[b0 + i];
       if (run >= uint64_t(k_rank)) {
         sel = b0 + i;
         break;
