@@ -382,10 +382,21 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uin
 // Packed BF16 helpers: a 32-bit word holds two BF16 values, element 2i in the
 // low half.  Magnitudes compare as unsigned 15-bit integers (sign cleared).
 
+// Packed BF16 pair operations on the hardware's bf16x2 units.  The operands are
+// magnitude patterns (sign cleared, finite), for which the BF16 order is the
+// unsigned integer order of the 15-bit patterns.
+__device__ __forceinline__ uint32_t bf2_gt_mask(uint32_t a, uint32_t b) {   // 0xFFFF per half where a > b
+  return __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+}
+__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 m = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&m);
+}
+
 // sign(x) min(|x|, t) for both halves, with tb2 = t's 15-bit pattern in both
 // halves: exact, since t is itself a BF16 value.
 __device__ __forceinline__ uint32_t clamp_pair(uint32_t w, uint32_t tb2) {
-  const uint32_t gt = __vcmpgtu2(w & 0x7FFF7FFFu, tb2);
+  const uint32_t gt = bf2_gt_mask(w & 0x7FFF7FFFu, tb2);
   return (w & ~gt) | (((w & 0x80008000u) | tb2) & gt);
 }
 
@@ -422,10 +433,10 @@ __device__ __forceinline__ uint32_t quantize8_clamp_f32(const uint4 v, float s, 
 
 // Running maximum of the 15-bit magnitude patterns of a chunk, per 16-bit half.
 __device__ __forceinline__ uint32_t maxmag8(const uint4 v, uint32_t acc) {
-  acc = __vmaxu2(acc, v.x & 0x7FFF7FFFu);
-  acc = __vmaxu2(acc, v.y & 0x7FFF7FFFu);
-  acc = __vmaxu2(acc, v.z & 0x7FFF7FFFu);
-  return __vmaxu2(acc, v.w & 0x7FFF7FFFu);
+  acc = bf2_max(acc, v.x & 0x7FFF7FFFu);
+  acc = bf2_max(acc, v.y & 0x7FFF7FFFu);
+  acc = bf2_max(acc, v.z & 0x7FFF7FFFu);
+  return bf2_max(acc, v.w & 0x7FFF7FFFu);
 }
 
 // Largest magnitude pattern of a warp's packed maxima, as an fp32 value.

@@ -227,8 +227,8 @@ __global__ void __launch_bounds__(256, 2) rows_outlier_kernel(
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
       if (CODES) mx = maxmag8(v[c], mx);
-      const uint32_t g = __vcmpgtu2(v[c].x & 0x7FFF7FFFu, tb2) | __vcmpgtu2(v[c].y & 0x7FFF7FFFu, tb2) |
-                         __vcmpgtu2(v[c].z & 0x7FFF7FFFu, tb2) | __vcmpgtu2(v[c].w & 0x7FFF7FFFu, tb2);
+      const uint32_t g = bf2_gt_mask(v[c].x & 0x7FFF7FFFu, tb2) | bf2_gt_mask(v[c].y & 0x7FFF7FFFu, tb2) |
+                         bf2_gt_mask(v[c].z & 0x7FFF7FFFu, tb2) | bf2_gt_mask(v[c].w & 0x7FFF7FFFu, tb2);
       msk[c] = 0;
       excl[c] = 0;
       uint32_t tot = 0;

@@ -204,6 +204,31 @@ def test_fused_rows_outliers_matches_oracle_and_separate_calls(fp4, shape, q):
     assert_no_device_flags(fp4)
 
 
+@pytest.mark.parametrize("q", [0.005, 0.3, 0.9999])
+def test_fused_rows_outliers_every_finite_bf16_pattern(fp4, q):
+    """All 65536 BF16 patterns (non-finite ones replaced by +-0) as a 256 x 256
+    matrix, shuffled by rows: the packed magnitude max, the outlier test and the
+    clamp must treat zeros, subnormals (q = 0.005 puts t among them), ties with
+    t and the largest finite values exactly as the oracle's integer order."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    finite = (bits & np.uint16(0x7F80)) != np.uint16(0x7F80)
+    bits = np.where(finite, bits, bits & np.uint16(0x8000)).astype(np.uint16)
+    A_bits = bits[np.random.default_rng(7).permutation(65536)].reshape(256, 256)
+    o = fp4.fp4_quantize_rows_outliers(dev_bf16(A_bits), q)
+    torch.cuda.synchronize()
+    t, _, _ = orc.quantile_threshold(A_bits, q)
+    A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
+    ref_codes, ref_s = orc.quantize_rows(A_c)
+    nnz = int(o["nnz"].item())
+    assert o["t"].cpu().numpy().view(np.uint32)[0] == np.float32(t).view(np.uint32)
+    assert np.array_equal(o["row_ptr"].cpu().numpy(), rp)
+    assert np.array_equal(o["col_idx"][:nnz].cpu().numpy(), ci)
+    assert np.array_equal(o["vals"][:nnz].cpu().numpy().view(np.uint32), cv.view(np.uint32))
+    assert np.array_equal(o["codes"].cpu().numpy(), ref_codes)
+    assert np.array_equal(o["scales"].cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert_no_device_flags(fp4)
+
+
 # ---------------------------------------------------------------- DGE weight gradient
 
 @pytest.mark.parametrize("M,K,N", [(64, 128, 256), (256, 512, 512), (200, 136, 264), (1000, 384, 520),
