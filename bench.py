@@ -1,5 +1,5 @@
 #!/usr/bin/env python
-"""Benchmark of the FP4 quantized linear layer (forward + DGE weight gradient).
+"""Benchmark of the FP4 quantized linear layer (forward + backward).
 
 One step = one pass of the whole hot path over one batch of synthetic input:
 for every distinct activation (linears that share an input share this phase)
@@ -8,11 +8,12 @@ and for every linear of the workload
   column quantization of W                               (fp4_quantize_cols)
   FP4 GEMM + scales + dA*W compensation -> BF16 Y       (fp4_linear_fwd)
   BF16 weight-gradient GEMM x DGE factor -> fp32 dW     (fp4_linear_wgrad_dge)
+  BF16 input-gradient GEMM dY W^T -> BF16 dX             (fp4_linear_dgrad)
 
-Metric: fwd + wgrad TFLOP/s = sum over linears of 4 M K N / step time, with
+Metric: fwd + bwd TFLOP/s = sum over linears of 6 M K N / step time, with
 inputs resident in HBM and L2 flushed (256 MiB write) before every step.
 `e2e` is the same metric through the C ABI from pinned HOST buffers: the
-host->device copy of A, W, dY and the device->host copy of Y and dW are inside
+host->device copy of A, W, dY and the device->host copy of Y, dW and dX are inside
 the timed region.  `--impl reference` times the CPU oracle instead (bounded
 sample, single thread).  Under torchrun each rank runs an independent replica
 on its own GPU (the layer has no data-path exchange on one GPU's batch);
@@ -143,11 +144,11 @@ class ActStep:
 
 
 class LinStep:
-    """One linear: column quantization of W, FP4 GEMM, DGE weight gradient."""
+    """One linear: column quantization of W, FP4 GEMM, DGE weight gradient, input gradient."""
 
-    PHASES = ("fp4_quantize_cols", "fp4_linear_fwd", "fp4_linear_wgrad_dge")
+    PHASES = ("fp4_quantize_cols", "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_linear_dgrad")
     # fwd: 2 compensation prep kernels (after a memset) and the GEMM
-    LAUNCHES = {"fp4_quantize_cols": 2, "fp4_linear_fwd": 3, "fp4_linear_wgrad_dge": 1}
+    LAUNCHES = {"fp4_quantize_cols": 2, "fp4_linear_fwd": 3, "fp4_linear_wgrad_dge": 1, "fp4_linear_dgrad": 1}
 
     def __init__(self, fp4, lin, act: ActStep, W, dY):
         import torch
@@ -161,6 +162,7 @@ class LinStep:
         self.Y = torch.empty((lin.M, N), dtype=torch.bfloat16, device=dev)
         self.ws_fwd = torch.empty(fp4.fp4_linear_fwd_workspace(lin.M, N, K), dtype=torch.uint8, device=dev)
         self.dW = torch.empty((K, N), dtype=torch.float32, device=dev)
+        self.dX = torch.empty((lin.M, K), dtype=torch.bfloat16, device=dev)
 
     def fns(self):
         fp4, lin, a = self.fp4, self.lin, self.act
@@ -169,6 +171,7 @@ class LinStep:
             lambda: fp4.fp4_linear_fwd(a.out["codes"], a.out["scales"], self.w_codes, self.s_w, lin.K, csr=a.out,
                                        W=self.W, out_type="bf16", Y=self.Y, workspace=self.ws_fwd),
             lambda: fp4.fp4_linear_wgrad_dge(a.A, self.dY, self.W, self.s_w, DGE_K, DGE_CLIP, dW=self.dW),
+            lambda: fp4.fp4_linear_dgrad(self.dY, self.W, dX=self.dX),
         ]
 
     def algorithmic(self):
@@ -177,6 +180,7 @@ class LinStep:
             "fp4_quantize_cols": (2.5 * K * N + 4 * N, "B", "hbm"),
             "fp4_linear_fwd": (2 * M * K * N, "FLOP", "tensor_fp4"),
             "fp4_linear_wgrad_dge": (2 * M * K * N, "FLOP", "tensor_bf16"),
+            "fp4_linear_dgrad": (2 * M * K * N, "FLOP", "tensor_bf16"),
         }
 
 
@@ -230,7 +234,8 @@ def _src_hash(files):
 
 
 KERNEL_SOURCES = {
-    "fp4_linear_wgrad_dge": ["gemm_wgrad.cu", "common.cuh"],
+    "fp4_linear_wgrad_dge": ["gemm_wgrad.cu", "bwd_gemm.cuh", "common.cuh"],
+    "fp4_linear_dgrad": ["gemm_dgrad.cu", "bwd_gemm.cuh", "common.cuh"],
     "fp4_linear_fwd": ["gemm_fwd.cu", "common.cuh"],
     "fp4_quantize_cols": ["quantize.cu", "common.cuh"],
     "fp4_quantize_rows_outliers": ["outlier.cu", "common.cuh"],
@@ -290,7 +295,7 @@ def run_gpu(args):
         dev_inputs.append((dev_cache[id(hA)], hW.cuda(), hG.cuda()))
     plan = StepPlan(fp4, work, dev_inputs)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    flops = sum(4 * l.M * l.K * l.N for l in work.linears)
+    flops = sum(6 * l.M * l.K * l.N for l in work.linears)
 
     for _ in range(args.warmup):
         plan.run()
@@ -329,9 +334,10 @@ def run_gpu(args):
     # ---- end to end through the C ABI from pinned host buffers
     hY = [torch.empty(l.Y.shape, dtype=l.Y.dtype).pin_memory() for l in plan.lins]
     hdW = [torch.empty(l.dW.shape, dtype=l.dW.dtype).pin_memory() for l in plan.lins]
+    hdX = [torch.empty(l.dX.shape, dtype=l.dX.dtype).pin_memory() for l in plan.lins]
     uniq_hA = {id(h[0]): h[0] for h in host}
     bi = sum(h.numel() * 2 for h in uniq_hA.values()) + sum(h[1].numel() * 2 + h[2].numel() * 2 for h in host)
-    bo = sum(y.numel() * 2 + d.numel() * 4 for y, d in zip(hY, hdW))
+    bo = sum(y.numel() * 2 + d.numel() * 4 + x.numel() * 2 for y, d, x in zip(hY, hdW, hdX))
     e2e_ms = []
     for k in range(args.warmup + args.steps):
         flush.fill_(float(k))
@@ -349,6 +355,7 @@ def run_gpu(args):
         for i, l in enumerate(plan.lins):
             hY[i].copy_(l.Y, non_blocking=True)
             hdW[i].copy_(l.dW, non_blocking=True)
+            hdX[i].copy_(l.dX, non_blocking=True)
         e1.record()
         e1.synchronize()
         if k >= args.warmup:
@@ -395,9 +402,10 @@ def run_gpu(args):
         "metric": "FP4 linear fwd+bwd TFLOPS on 1 GB300, % of dense FP4 peak; quantize GB/s vs HBM",
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp4_e2m1 fwd / bf16 wgrad, fp32 accumulate", "data": "synthetic (seeded, LLaMA-shaped)",
+        "dtype": "fp4_e2m1 fwd / bf16 wgrad + dgrad, fp32 accumulate", "data": "synthetic (seeded, LLaMA-shaped)",
         "config": {"workload": args.workload, "linears": [[l.name, l.M, l.K, l.N, l.q] for l in work.linears],
-                   "bwd": "weight gradient with DGE (dgrad not on the pages)", "l2": "flushed before every step",
+                   "bwd": "weight gradient with DGE + input gradient dY W^T (BF16; the pages give no dgrad)",
+                   "l2": "flushed before every step",
                    "launch": "one CUDA graph per phase, replayed after a 0.2 ms GPU head start",
                    "parallelism": f"replicas x{world}"},
         "fp4_peak_frac": round(value / world / fp4_peak, 4),
@@ -430,7 +438,7 @@ work = wl.WORKLOADS[sys.argv[2]]
 rows_sample = int(sys.argv[3])
 nsteps = int(sys.argv[4])
 inputs = [(lin, work.activation(lin), work.weight(lin), work.grad(lin)) for lin in work.linears]
-flops = sum(4 * lin.M * lin.K * lin.N for lin in work.linears)
+flops = sum(6 * lin.M * lin.K * lin.N for lin in work.linears)
 steps = []
 for _ in range(nsteps):
     total_est = 0.0
@@ -453,8 +461,10 @@ for _ in range(nsteps):
         ks = np.arange(min(rows_sample, lin.K))
         orc.wgrad_dge(A_bits, dY_bits, W_bits, s_w, 5.0, 3.0, rows=ks)
         t5 = time.perf_counter()
+        orc.f64_to_bf16(orc.linear_dgrad(dY_bits, W_bits, rows=rs))
+        t6 = time.perf_counter()
         total_est += ((t1 - t0) + (t2 - t1) * lin.M / len(rs) + (t3 - t2) + (t4 - t3) * lin.M / len(rs)
-                      + (t5 - t4) * lin.K / len(ks))
+                      + (t5 - t4) * lin.K / len(ks) + (t6 - t5) * lin.M / len(rs))
     steps.append(total_est)
 print(json.dumps(dict(steps=steps, flops=flops)))
 """
@@ -472,8 +482,8 @@ def _oracle_steps(workload: str, rows_sample: int, nsteps: int):
 
 def _sample_text(rows_sample: int) -> str:
     return (f"per step: quantile + clamp + CSR of A and column quantization of W in full; row quantization and "
-            f"FP4 GEMM + epilogue on the first {rows_sample} rows, DGE wgrad on the first {rows_sample} feature "
-            f"rows, each scaled linearly to the full size; one thread (OPENBLAS/OMP threads = 1)")
+            f"FP4 GEMM + epilogue and dgrad on the first {rows_sample} rows, DGE wgrad on the first {rows_sample} "
+            f"feature rows, each scaled linearly to the full size; one thread (OPENBLAS/OMP threads = 1)")
 
 
 def cpu_baseline(workload: str, rows_sample: int = 64):

@@ -294,6 +294,30 @@ fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* dY, int6
                                 fp4_stream_t stream);
 
 /*
+ * fp4_linear_dgrad -- BF16 input-gradient GEMM on tcgen05 (kind::f16):
+ *   dX[m,k] = sum_n dY[m,n] W[k,n]        (fp32 accumulate; dX = dY W^T)
+ *
+ * Not on the pages: they give the forward pass and the DGE weight gradient
+ * (page "首个 FP4 ...", czzqal.com, DGE passage) but not the input gradient.
+ * This is the chain rule of Y = A W, the plainest reading that closes the
+ * linear's backward: the same BF16 engine as fp4_linear_wgrad_dge, with the
+ * BF16 W the caller passes (the unquantized weight, as the compensation uses).
+ * The reduction over N runs in 1024-element chunks summed in fp32 registers.
+ *
+ *   dY  device BF16 M x lddy (tokens x out), 16-byte aligned, lddy % 8 == 0
+ *   W   device BF16 K x ldw (in x out), 16-byte aligned, ldw % 8 == 0
+ *   M, N, K  M >= 1; N, K >= 8; N % 8 == 0; K % 8 == 0; all < 2^31
+ *   dX  device M x lddx (tokens x in) of dx_type, 16-byte aligned, lddx % 8 == 0,
+ *       lddx >= K; must not alias dY or W
+ *   dx_type  FP4_OUT_BF16 (round to nearest even) or FP4_OUT_FP32
+ * Errors: INVALID_ARG (null pointer, other dx_type), SHAPE, ALIGNMENT,
+ *         DEVICE_UNSUPPORTED, CUDA; device-side TIMEOUT flag as for fp4_linear_fwd.
+ */
+fp4_status fp4_linear_dgrad(const void* dY, int64_t lddy, const void* W, int64_t ldw, int64_t M,
+                            int64_t N, int64_t K, void* dX, int dx_type, int64_t lddx,
+                            fp4_stream_t stream);
+
+/*
  * fp4_device_status -- synchronize `stream`, then return the sticky device
  * flags (FP4_FLAG_*) of the current device in *flags_out and clear them.
  * The return value is FP4_ERR_TIMEOUT / FP4_ERR_CAPACITY / FP4_ERR_INTERNAL

@@ -39,7 +39,8 @@ R3 the sign of a value that rounds to zero is kept (code 0x8); R4 a zero or
    compensation multiplies dA by the original BF16 W; R9 the DGE surrogate is a
    per-interval power function with exponent 1/k and a clipped derivative;
    R11 accumulation and outputs in fp32 / BF16 (the pages' FP16 output is the
-   authors' emulation detail); R12 element 2c of a row goes in the low nibble.
+   authors' emulation detail); R12 element 2c of a row goes in the low nibble;
+   R16 the input gradient (absent from the pages) is dY W^T with the BF16 W.
 
 Precision: fp64 wherever the pages fix no precision.  The quantizer itself
 works in fp32 because its definition (R1) is an fp32 division and multiply.
@@ -399,6 +400,30 @@ def wgrad_dge(A_bits, dY_bits, W_bits, s_w, k: float, clip: float,
     W = bf16_to_f32(np.asarray(W_bits)[np.ix_(rows, cols)])
     x = np.abs(W * np.asarray(s_w, dtype=np.float32)[cols][None, :]).astype(np.float64)
     return (G * dge_derivative(x, k, clip)).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# Input gradient (not on the pages)
+# --------------------------------------------------------------------------
+
+
+def linear_dgrad(dY_bits, W_bits, rows: Optional[Sequence[int]] = None,
+                 cols: Optional[Sequence[int]] = None) -> np.ndarray:
+    """dX[m,k] = sum_n dY[m,n] W[k,n], i.e. dX = dY W^T, in fp64.
+
+    The pages give the forward pass and the DGE-corrected weight gradient but
+    not the input gradient.  Reading R16: the chain rule of the forward's
+    product A W, taken with the BF16 weight the caller passes (the unquantized
+    W, as the compensation term uses).  Products of BF16 values are exact in
+    fp64, so the result is the exact sum up to fp64 rounding; the caller rounds
+    it to the output type.  rows select dX rows (tokens), cols select dX
+    columns (input features).
+    """
+    dY = bf16_to_f32(np.asarray(dY_bits)).astype(np.float64)
+    W = bf16_to_f32(np.asarray(W_bits)).astype(np.float64)
+    rows = np.arange(dY.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+    cols = np.arange(W.shape[0]) if cols is None else np.asarray(cols, dtype=np.int64)
+    return dY[rows] @ W[cols].T
 
 
 # --------------------------------------------------------------------------

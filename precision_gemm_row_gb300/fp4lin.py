@@ -26,8 +26,8 @@ FLAG_TIMEOUT, FLAG_CAPACITY, FLAG_INTERNAL = 0x1, 0x2, 0x4
 EXPORTS = (
     "fp4_status_string", "fp4_abi_version", "fp4_last_cuda_error", "fp4_quantize_rows", "fp4_quantize_cols_workspace",
     "fp4_quantize_cols", "fp4_quantize_cols_noalloc", "outlier_max_nnz", "outlier_clamp_quantile_workspace", "outlier_clamp_quantile",
-    "fp4_quantize_rows_outliers", "fp4_linear_fwd_workspace", "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_device_status",
-    "fp4_selftest_bounded_wait",
+    "fp4_quantize_rows_outliers", "fp4_linear_fwd_workspace", "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_linear_dgrad",
+    "fp4_device_status", "fp4_selftest_bounded_wait",
 )
 
 
@@ -65,6 +65,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                     _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_sz, _c_vp]),
         "fp4_linear_wgrad_dge": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64,
                                           _c_i64, _c_f, _c_f, _c_vp, _c_i64, _c_vp]),
+        "fp4_linear_dgrad": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64,
+                                      _c_vp]),
         "fp4_device_status": (_c_int, [_c_vp, ctypes.POINTER(_c_u32)]),
         "fp4_selftest_bounded_wait": (_c_int, [_c_u32, _c_vp]),
     }
@@ -284,6 +286,26 @@ def fp4_linear_wgrad_dge(A: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, s_w
         _p(A), lda, _p(dY), lddy, _p(W), ldw, _p(s_w), M, N, K, float(dge_k), float(dge_clip), _p(dW), lddw,
         _s(stream)))
     return dW
+
+
+def fp4_linear_dgrad(dY: torch.Tensor, W: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16,
+                     dX: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """dX = dY W^T (M x K), BF16 or fp32; fp32 accumulation."""
+    lddy = _rowmajor(dY, "dY", torch.bfloat16)
+    ldw = _rowmajor(W, "W", torch.bfloat16)
+    M, N = dY.shape
+    K = W.shape[0]
+    if W.shape[1] != N:
+        raise ValueError(f"W must be K x {N} (got {tuple(W.shape)})")
+    if dX is None:
+        dX = torch.empty((M, K), dtype=out_dtype, device=dY.device)
+    if dX.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError(f"dX must be bfloat16 or float32 (got {dX.dtype})")
+    lddx = _rowmajor(dX, "dX", dX.dtype)
+    dx_type = FP4_OUT_BF16 if dX.dtype == torch.bfloat16 else FP4_OUT_FP32
+    _check("fp4_linear_dgrad", _lib.fp4_linear_dgrad(
+        _p(dY), lddy, _p(W), ldw, M, N, K, _p(dX), dx_type, lddx, _s(stream)))
+    return dX
 
 
 # ---------------------------------------------------------------- status

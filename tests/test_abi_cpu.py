@@ -29,7 +29,7 @@ def _declared_functions():
 def test_header_declares_the_hot_path_entry_points():
     names = set(_declared_functions())
     for fn in ("fp4_quantize_rows", "fp4_quantize_cols", "outlier_clamp_quantile", "fp4_linear_fwd",
-               "fp4_linear_wgrad_dge"):
+               "fp4_linear_wgrad_dge", "fp4_linear_dgrad"):
         assert fn in names
 
 
@@ -121,5 +121,11 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
                             fake, 16, None) == 4
     # DGE parameters
     assert L.fp4_linear_wgrad_dge(fake, 64, fake, 8, fake, 8, fake, 4, 8, 64, 0.0, 3.0, fake, 8, None) == 1
+    # input gradient: raw accumulator is not an output type; ragged N; misaligned leading dimension
+    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 64, 16, fake, 2, 16, None) == 1
+    assert L.fp4_linear_dgrad(None, 64, fake, 64, 4, 64, 16, fake, 0, 16, None) == 1
+    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 60, 16, fake, 0, 16, None) == 2
+    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 64, 16, fake, 0, 12, None) == 2
+    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 64, 16, fake, 1, 20, None) == 3
     assert L.fp4_quantize_cols(fake, 64, 12, 16, fake, 32, fake, fake, 1 << 10, None) == 2
     assert L.fp4_selftest_bounded_wait(0, None) == 1

@@ -8,7 +8,8 @@ Student-t stress case), run through the same launches bench.py times
 * row codes / scales bit-exact on sampled rows; column codes / scales bit-exact
   on sampled columns;
 * raw FP4 accumulators bit-exact, BF16 Y (1 ulp + fp32 sum bound) on sampled rows;
-* DGE weight gradient within 1e-5 relative Frobenius on sampled feature rows.
+* DGE weight gradient within 1e-5 relative Frobenius on sampled feature rows;
+* BF16 input gradient dY W^T within 1 ulp + the tensor-core sum bound on sampled rows.
 """
 import types
 
@@ -18,8 +19,8 @@ import torch
 
 from oracle import fp4_linear as orc
 from precision_gemm_row_gb300 import workloads as wl
-from tests.gpu_common import (FROB_TOL, assert_bf16_compensated_close, assert_no_device_flags, dev_bf16, host_bits,
-                              rel_frobenius)
+from tests.gpu_common import (FROB_TOL, TC_SUM_BOUND, assert_bf16_compensated_close, assert_no_device_flags,
+                              dev_bf16, host_bits, rel_frobenius)
 
 pytestmark = pytest.mark.gpu
 
@@ -117,4 +118,9 @@ def test_full_size_linear(fp4, workload, linear):
     dw_ref = orc.wgrad_dge(A_bits, dY_bits, W_bits, s_w, 5.0, 3.0, rows=frows)
     dw_gpu = step.dW[torch.from_numpy(frows).cuda()].cpu().numpy()
     assert rel_frobenius(dw_gpu, dw_ref) <= FROB_TOL
+    # input gradient on sampled token rows
+    dx_ref = orc.linear_dgrad(dY_bits, W_bits, rows=rows)
+    dx_mag = orc.linear_dgrad(dY_bits & np.uint16(0x7FFF), W_bits & np.uint16(0x7FFF), rows=rows)
+    assert_bf16_compensated_close(host_bits(step.dX[torch.from_numpy(rows).cuda()]), dx_ref, dx_mag,
+                                  bound=TC_SUM_BOUND)
     assert_no_device_flags(fp4)

@@ -8,8 +8,8 @@ import torch
 
 from oracle import fp4_linear as orc
 from precision_gemm_row_gb300 import workloads as wl
-from tests.gpu_common import (BF16_ULP_TOL, FROB_TOL, assert_bf16_compensated_close, assert_no_device_flags,
-                              bf16_ulp_distance, dev_bf16, host_bits, rel_frobenius)
+from tests.gpu_common import (BF16_ULP_TOL, FROB_TOL, TC_SUM_BOUND, assert_bf16_compensated_close,
+                              assert_no_device_flags, bf16_ulp_distance, dev_bf16, host_bits, rel_frobenius)
 
 pytestmark = pytest.mark.gpu
 
@@ -246,6 +246,68 @@ def test_wgrad_dge(fp4, M, K, N, k, clip):
     ref = orc.wgrad_dge(A_bits, dY_bits, W_bits, s_w, k, clip)
     err = rel_frobenius(dW.cpu().numpy(), ref)
     assert err <= FROB_TOL, err
+    assert_no_device_flags(fp4)
+
+
+# ---------------------------------------------------------------- input gradient
+
+def _dgrad_ref(dY_bits, W_bits):
+    ref = orc.linear_dgrad(dY_bits, W_bits)
+    mag = orc.linear_dgrad(dY_bits & np.uint16(0x7FFF), W_bits & np.uint16(0x7FFF))
+    return ref, mag
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 128, 256), (200, 264, 136), (1000, 520, 392), (5, 8, 8), (129, 72, 1032),
+                                   (300, 2056, 264), (2304, 4104, 520), (513, 16384, 8)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_dgrad(fp4, M, N, K, out):
+    """N >= 2048 (a long reduction) runs CTA pairs (256-row tiles); M = 200, 1000,
+    300, 2304, 513 leave partial row tiles, K = 136, 392, 264, 520, 8 partial
+    column tiles, N = 264, 72, 2056, 4104 a partial last stage of 64."""
+    dY_bits = _normal_bits(M + 7, (M, N), 1e-3)
+    W_bits = _normal_bits(K + 11, (K, N), 0.02)
+    dX = fp4.fp4_linear_dgrad(dev_bf16(dY_bits), dev_bf16(W_bits),
+                              out_dtype=torch.bfloat16 if out == "bf16" else torch.float32)
+    assert dX.shape == (M, K)
+    ref, mag = _dgrad_ref(dY_bits, W_bits)
+    if out == "bf16":
+        assert_bf16_compensated_close(host_bits(dX), ref, mag, bound=TC_SUM_BOUND)
+        got = orc.bf16_to_f32(host_bits(dX)).astype(np.float64)
+        # rounding to BF16 dominates: the fp32 sums are far inside half an ulp
+        assert rel_frobenius(got, ref) <= 2.0 ** -8
+    else:
+        got = dX.cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - ref) <= TC_SUM_BOUND * mag)
+        assert rel_frobenius(got, ref) <= FROB_TOL
+    assert_no_device_flags(fp4)
+
+
+def test_dgrad_exact_on_integer_products(fp4):
+    """Small integers: every product and partial sum is exact in fp32, so dX is
+    the exact integer matrix bit for bit (checks operand order and tile
+    placement without rounding in the way)."""
+    M, N, K = 384, 4096, 264
+    rng = np.random.default_rng(3)
+    dY = rng.integers(-3, 4, size=(M, N)).astype(np.float32)
+    W = rng.integers(-3, 4, size=(K, N)).astype(np.float32)
+    dY_bits, W_bits = wl.f32_to_bf16_bits(dY), wl.f32_to_bf16_bits(W)
+    dX = fp4.fp4_linear_dgrad(dev_bf16(dY_bits), dev_bf16(W_bits), out_dtype=torch.float32)
+    ref = orc.linear_dgrad(dY_bits, W_bits)
+    assert np.array_equal(dX.cpu().numpy(), ref.astype(np.float32))
+    assert_no_device_flags(fp4)
+
+
+def test_dgrad_output_leading_dimension(fp4):
+    """dX written into a wider buffer: the columns past K keep their canary."""
+    M, N, K, ld = 300, 520, 264, 272
+    dY_bits = _normal_bits(1, (M, N), 1e-3)
+    W_bits = _normal_bits(2, (K, N), 0.02)
+    buf = torch.full((M, ld), -7.0, dtype=torch.float32, device="cuda")
+    fp4.fp4_linear_dgrad(dev_bf16(dY_bits), dev_bf16(W_bits), dX=buf[:, :K])
+    ref, mag = _dgrad_ref(dY_bits, W_bits)
+    host = buf.cpu().numpy()
+    assert np.all(host[:, K:] == -7.0)
+    assert np.all(np.abs(host[:, :K].astype(np.float64) - ref) <= TC_SUM_BOUND * mag)
     assert_no_device_flags(fp4)
 
 

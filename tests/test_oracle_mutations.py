@@ -151,3 +151,13 @@ def test_unscaled_weight_in_dge_is_caught(monkeypatch):
 
     monkeypatch.setattr(orc, "wgrad_dge", unscaled)
     _expect_failure(pins.test_wgrad_factor_symmetric_in_sign_and_uses_scaled_weight)
+
+
+def test_untransposed_weight_in_dgrad_is_caught(monkeypatch):
+    def no_transpose(dY_bits, W_bits, rows=None, cols=None):
+        dY = orc.bf16_to_f32(dY_bits).astype(np.float64)
+        W = orc.bf16_to_f32(W_bits).astype(np.float64)
+        return dY @ W        # dY W instead of dY W^T (same shape when K = N)
+
+    monkeypatch.setattr(orc, "linear_dgrad", no_transpose)
+    _expect_failure(pins.test_dgrad_is_the_adjoint_of_the_forward_product, 24, 24)

@@ -421,3 +421,49 @@ def test_wgrad_factor_symmetric_in_sign_and_uses_scaled_weight():
             assert dW[r, j] == np.float32(G[r, j] * float(orc.dge_derivative(np.array([x]), 5.0, 3.0)[0]))
     sub = orc.wgrad_dge(A, dY, W, s_w, 5.0, 3.0, rows=[4, 1], cols=[0, 3])
     assert np.array_equal(sub, dW[np.ix_([4, 1], [0, 3])])
+
+
+# ---------------------------------------------------------------- input gradient (reading R16)
+
+def test_dgrad_bruteforce_fractions():
+    """Every entry against an exact rational sum of the BF16 products."""
+    rng = np.random.default_rng(21)
+    M, N, K = 3, 9, 4
+    dY_bits = orc.f64_to_bf16(rng.standard_normal((M, N)) * 1e-3)
+    W_bits = orc.f64_to_bf16(rng.standard_normal((K, N)) * 0.02)
+    dY = orc.bf16_to_f32(dY_bits)
+    W = orc.bf16_to_f32(W_bits)
+    got = orc.linear_dgrad(dY_bits, W_bits)
+    assert got.shape == (M, K)
+    for m in range(M):
+        for k in range(K):
+            exact = sum(Fraction(float(dY[m, n])) * Fraction(float(W[k, n])) for n in range(N))
+            assert got[m, k] == float(exact)
+
+
+@pytest.mark.parametrize("K,N", [(24, 24), (16, 40), (40, 16)])
+def test_dgrad_is_the_adjoint_of_the_forward_product(K, N):
+    """The input gradient of L = <dY, X W> is the unique G with <G, X> = <dY, X W>
+    for every X; a transposed or swapped operand breaks this (the square case
+    K = N catches W in place of W^T)."""
+    rng = np.random.default_rng(K * 100 + N)
+    M = 7
+    dY_bits = orc.f64_to_bf16(rng.standard_normal((M, N)))
+    W_bits = orc.f64_to_bf16(rng.standard_normal((K, N)))
+    G = orc.linear_dgrad(dY_bits, W_bits)
+    dY = orc.bf16_to_f32(dY_bits).astype(np.float64)
+    W = orc.bf16_to_f32(W_bits).astype(np.float64)
+    for trial in range(3):
+        X = rng.standard_normal((M, K))
+        lhs = float(np.sum(G * X))
+        rhs = float(np.sum(dY * (X @ W)))
+        assert abs(lhs - rhs) <= 1e-12 * (np.sum(np.abs(G) * np.abs(X)) + 1.0)
+
+
+def test_dgrad_sampled_rows_cols_match_full():
+    rng = np.random.default_rng(5)
+    dY_bits = orc.f64_to_bf16(rng.standard_normal((20, 48)))
+    W_bits = orc.f64_to_bf16(rng.standard_normal((12, 48)))
+    full = orc.linear_dgrad(dY_bits, W_bits)
+    rows, cols = [0, 7, 19], [11, 2]
+    assert np.array_equal(orc.linear_dgrad(dY_bits, W_bits, rows=rows, cols=cols), full[np.ix_(rows, cols)])
