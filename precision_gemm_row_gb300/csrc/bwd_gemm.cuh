@@ -20,14 +20,18 @@
 // (round to nearest), so the error stays at the chunk level.  While the
 // epilogue drains one buffer the MMA warp fills the other.
 //
-// Roles (10 warps): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
-// warps 2-9 epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (one output row per
-// thread) and columns (w-2)/4 * 128 .. +127 of the 256-wide tile, adding each
+// Roles (18 warps): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
+// warps 2-17 epilogue: warp w reads TMEM lanes 32*(w%4)..+31 (one output row per
+// thread) and columns (w-2)/4 * 64 .. +63 of the 256-wide tile, adding each
 // chunk into fp32 registers.  After the last chunk of a tile the warp hands its
-// sums, 32 x 32 blocks at a time, through a swizzled staging tile to the
+// sums, 16 rows x 32 columns at a time, through a swizzled staging tile to the
 // epilogue functor, which sees coalesced row chunks (lane l: 4 columns, chunk
 // l % 8, of rows l / 8 + 4 i), while the tensor core already fills both TMEM
-// buffers with the next tile.  Every mbarrier wait is bounded; on expiry the
+// buffers with the next tile.  Sixteen epilogue warps (64 sums per thread, not
+// 128) keep this final pass short enough to hide behind the two chunks the
+// tensor core accumulates meanwhile; with eight, the DGE factor arithmetic
+// (latency-bound at two warps per scheduler) stalled the MMAs at every tile.
+// Every mbarrier wait is bounded; on expiry the
 // CTA records FP4_FLAG_TIMEOUT, drains its TMA loads and MMAs, frees TMEM and
 // exits.
 //
@@ -38,8 +42,10 @@
 // columns.  Short reduction loops run single-CTA 128 x 256 tiles.
 //
 // The epilogue functor provides
+//   void prefetch(int row0, int col0, int lane) const;    called when a tile's last chunk starts:
+//                                                          the warp's 32 rows x 64 columns follow
 //   struct Pre;                                           values loaded before the block is staged
-//   Pre load(int row0, int gcol, bool col_ok, int lane) const;   rows row0 + lane / 8 + 4 i (i < 8)
+//   Pre load(int row0, int gcol, bool col_ok, int lane) const;   rows row0 + lane / 8 + 4 i (i < 4)
 //   void store(const Pre&, int i, int grow, int gcol, float4 g) const;   4 results of row grow
 #pragma once
 
@@ -52,18 +58,19 @@ constexpr int kBM = 128;      // output rows per CTA tile
 constexpr int kBN = 256;      // output columns per tile
 constexpr int kBT = 64;       // reduction elements per stage
 constexpr int kMmaT = 16;     // reduction elements per MMA (BF16 K = 16)
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = 64 + 32 * kEpiWarps;   // 576 (18 warps: up to 5 per scheduler, so 96 registers)
 constexpr int kNAcc = 2;
 constexpr int kChunkStages = 16;                 // 1024 reduction elements per TMEM accumulation chunk
-constexpr int kEpiCols = kBN / 2;                // columns per epilogue warp
-constexpr int kBlk = 32;                         // epilogue block: 32 rows x 32 columns per warp
+constexpr int kEpiCols = kBN / (kEpiWarps / 4);  // columns per epilogue warp (64)
+constexpr int kBlk = 32;                         // epilogue block: 32 rows x 32 columns per warp,
+constexpr int kHalf = 16;                        // staged 16 rows at a time
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 64;                          // elements per TMA box side (128 bytes of BF16)
 constexpr int kBoxBytes = kBox * kBT * 2;         // 8 KB
-// epilogue staging per warp: one 32 x 32 fp32 block (128-byte swizzle), read
+// epilogue staging per warp: 16 rows x 32 fp32 columns (128-byte swizzle), read
 // back as coalesced row chunks (TMA stays free for the main loop's stages)
-constexpr int kOutBytes = kBlk * kBlk * 4;        // 4 KB
+constexpr int kOutBytes = kHalf * kBlk * 4;       // 2 KB
 constexpr int kEpiWarpBytes = kOutBytes;
 constexpr int kGroupRows = 8;                     // tile raster: groups of 8 row blocks
 
@@ -270,7 +277,7 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
     const int q = warp & 3;
     const int c_base = (ew / 4) * kEpiCols;
     const uint32_t lane_base = uint32_t(q * 32) << 16;
-    uint8_t* out_s = sEpi + ew * kEpiWarpBytes;          // 32 x 32 fp32, 128-byte swizzle
+    uint8_t* out_s = sEpi + ew * kEpiWarpBytes;          // 16 x 32 fp32, 128-byte swizzle
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -283,6 +290,8 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
 #pragma unroll
       for (int c = 0; c < kEpiCols; ++c) sum[c] = 0.0f;
       for (int lb0 = 0; lb0 < lblocks; lb0 += kChunkStages) {
+        // what the final pass reads is fetched into L2 while the last chunk accumulates
+        if (lb0 + kChunkStages >= lblocks) epi.prefetch(row0, nb * kBN + c_base, lane);
         // the warp leaves the wait converged and with one verdict (tcgen05.ld is warp-wide)
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns))) {
           ok = false;
@@ -319,23 +328,30 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
         if (col0 >= p.C) break;  // same for the whole warp
         const int c = lane & 7, gcol = col0 + 4 * c;
         const bool col_ok = gcol < p.C;   // C % 8 == 0: the 4 columns are all in or all out
-        // the functor's loads first (one memory latency), then the staging
-        const typename Epi::Pre pre = epi.load(row0, gcol, col_ok, lane);
-        __syncwarp();  // the staging tile is free
-        uint8_t* orow = out_s + lane * 128;   // this lane's row: chunk k at k ^ (lane & 7)
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          *reinterpret_cast<float4*>(orow + ((k ^ (lane & 7)) << 4)) =
-              make_float4(sum[j * kBlk + 4 * k], sum[j * kBlk + 4 * k + 1], sum[j * kBlk + 4 * k + 2],
-                          sum[j * kBlk + 4 * k + 3]);
-        __syncwarp();
+        for (int h = 0; h < kBlk / kHalf; ++h) {
+          const int hrow0 = row0 + h * kHalf;
+          // the functor's loads first (one memory latency), then the staging
+          const typename Epi::Pre pre = epi.load(hrow0, gcol, col_ok, lane);
+          __syncwarp();  // the staging tile is free
+          if ((lane >> 4) == h) {
+            // lanes 16h..16h+15 hold rows 16h..16h+15: staged row lane % 16, chunk k at k ^ (lane & 7)
+            uint8_t* orow = out_s + (lane & (kHalf - 1)) * 128;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = (lane >> 3) + 4 * i;
-          const int grow = row0 + r;
-          if (grow < p.R && col_ok) {
-            const float4 g = *reinterpret_cast<const float4*>(out_s + r * 128 + ((c ^ (r & 7)) << 4));
-            epi.store(pre, i, grow, gcol, g);
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<float4*>(orow + ((k ^ (lane & 7)) << 4)) =
+                  make_float4(sum[j * kBlk + 4 * k], sum[j * kBlk + 4 * k + 1], sum[j * kBlk + 4 * k + 2],
+                              sum[j * kBlk + 4 * k + 3]);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < kHalf / 4; ++i) {
+            const int r = (lane >> 3) + 4 * i;
+            const int grow = hrow0 + r;
+            if (grow < p.R && col_ok) {
+              const float4 g = *reinterpret_cast<const float4*>(out_s + r * 128 + ((c ^ (r & 7)) << 4));
+              epi.store(pre, i, grow, gcol, g);
+            }
           }
         }
       }

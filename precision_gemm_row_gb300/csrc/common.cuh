@@ -108,6 +108,10 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 // has finished reading its shared-memory source.
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // Hint: bring the global-memory line holding `ptr` into L1 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ void prefetch_l1(const void* ptr) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
 }

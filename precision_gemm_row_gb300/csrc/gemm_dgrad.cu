@@ -21,6 +21,7 @@ struct StoreEpilogue {
   int64_t ld;   // elements
   bool bf16;
 
+  __device__ __forceinline__ void prefetch(int, int, int) const {}
   struct Pre {};
   __device__ __forceinline__ Pre load(int, int, bool, int) const { return Pre{}; }
   __device__ __forceinline__ void store(const Pre&, int, int grow, int gcol, float4 g) const {

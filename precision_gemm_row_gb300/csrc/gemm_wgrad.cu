@@ -42,19 +42,27 @@ struct DgeEpilogue {
   const float* s_w;
   float* dW;
   int64_t lddw;
-  int rows;   // K
+  int rows, cols;   // K, N
   float inv_k, expo, clip, pw0;
+
+  // W rows row0..row0+31 (columns col0..col0+63: one 128-byte line per row)
+  // and s_w[col0..col0+63] (two lines) into L2
+  __device__ __forceinline__ void prefetch(int row0, int col0, int lane) const {
+    const int grow = row0 + lane;
+    if (grow < rows && col0 < cols) prefetch_l2(W + int64_t(grow) * ldw + col0);
+    if (lane < 2 && col0 + 32 * lane < cols) prefetch_l2(s_w + col0 + 32 * lane);
+  }
 
   struct Pre {
     float4 sw;
-    uint2 w[8];
+    uint2 w[4];
   };
   __device__ __forceinline__ Pre load(int row0, int gcol, bool col_ok, int lane) const {
     Pre pr;
     pr.sw = make_float4(1.f, 1.f, 1.f, 1.f);
     if (col_ok) pr.sw = make_float4(__ldg(s_w + gcol), __ldg(s_w + gcol + 1), __ldg(s_w + gcol + 2), __ldg(s_w + gcol + 3));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
       const int grow = row0 + (lane >> 3) + 4 * i;
       pr.w[i] = (col_ok && grow < rows) ? __ldg(reinterpret_cast<const uint2*>(W + int64_t(grow) * ldw + gcol))
                                         : make_uint2(0u, 0u);
@@ -110,6 +118,7 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   e.dW = dW;
   e.lddw = lddw;
   e.rows = int(K);
+  e.cols = int(N);
   e.inv_k = 1.0f / dge_k;
   e.expo = 1.0f / dge_k - 1.0f;
   e.clip = dge_clip;
