@@ -163,6 +163,10 @@ class LinStep:
         self.ws_fwd = torch.empty(fp4.fp4_linear_fwd_workspace(lin.M, N, K), dtype=torch.uint8, device=dev)
         self.dW = torch.empty((K, N), dtype=torch.float32, device=dev)
         self.dX = torch.empty((lin.M, K), dtype=torch.bfloat16, device=dev)
+        # split-tail workspaces of the backward GEMMs (None when the shapes never split)
+        wb, db = fp4.fp4_linear_wgrad_dge_workspace(lin.M, N, K), fp4.fp4_linear_dgrad_workspace(lin.M, N, K)
+        self.ws_wgrad = torch.empty(wb, dtype=torch.uint8, device=dev) if wb else None
+        self.ws_dgrad = torch.empty(db, dtype=torch.uint8, device=dev) if db else None
 
     def fns(self):
         fp4, lin, a = self.fp4, self.lin, self.act
@@ -170,8 +174,9 @@ class LinStep:
             lambda: fp4.fp4_quantize_cols(self.W, codes_t=self.w_codes, scales=self.s_w, workspace=self.ws_cols),
             lambda: fp4.fp4_linear_fwd(a.out["codes"], a.out["scales"], self.w_codes, self.s_w, lin.K, csr=a.out,
                                        W=self.W, out_type="bf16", Y=self.Y, workspace=self.ws_fwd),
-            lambda: fp4.fp4_linear_wgrad_dge(a.A, self.dY, self.W, self.s_w, DGE_K, DGE_CLIP, dW=self.dW),
-            lambda: fp4.fp4_linear_dgrad(self.dY, self.W, dX=self.dX),
+            lambda: fp4.fp4_linear_wgrad_dge(a.A, self.dY, self.W, self.s_w, DGE_K, DGE_CLIP, dW=self.dW,
+                                             workspace=self.ws_wgrad),
+            lambda: fp4.fp4_linear_dgrad(self.dY, self.W, dX=self.dX, workspace=self.ws_dgrad),
         ]
 
     def algorithmic(self):

@@ -285,13 +285,27 @@ fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_bytes, const
  *   dW  device fp32 K x lddw, 16-byte aligned, lddw % 4 == 0; written once per
  *       element while other tiles still read W and s_w, so dW must not alias
  *       A, dY, W or s_w
- * Errors: INVALID_ARG, SHAPE, ALIGNMENT, DEVICE_UNSUPPORTED, CUDA;
- *         device-side TIMEOUT flag as for fp4_linear_fwd.
+ *   workspace  device, 256-byte aligned, ws_bytes >= fp4_linear_wgrad_dge_workspace(M, N, K),
+ *       or NULL.  With it, a last wave of tiles that would leave at least half
+ *       of the SM pairs idle is computed as two halves of the token range on
+ *       two pairs, combined through the workspace (the result is the same
+ *       whichever half finishes first).  Must not be shared by calls that may
+ *       run at the same time; owned by the caller.
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE (non-NULL and too small),
+ *         DEVICE_UNSUPPORTED, CUDA; device-side TIMEOUT flag as for fp4_linear_fwd.
  */
 fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* dY, int64_t lddy, const void* W,
                                 int64_t ldw, const float* s_w, int64_t M, int64_t N, int64_t K,
                                 float dge_k, float dge_clip, float* dW, int64_t lddw,
-                                fp4_stream_t stream);
+                                void* workspace, size_t ws_bytes, fp4_stream_t stream);
+
+/*
+ * fp4_linear_wgrad_dge_workspace -- bytes of workspace fp4_linear_wgrad_dge
+ * uses for these sizes on the current device (0: it never splits a tile, and
+ * a NULL workspace is as good).  Returns 0 for non-positive sizes or an
+ * unsupported device.
+ */
+size_t fp4_linear_wgrad_dge_workspace(int64_t M, int64_t N, int64_t K);
 
 /*
  * fp4_linear_dgrad -- BF16 input-gradient GEMM on tcgen05 (kind::f16):
@@ -310,12 +324,21 @@ fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* dY, int6
  *   dX  device M x lddx (tokens x in) of dx_type, 16-byte aligned, lddx % 8 == 0,
  *       lddx >= K; must not alias dY or W
  *   dx_type  FP4_OUT_BF16 (round to nearest even) or FP4_OUT_FP32
+ *   workspace  device, 256-byte aligned, ws_bytes >= fp4_linear_dgrad_workspace(M, N, K),
+ *       or NULL: the split tail of fp4_linear_wgrad_dge, over the N range
  * Errors: INVALID_ARG (null pointer, other dx_type), SHAPE, ALIGNMENT,
- *         DEVICE_UNSUPPORTED, CUDA; device-side TIMEOUT flag as for fp4_linear_fwd.
+ *         WORKSPACE (non-NULL and too small), DEVICE_UNSUPPORTED, CUDA;
+ *         device-side TIMEOUT flag as for fp4_linear_fwd.
  */
 fp4_status fp4_linear_dgrad(const void* dY, int64_t lddy, const void* W, int64_t ldw, int64_t M,
                             int64_t N, int64_t K, void* dX, int dx_type, int64_t lddx,
-                            fp4_stream_t stream);
+                            void* workspace, size_t ws_bytes, fp4_stream_t stream);
+
+/*
+ * fp4_linear_dgrad_workspace -- bytes of workspace fp4_linear_dgrad uses for
+ * these sizes on the current device (0 when it never splits a tile).
+ */
+size_t fp4_linear_dgrad_workspace(int64_t M, int64_t N, int64_t K);
 
 /*
  * fp4_device_status -- synchronize `stream`, then return the sticky device

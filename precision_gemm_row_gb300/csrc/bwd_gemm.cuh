@@ -35,6 +35,14 @@
 // CTA records FP4_FLAG_TIMEOUT, drains its TMA loads and MMAs, frees TMEM and
 // exits.
 //
+// Split tail: when the last wave of tiles would occupy at most half of the CTA
+// pairs, each of its tiles is computed as two halves of the reduction range on
+// two pairs (work items after the whole tiles, one per pair).  Each half
+// publishes its fp32 sums to the caller's workspace and counts itself in; the
+// half that counts second adds the other's sums to its own (a + b, so the
+// result does not depend on which half finishes first) and runs the epilogue.
+// No CTA ever waits for another.
+//
 // PAIR: tiles of 256 x 256 per CTA pair (a cluster of two CTAs on two SMs): each
 // CTA loads its 128 rows of P and 128 of the tile's 256 rows of Q per stage (32
 // KB instead of 48 KB for the same MMA work), the leader issues M = 256
@@ -96,9 +104,39 @@ struct Cfg {
 
 struct Shape {
   int R, C, L;        // output rows, output columns, reduction length
+  int whole, split;   // tiles computed whole, then `split` tiles computed as two halves
+  float* part;        // split > 0: the halves' partial sums (SplitPlan layout)
+  uint32_t* cnt;      // split > 0: one arrival counter per tile, warp and CTA, zeroed before launch
   uint32_t* status;
   uint64_t wait_ns;
 };
+
+// One unit of a pair's work: a whole tile (slot < 0) or one half of a split
+// tile (slot = 2 x split index + half) over chunks [c0, c1).
+struct Work {
+  int tile, c0, c1, slot;
+};
+
+// Work items are dealt round robin: items [0, whole) are whole tiles and
+// [whole, whole + 2 split) the halves.  whole is a multiple of the number of
+// pairs whenever split > 0, so every half runs in the last round on its own pair.
+__device__ __forceinline__ bool work_item(int k, int pair_id, int npairs, int nchunks, const Shape& p, Work& w) {
+  const int item = pair_id + k * npairs;
+  if (item < p.whole) {
+    w.tile = item;
+    w.c0 = 0;
+    w.c1 = nchunks;
+    w.slot = -1;
+    return true;
+  }
+  const int s = item - p.whole;
+  if (s >= 2 * p.split) return false;
+  w.tile = p.whole + (s >> 1);
+  w.c0 = (s & 1) ? nchunks / 2 : 0;
+  w.c1 = (s & 1) ? nchunks : nchunks / 2;
+  w.slot = s;
+  return true;
+}
 
 // Tile t -> (row block, column block): groups of kGroupRows row blocks, row
 // blocks fastest within a group, so the CTAs running at one time share few
@@ -156,8 +194,8 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
   constexpr int kTileR = kBM * C::kCtas;   // output rows per tile (per pair)
   const int num_r = (p.R + kTileR - 1) / kTileR;
   const int num_n = (p.C + kBN - 1) / kBN;
-  const int tiles = num_r * num_n;
   const int lblocks = (p.L + kBT - 1) / kBT;
+  const int nchunks = (lblocks + kChunkStages - 1) / kChunkStages;
   const int pair_id = int(blockIdx.x) / C::kCtas, npairs = int(gridDim.x) / C::kCtas;
 
   if (warp == 0) {
@@ -166,12 +204,14 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
     uint32_t phase = 0;
     uint32_t issued = 0;
     bool ok = true;
-    for (int tile = pair_id; tile < tiles && ok; tile += npairs) {
+    Work w;
+    for (int k = 0; ok && work_item(k, pair_id, npairs, nchunks, p, w); ++k) {
       int rb, nb;
-      tile_coords(tile, num_r, num_n, rb, nb);
+      tile_coords(w.tile, num_r, num_n, rb, nb);
       const int arow = rb * kTileR + int(rank) * kBM;          // this CTA's 128 rows of P
       const int bcol = nb * kBN + int(rank) * C::kBCols;       // this CTA's rows of Q
-      for (int lb = 0; lb < lblocks; ++lb) {
+      const int lb_end = w.c1 * kChunkStages < lblocks ? w.c1 * kChunkStages : lblocks;
+      for (int lb = w.c0 * kChunkStages; lb < lb_end; ++lb) {
         if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
           ok = false;
           break;
@@ -220,8 +260,10 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
     uint32_t acc_phase = 0;
     bool ok = true;
     const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-    for (int tile = pair_id; tile < tiles && ok; tile += npairs) {
-      for (int lb0 = 0; lb0 < lblocks && ok; lb0 += kChunkStages) {
+    Work w;
+    for (int k = 0; ok && work_item(k, pair_id, npairs, nchunks, p, w); ++k) {
+      for (int ch = w.c0; ch < w.c1 && ok; ++ch) {
+        const int lb0 = ch * kChunkStages;
         const int lb1 = lb0 + kChunkStages < lblocks ? lb0 + kChunkStages : lblocks;
         if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
           ok = false;
@@ -282,16 +324,17 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
     uint32_t acc_phase = 0;
     bool ok = true;
     constexpr int kNBlk = kEpiCols / kBlk;
-    for (int tile = pair_id; tile < tiles && ok; tile += npairs) {
+    Work w;
+    for (int k = 0; ok && work_item(k, pair_id, npairs, nchunks, p, w); ++k) {
       int rb, nb;
-      tile_coords(tile, num_r, num_n, rb, nb);
+      tile_coords(w.tile, num_r, num_n, rb, nb);
       const int row0 = rb * kTileR + int(rank) * kBM + q * 32;  // first output row of this warp's 32-row slab
       float sum[kEpiCols];
 #pragma unroll
       for (int c = 0; c < kEpiCols; ++c) sum[c] = 0.0f;
-      for (int lb0 = 0; lb0 < lblocks; lb0 += kChunkStages) {
+      for (int ch = w.c0; ch < w.c1; ++ch) {
         // what the final pass reads is fetched into L2 while the last chunk accumulates
-        if (lb0 + kChunkStages >= lblocks) epi.prefetch(row0, nb * kBN + c_base, lane);
+        if (ch + 1 == w.c1) epi.prefetch(row0, nb * kBN + c_base, lane);
         // the warp leaves the wait converged and with one verdict (tcgen05.ld is warp-wide)
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(accf0 + 8 * acc, acc_phase, p.wait_ns))) {
           ok = false;
@@ -319,9 +362,37 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
         }
       }
       if (!ok) break;
+      if (row0 >= p.R) continue;
+      if (w.slot >= 0) {
+        // half of a split tile: publish this warp's sums (thread-major, coalesced),
+        // count in, and finish the tile only if the other half is already in
+        constexpr int kVec = kEpiCols / 4;
+        const size_t wbase = ((size_t(w.slot) * C::kCtas + rank) * kEpiWarps + ew) * kVec * 32;
+        float4* mine = reinterpret_cast<float4*>(p.part) + wbase;
+#pragma unroll
+        for (int v = 0; v < kVec; ++v)
+          mine[v * 32 + lane] = make_float4(sum[4 * v], sum[4 * v + 1], sum[4 * v + 2], sum[4 * v + 3]);
+        __threadfence();   // each lane's stores are visible before the count
+        __syncwarp();
+        uint32_t before = 0;
+        if (lane == 0)
+          before = atomicAdd(p.cnt + (size_t(w.slot >> 1) * C::kCtas + rank) * kEpiWarps + ew, 1u);
+        before = __shfl_sync(0xFFFFFFFFu, before, 0);
+        if (before == 0) continue;   // the other half finishes these rows
+        __threadfence();
+        const float4* other = reinterpret_cast<const float4*>(p.part) +
+                              ((size_t(w.slot ^ 1) * C::kCtas + rank) * kEpiWarps + ew) * kVec * 32;
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+          const float4 o = __ldcg(other + v * 32 + lane);
+          sum[4 * v] += o.x;
+          sum[4 * v + 1] += o.y;
+          sum[4 * v + 2] += o.z;
+          sum[4 * v + 3] += o.w;
+        }
+      }
       // the sums go through the staging tile to the functor as coalesced row
       // chunks; this runs while the tensor core starts the next tile
-      if (row0 >= p.R) continue;
 #pragma unroll
       for (int j = 0; j < kNBlk; ++j) {
         const int col0 = nb * kBN + c_base + j * kBlk;
@@ -369,10 +440,56 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
   }
 }
 
-// Launches kernel<...> (a __global__ wrapper of run) on min(tiles, SMs) CTAs,
-// in clusters of two when PAIR.
+// ------------------------------------------------------------------ host side
+
+// CTA pairs once the reduction loop is long (32 or more stages of 64); short
+// loops keep single-CTA tiles.
+inline bool use_pairs(int64_t red) { return red >= 2048; }
+
+// Tile count, split tail and workspace layout of one backward GEMM on a device
+// with `sms` SMs: [counters, 256-byte aligned][partial sums].
+struct SplitPlan {
+  int64_t tiles, units, whole, split;
+  size_t cnt_bytes, part_bytes, total;
+};
+
+inline SplitPlan plan_split(int64_t rows, int64_t cols, int64_t red, int sms) {
+  const int ctas = use_pairs(red) ? 2 : 1;
+  SplitPlan sp{};
+  sp.tiles = ((rows + kBM * ctas - 1) / (kBM * ctas)) * ((cols + kBN - 1) / kBN);
+  sp.units = sms / ctas;
+  const int64_t nchunks = ((red + kBT - 1) / kBT + kChunkStages - 1) / kChunkStages;
+  const int64_t rem = sp.tiles % sp.units;
+  sp.split = (nchunks >= 2 && rem > 0 && 2 * rem <= sp.units) ? rem : 0;
+  sp.whole = sp.tiles - sp.split;
+  sp.cnt_bytes = (size_t(sp.split) * ctas * kEpiWarps * 4 + 255) / 256 * 256;
+  sp.part_bytes = size_t(2 * sp.split) * ctas * kEpiWarps * kEpiCols * 32 * 4;
+  sp.total = sp.split ? sp.cnt_bytes + sp.part_bytes : 0;
+  return sp;
+}
+
+// Checks the caller's workspace against the plan and fills the schedule of
+// `s`: the split tail when the workspace is given, else every tile whole.
+inline fp4_status schedule(Shape& s, const SplitPlan& sp, void* workspace, size_t ws_bytes, cudaStream_t cs) {
+  s.whole = int(sp.tiles);
+  s.split = 0;
+  s.part = nullptr;
+  s.cnt = nullptr;
+  if (workspace == nullptr || sp.split == 0) return FP4_OK;
+  if (ws_bytes < sp.total) return FP4_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FP4_ERR_ALIGNMENT;
+  s.whole = int(sp.whole);
+  s.split = int(sp.split);
+  s.cnt = static_cast<uint32_t*>(workspace);
+  s.part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + sp.cnt_bytes);
+  if (cudaMemsetAsync(s.cnt, 0, sp.cnt_bytes, cs) != cudaSuccess) return launch_status();
+  return FP4_OK;
+}
+
+// Launches kernel<...> (a __global__ wrapper of run) with one CTA (pair) per
+// work item up to one per SM (pair), in clusters of two when PAIR.
 template <bool KMAJOR, bool PAIR, class Kern, class... Args>
-fp4_status launch(Kern kern, int rows, int cols, int sms, cudaStream_t cs, Args... args) {
+fp4_status launch(Kern kern, const Shape& s, int sms, cudaStream_t cs, Args... args) {
   using C = Cfg<KMAJOR, PAIR>;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -382,11 +499,11 @@ fp4_status launch(Kern kern, int rows, int cols, int sms, cudaStream_t cs, Args.
       return FP4_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const int64_t tiles = ((int64_t(rows) + kBM * C::kCtas - 1) / (kBM * C::kCtas)) * ((int64_t(cols) + kBN - 1) / kBN);
+  const int64_t items = int64_t(s.whole) + 2 * int64_t(s.split);
   const int64_t units = sms / C::kCtas;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(unsigned(C::kCtas * (tiles < units ? tiles : units)));
+  cfg.gridDim = dim3(unsigned(C::kCtas * (items < units ? items : units)));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = cs;

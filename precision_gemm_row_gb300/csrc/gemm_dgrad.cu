@@ -50,7 +50,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
 }  // namespace fp4
 
 FP4_API fp4_status fp4_linear_dgrad(const void* dY, int64_t lddy, const void* W, int64_t ldw, int64_t M, int64_t N,
-                                    int64_t K, void* dX, int dx_type, int64_t lddx, fp4_stream_t stream) {
+                                    int64_t K, void* dX, int dx_type, int64_t lddx, void* workspace, size_t ws_bytes,
+                                    fp4_stream_t stream) {
   using namespace fp4;
   if (!dY || !W || !dX) return FP4_ERR_INVALID_ARG;
   if (dx_type != FP4_OUT_BF16 && dx_type != FP4_OUT_FP32) return FP4_ERR_INVALID_ARG;
@@ -79,9 +80,16 @@ FP4_API fp4_status fp4_linear_dgrad(const void* dY, int64_t lddy, const void* W,
   s.L = int(N);
   s.status = status_word();
   s.wait_ns = kWaitLimitNs;
-  // CTA pairs once the reduction loop is long (32 or more stages of 64); short
-  // loops keep single-CTA tiles
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (N >= 2048) return bwd::launch<true, true>(dgrad_kernel<true>, s.R, s.C, sms, cs, tmG, tmW, s, e);
-  return bwd::launch<true, false>(dgrad_kernel<false>, s.R, s.C, sms, cs, tmG, tmW, s, e);
+  st = bwd::schedule(s, bwd::plan_split(M, K, N, sms), workspace, ws_bytes, cs);
+  if (st != FP4_OK) return st;
+  if (bwd::use_pairs(N)) return bwd::launch<true, true>(dgrad_kernel<true>, s, sms, cs, tmG, tmW, s, e);
+  return bwd::launch<true, false>(dgrad_kernel<false>, s, sms, cs, tmG, tmW, s, e);
+}
+
+FP4_API size_t fp4_linear_dgrad_workspace(int64_t M, int64_t N, int64_t K) {
+  using namespace fp4;
+  int sms = 0;
+  if (M < 1 || N < 1 || K < 1 || check_device(&sms) != FP4_OK) return 0;
+  return bwd::plan_split(M, K, N, sms).total;
 }

@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
 
 FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* dY, int64_t lddy, const void* W,
                                         int64_t ldw, const float* s_w, int64_t M, int64_t N, int64_t K, float dge_k,
-                                        float dge_clip, float* dW, int64_t lddw, fp4_stream_t stream) {
+                                        float dge_clip, float* dW, int64_t lddw, void* workspace, size_t ws_bytes,
+                                        fp4_stream_t stream) {
   using namespace fp4;
   if (!A || !dY || !W || !s_w || !dW) return FP4_ERR_INVALID_ARG;
   if (!(dge_k > 0.0f) || !(dge_clip > 0.0f) || !isfinite(dge_k)) return FP4_ERR_INVALID_ARG;
@@ -129,9 +130,16 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   s.L = int(M);
   s.status = status_word();
   s.wait_ns = kWaitLimitNs;
-  // CTA pairs once the token loop is long (32 or more stages of 64 tokens); short
-  // loops keep single-CTA tiles
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (M >= 2048) return bwd::launch<false, true>(wgrad_dge_kernel<true>, s.R, s.C, sms, cs, tmA, tmG, s, e);
-  return bwd::launch<false, false>(wgrad_dge_kernel<false>, s.R, s.C, sms, cs, tmA, tmG, s, e);
+  st = bwd::schedule(s, bwd::plan_split(K, N, M, sms), workspace, ws_bytes, cs);
+  if (st != FP4_OK) return st;
+  if (bwd::use_pairs(M)) return bwd::launch<false, true>(wgrad_dge_kernel<true>, s, sms, cs, tmA, tmG, s, e);
+  return bwd::launch<false, false>(wgrad_dge_kernel<false>, s, sms, cs, tmA, tmG, s, e);
+}
+
+FP4_API size_t fp4_linear_wgrad_dge_workspace(int64_t M, int64_t N, int64_t K) {
+  using namespace fp4;
+  int sms = 0;
+  if (M < 1 || N < 1 || K < 1 || check_device(&sms) != FP4_OK) return 0;
+  return bwd::plan_split(K, N, M, sms).total;
 }

@@ -26,7 +26,8 @@ FLAG_TIMEOUT, FLAG_CAPACITY, FLAG_INTERNAL = 0x1, 0x2, 0x4
 EXPORTS = (
     "fp4_status_string", "fp4_abi_version", "fp4_last_cuda_error", "fp4_quantize_rows", "fp4_quantize_cols_workspace",
     "fp4_quantize_cols", "fp4_quantize_cols_noalloc", "outlier_max_nnz", "outlier_clamp_quantile_workspace", "outlier_clamp_quantile",
-    "fp4_quantize_rows_outliers", "fp4_linear_fwd_workspace", "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_linear_dgrad",
+    "fp4_quantize_rows_outliers", "fp4_linear_fwd_workspace", "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_linear_wgrad_dge_workspace",
+    "fp4_linear_dgrad", "fp4_linear_dgrad_workspace",
     "fp4_device_status", "fp4_selftest_bounded_wait",
 )
 
@@ -64,9 +65,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "fp4_linear_fwd": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp,
                                     _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_sz, _c_vp]),
         "fp4_linear_wgrad_dge": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64,
-                                          _c_i64, _c_f, _c_f, _c_vp, _c_i64, _c_vp]),
+                                          _c_i64, _c_f, _c_f, _c_vp, _c_i64, _c_vp, _c_sz, _c_vp]),
+        "fp4_linear_wgrad_dge_workspace": (_c_sz, [_c_i64, _c_i64, _c_i64]),
         "fp4_linear_dgrad": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64,
-                                      _c_vp]),
+                                      _c_vp, _c_sz, _c_vp]),
+        "fp4_linear_dgrad_workspace": (_c_sz, [_c_i64, _c_i64, _c_i64]),
         "fp4_device_status": (_c_int, [_c_vp, ctypes.POINTER(_c_u32)]),
         "fp4_selftest_bounded_wait": (_c_int, [_c_u32, _c_vp]),
     }
@@ -270,10 +273,35 @@ def fp4_linear_fwd(a_codes: torch.Tensor, s_a: Optional[torch.Tensor], w_codes_t
     return Y
 
 
+def _bwd_workspace(workspace, nbytes: int, device):
+    """(pointer, bytes) for the backward GEMMs' split-tail workspace: "auto"
+    allocates what the call needs (nothing when it never splits), None runs
+    without, or a caller-owned CUDA uint8 tensor."""
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', None or a CUDA uint8 tensor")
+        if nbytes == 0:
+            return None, 0
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if workspace is None:
+        return None, 0
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def fp4_linear_wgrad_dge_workspace(M: int, N: int, K: int) -> int:
+    """Bytes of split-tail workspace fp4_linear_wgrad_dge uses on the current device."""
+    return int(_lib.fp4_linear_wgrad_dge_workspace(M, N, K))
+
+
+def fp4_linear_dgrad_workspace(M: int, N: int, K: int) -> int:
+    """Bytes of split-tail workspace fp4_linear_dgrad uses on the current device."""
+    return int(_lib.fp4_linear_dgrad_workspace(M, N, K))
+
+
 def fp4_linear_wgrad_dge(A: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, s_w: torch.Tensor,
                          dge_k: float = 5.0, dge_clip: float = 3.0, dW: Optional[torch.Tensor] = None,
-                         stream=None) -> torch.Tensor:
-    """dW = (A^T dY) * f'(|W s_W|), fp32 (K x N)."""
+                         workspace="auto", stream=None) -> torch.Tensor:
+    """dW = (A^T dY) * f'(|W s_W|), fp32 (K x N).  workspace: see _bwd_workspace."""
     lda = _rowmajor(A, "A", torch.bfloat16)
     lddy = _rowmajor(dY, "dY", torch.bfloat16)
     ldw = _rowmajor(W, "W", torch.bfloat16)
@@ -282,15 +310,16 @@ def fp4_linear_wgrad_dge(A: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, s_w
     if dW is None:
         dW = torch.empty((K, N), dtype=torch.float32, device=A.device)
     lddw = _rowmajor(dW, "dW", torch.float32)
+    ws, ws_bytes = _bwd_workspace(workspace, fp4_linear_wgrad_dge_workspace(M, N, K), A.device)
     _check("fp4_linear_wgrad_dge", _lib.fp4_linear_wgrad_dge(
         _p(A), lda, _p(dY), lddy, _p(W), ldw, _p(s_w), M, N, K, float(dge_k), float(dge_clip), _p(dW), lddw,
-        _s(stream)))
+        _p(ws), ws_bytes, _s(stream)))
     return dW
 
 
 def fp4_linear_dgrad(dY: torch.Tensor, W: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16,
-                     dX: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """dX = dY W^T (M x K), BF16 or fp32; fp32 accumulation."""
+                     dX: Optional[torch.Tensor] = None, workspace="auto", stream=None) -> torch.Tensor:
+    """dX = dY W^T (M x K), BF16 or fp32; fp32 accumulation.  workspace: see _bwd_workspace."""
     lddy = _rowmajor(dY, "dY", torch.bfloat16)
     ldw = _rowmajor(W, "W", torch.bfloat16)
     M, N = dY.shape
@@ -303,8 +332,9 @@ def fp4_linear_dgrad(dY: torch.Tensor, W: torch.Tensor, out_dtype: torch.dtype =
         raise ValueError(f"dX must be bfloat16 or float32 (got {dX.dtype})")
     lddx = _rowmajor(dX, "dX", dX.dtype)
     dx_type = FP4_OUT_BF16 if dX.dtype == torch.bfloat16 else FP4_OUT_FP32
+    ws, ws_bytes = _bwd_workspace(workspace, fp4_linear_dgrad_workspace(M, N, K), dY.device)
     _check("fp4_linear_dgrad", _lib.fp4_linear_dgrad(
-        _p(dY), lddy, _p(W), ldw, M, N, K, _p(dX), dx_type, lddx, _s(stream)))
+        _p(dY), lddy, _p(W), ldw, M, N, K, _p(dX), dx_type, lddx, _p(ws), ws_bytes, _s(stream)))
     return dX
 
 

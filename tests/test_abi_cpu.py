@@ -120,12 +120,12 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert L.fp4_linear_fwd(fake, 32, fake, fake, 32, fake, 4, 8, 64, fake, fake, fake, fake, 8, fake, 0, 8,
                             fake, 16, None) == 4
     # DGE parameters
-    assert L.fp4_linear_wgrad_dge(fake, 64, fake, 8, fake, 8, fake, 4, 8, 64, 0.0, 3.0, fake, 8, None) == 1
+    assert L.fp4_linear_wgrad_dge(fake, 64, fake, 8, fake, 8, fake, 4, 8, 64, 0.0, 3.0, fake, 8, None, 0, None) == 1
     # input gradient: raw accumulator is not an output type; ragged N; misaligned leading dimension
-    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 64, 16, fake, 2, 16, None) == 1
-    assert L.fp4_linear_dgrad(None, 64, fake, 64, 4, 64, 16, fake, 0, 16, None) == 1
-    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 60, 16, fake, 0, 16, None) == 2
-    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 64, 16, fake, 0, 12, None) == 2
-    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 64, 16, fake, 1, 20, None) == 3
+    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 64, 16, fake, 2, 16, None, 0, None) == 1
+    assert L.fp4_linear_dgrad(None, 64, fake, 64, 4, 64, 16, fake, 0, 16, None, 0, None) == 1
+    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 60, 16, fake, 0, 16, None, 0, None) == 2
+    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 64, 16, fake, 0, 12, None, 0, None) == 2
+    assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 64, 16, fake, 1, 20, None, 0, None) == 3
     assert L.fp4_quantize_cols(fake, 64, 12, 16, fake, 32, fake, fake, 1 << 10, None) == 2
     assert L.fp4_selftest_bounded_wait(0, None) == 1

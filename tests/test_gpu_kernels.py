@@ -232,17 +232,20 @@ def test_fused_rows_outliers_every_finite_bf16_pattern(fp4, q):
 # ---------------------------------------------------------------- DGE weight gradient
 
 @pytest.mark.parametrize("M,K,N", [(64, 128, 256), (256, 512, 512), (200, 136, 264), (1000, 384, 520),
-                                   (2048, 200, 264), (2304, 520, 520), (4100, 384, 136)])
+                                   (1500, 1032, 520), (2048, 200, 264), (2304, 520, 520), (4100, 384, 136)])
 @pytest.mark.parametrize("k,clip", [(5.0, 3.0), (1.0, 3.0)])
-def test_wgrad_dge(fp4, M, K, N, k, clip):
+@pytest.mark.parametrize("workspace", ["auto", None])
+def test_wgrad_dge(fp4, M, K, N, k, clip, workspace):
     """M >= 2048 tokens runs the GEMM as CTA pairs (256-row dW tiles; K = 200, 520
-    and 384 leave partial pair tiles, N = 264 / 136 partial column tiles)."""
+    and 384 leave partial pair tiles, N = 264 / 136 partial column tiles).  With a
+    workspace, these few-tile shapes with 2 or more 1024-token chunks (M = 1500
+    and up) compute every tile as two halves of the token range."""
     A_bits = _normal_bits(M + 1, (M, K))
     dY_bits = _normal_bits(N + 2, (M, N), 1e-3)
     W_bits = _normal_bits(K + 3, (K, N), 0.02)
     _, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
     dW = fp4.fp4_linear_wgrad_dge(dev_bf16(A_bits), dev_bf16(dY_bits), dev_bf16(W_bits),
-                                  torch.from_numpy(s_w).cuda(), k, clip)
+                                  torch.from_numpy(s_w).cuda(), k, clip, workspace=workspace)
     ref = orc.wgrad_dge(A_bits, dY_bits, W_bits, s_w, k, clip)
     err = rel_frobenius(dW.cpu().numpy(), ref)
     assert err <= FROB_TOL, err
@@ -258,16 +261,20 @@ def _dgrad_ref(dY_bits, W_bits):
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 128, 256), (200, 264, 136), (1000, 520, 392), (5, 8, 8), (129, 72, 1032),
-                                   (300, 2056, 264), (2304, 4104, 520), (513, 16384, 8)])
+                                   (300, 1096, 264), (300, 2056, 264), (2304, 4104, 520), (513, 16384, 8)])
 @pytest.mark.parametrize("out", ["bf16", "fp32"])
-def test_dgrad(fp4, M, N, K, out):
+@pytest.mark.parametrize("workspace", ["auto", None])
+def test_dgrad(fp4, M, N, K, out, workspace):
     """N >= 2048 (a long reduction) runs CTA pairs (256-row tiles); M = 200, 1000,
     300, 2304, 513 leave partial row tiles, K = 136, 392, 264, 520, 8 partial
-    column tiles, N = 264, 72, 2056, 4104 a partial last stage of 64."""
+    column tiles, N = 264, 72, 1096, 2056, 4104 a partial last stage of 64.
+    With a workspace, shapes with 2 or more 1024-element chunks (N = 1096 and
+    up) split their few tiles into two halves of the N range (N = 2056 gives
+    halves of 1 and 2 chunks)."""
     dY_bits = _normal_bits(M + 7, (M, N), 1e-3)
     W_bits = _normal_bits(K + 11, (K, N), 0.02)
     dX = fp4.fp4_linear_dgrad(dev_bf16(dY_bits), dev_bf16(W_bits),
-                              out_dtype=torch.bfloat16 if out == "bf16" else torch.float32)
+                              out_dtype=torch.bfloat16 if out == "bf16" else torch.float32, workspace=workspace)
     assert dX.shape == (M, K)
     ref, mag = _dgrad_ref(dY_bits, W_bits)
     if out == "bf16":
@@ -279,6 +286,30 @@ def test_dgrad(fp4, M, N, K, out):
         got = dX.cpu().numpy().astype(np.float64)
         assert np.all(np.abs(got - ref) <= TC_SUM_BOUND * mag)
         assert rel_frobenius(got, ref) <= FROB_TOL
+    assert_no_device_flags(fp4)
+
+
+def test_split_tail_is_deterministic_and_matches_whole_tiles(fp4):
+    """The split tail (1.3B MLP up shapes: 176 weight-gradient tiles on 76 SM
+    pairs leave 24 tiles for a last wave, computed as two halves) gives the same
+    bits on every run, whichever half finishes first, and agrees with whole
+    tiles to fp32 rounding of the two partial sums."""
+    M, K, N = 8192, 2048, 5504
+    assert fp4.fp4_linear_wgrad_dge_workspace(M, N, K) > 0
+    A = torch.randn(M, K, device="cuda").bfloat16()
+    dY = (torch.randn(M, N, device="cuda") * 1e-3).bfloat16()
+    W = (torch.randn(K, N, device="cuda") * 0.02).bfloat16()
+    s_w = (6.0 / W.float().abs().amax(0)).contiguous()
+    runs = [fp4.fp4_linear_wgrad_dge(A, dY, W, s_w) for _ in range(3)]
+    whole = fp4.fp4_linear_wgrad_dge(A, dY, W, s_w, workspace=None)
+    for r in runs[1:]:
+        assert torch.equal(r.view(torch.int32), runs[0].view(torch.int32))
+    assert rel_frobenius(runs[0].cpu().numpy(), whole.cpu().numpy()) < 1e-6
+    dX = [fp4.fp4_linear_dgrad(dY, W, out_dtype=torch.float32) for _ in range(3)]
+    dX_whole = fp4.fp4_linear_dgrad(dY, W, out_dtype=torch.float32, workspace=None)
+    for r in dX[1:]:
+        assert torch.equal(r.view(torch.int32), dX[0].view(torch.int32))
+    assert rel_frobenius(dX[0].cpu().numpy(), dX_whole.cpu().numpy()) < 1e-6
     assert_no_device_flags(fp4)
 
 
