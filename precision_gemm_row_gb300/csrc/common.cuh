@@ -369,14 +369,15 @@ __device__ __forceinline__ float scale_from_absmax(float absmax) {
 }
 
 // Two E2M1 codes in one byte (lo in bits 3..0, hi in bits 7..4) by the hardware
-// conversion (round to nearest even, saturating to +-6).  The sign bits are
-// then set from the inputs, so a value that rounds to zero keeps its sign.
+// conversion (round to nearest even, saturating to +-6).  On sm_103a it keeps
+// the sign of -0 and of negative values that round to zero (code 0x8), as the
+// quantizer's definition requires; the exhaustive BF16-pattern tests check it.
 __device__ __forceinline__ uint32_t e2m1x2_encode(float lo, float hi) {
   uint16_t r;
   asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
       : "=h"(r)
       : "f"(hi), "f"(lo));
-  return (uint32_t(r) & 0x77u) | ((__float_as_uint(lo) >> 28) & 0x8u) | ((__float_as_uint(hi) >> 24) & 0x80u);
+  return uint32_t(r);
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
@@ -392,6 +393,10 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uin
 __device__ __forceinline__ uint32_t bf2_gt_mask(uint32_t a, uint32_t b) {   // 0xFFFF per half where a > b
   return __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
 }
+__device__ __forceinline__ uint32_t bf2_min(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 m = __hmin2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&m);
+}
 __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
   const __nv_bfloat162 m = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
   return *reinterpret_cast<const uint32_t*>(&m);
@@ -400,8 +405,7 @@ __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
 // sign(x) min(|x|, t) for both halves, with tb2 = t's 15-bit pattern in both
 // halves: exact, since t is itself a BF16 value.
 __device__ __forceinline__ uint32_t clamp_pair(uint32_t w, uint32_t tb2) {
-  const uint32_t gt = bf2_gt_mask(w & 0x7FFF7FFFu, tb2);
-  return (w & ~gt) | (((w & 0x80008000u) | tb2) & gt);
+  return (w & 0x80008000u) | bf2_min(w & 0x7FFF7FFFu, tb2);
 }
 
 // Two E2M1 codes (one byte) of the fp32 products x * s of a BF16 pair.
@@ -435,13 +439,13 @@ __device__ __forceinline__ uint32_t quantize8_clamp_f32(const uint4 v, float s, 
   return out;
 }
 
-// Running maximum of the 15-bit magnitude patterns of a chunk, per 16-bit half.
-__device__ __forceinline__ uint32_t maxmag8(const uint4 v, uint32_t acc) {
-  acc = bf2_max(acc, v.x & 0x7FFF7FFFu);
-  acc = bf2_max(acc, v.y & 0x7FFF7FFFu);
-  acc = bf2_max(acc, v.z & 0x7FFF7FFFu);
-  return bf2_max(acc, v.w & 0x7FFF7FFFu);
+// Largest 15-bit magnitude pattern of a chunk, per 16-bit half.
+__device__ __forceinline__ uint32_t chunk_maxmag(const uint4 v) {
+  return bf2_max(bf2_max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu), bf2_max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
 }
+
+// Running maximum of the magnitude patterns of a chunk, per 16-bit half.
+__device__ __forceinline__ uint32_t maxmag8(const uint4 v, uint32_t acc) { return bf2_max(acc, chunk_maxmag(v)); }
 
 // Largest magnitude pattern of a warp's packed maxima, as an fp32 value.
 __device__ __forceinline__ uint32_t warp_max_bits(uint32_t acc2) {

@@ -9,7 +9,7 @@
 //     pattern per CTA in shared memory, merged into a global histogram; the
 //     last CTA to finish (atomic ticket) scans it for the exact k-th order
 //     statistic t.
-//  2. rows_outlier: one row per warp (or a few warps for long rows), held in
+//  2. rows_outlier: one row per warp (or several warps for long rows), held in
 //     registers: counts |A| > t per 16-byte chunk and writes the row's count
 //     and its first kRowSlots entries (column, A - sign(A) t), in column order,
 //     into fixed per-row slots (no atomics); optionally writes A_clamped, and
@@ -28,7 +28,7 @@ namespace {
 constexpr int kBins = 32768;
 constexpr int kHistThreads = 1024;
 
-constexpr int kRowSlots = 8;   // entries per row kept by the row pass (more are re-read from A)
+constexpr int kRowSlots = 16;  // entries per row kept by the row pass (more are re-read from A)
 
 struct Ctrl {
   uint32_t done;          // CTAs finished with the histogram
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kHistThreads, 1)
   }
 }
 
-constexpr int kRowWarps = 8;
+constexpr int kMaxRowWarps = 16;   // warps per CTA of the row pass
 
 // 8-bit mask of the elements of a 16-byte BF16 chunk whose magnitude pattern exceeds tb.
 __device__ __forceinline__ uint32_t outlier_mask8(const uint4 v, uint32_t tb) {
@@ -180,16 +180,16 @@ __device__ __forceinline__ uint32_t outlier_mask8(const uint4 v, uint32_t tb) {
 // Each row is handled by `wpr` warps; lane l of warp w holds the row's 16-byte
 // chunks ci = l + 32 (w + wpr c), c < CH, in registers.  Column order of the
 // entries is chunk-slot c first, then warp, then lane, which is what the
-// offsets below follow.
+// offsets below follow.  A CTA holds blockDim.x / 32 / wpr rows.
 template <int CH, bool CODES>
-__global__ void __launch_bounds__(256, 2) rows_outlier_kernel(
+__global__ void __launch_bounds__(512, 1) rows_outlier_kernel(
     const uint16_t* __restrict__ A, int64_t M, int K, int64_t lda, Ctrl* ctrl, const float* __restrict__ t_ptr,
     int32_t* __restrict__ row_cnt, int32_t* __restrict__ scol, float* __restrict__ sval, uint16_t* __restrict__ A_c,
     int64_t ldac, uint8_t* __restrict__ codes, int64_t ldc, float* __restrict__ scales, int wpr) {
-  __shared__ uint32_t red[kRowWarps];
-  __shared__ uint32_t tcnt[kRowWarps][CH];
+  __shared__ uint32_t red[kMaxRowWarps];
+  __shared__ uint32_t tcnt[kMaxRowWarps][CH];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows_per_cta = kRowWarps / wpr;
+  const int rows_per_cta = int(blockDim.x >> 5) / wpr;
   const int r_in_cta = warp / wpr, w_in_row = warp % wpr;
   const int wrow0 = r_in_cta * wpr;  // first warp of this row
   const int nchunk = K >> 3;
@@ -226,9 +226,10 @@ __global__ void __launch_bounds__(256, 2) rows_outlier_kernel(
     uint32_t mx = 0;
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
-      if (CODES) mx = maxmag8(v[c], mx);
-      const uint32_t g = bf2_gt_mask(v[c].x & 0x7FFF7FFFu, tb2) | bf2_gt_mask(v[c].y & 0x7FFF7FFFu, tb2) |
-                         bf2_gt_mask(v[c].z & 0x7FFF7FFFu, tb2) | bf2_gt_mask(v[c].w & 0x7FFF7FFFu, tb2);
+      // one packed maximum per chunk serves the row's absmax and the outlier test
+      const uint32_t m2 = chunk_maxmag(v[c]);
+      if (CODES) mx = bf2_max(mx, m2);
+      const uint32_t g = bf2_gt_mask(m2, tb2);
       msk[c] = 0;
       excl[c] = 0;
       uint32_t tot = 0;
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(256, 2) rows_outlier_kernel(
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
           const int ci = lane + 32 * (w_in_row + wpr * c);
-          if (ci < nchunk) dst[ci] = msk[c] ? quantize8<true>(v[c], sc, tb2) : quantize8<false>(v[c], sc, tb2);
+          if (ci < nchunk) dst[ci] = quantize8<true>(v[c], sc, tb2);   // the clamp is a no-op without outliers
         }
       }
     }
@@ -404,28 +405,38 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
     }
     const uint4* src = reinterpret_cast<const uint4*>(A + row * lda);
     int64_t base = dst;
-    for (int c0 = 0; c0 < nchunk; c0 += 32) {
-      const int ci = c0 + lane;
-      const uint4 v = ci < nchunk ? __ldg(src + ci) : make_uint4(0u, 0u, 0u, 0u);
-      uint32_t m = ci < nchunk ? outlier_mask8(v, tb) : 0u;
-      const uint32_t cnt = __popc(m);
-      uint32_t incl = cnt;
+    constexpr int kDepth = 4;   // 32-chunk groups loaded before any is scanned
+    for (int c00 = 0; c00 < nchunk; c00 += 32 * kDepth) {
+      uint4 vv[kDepth];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
+      for (int u = 0; u < kDepth; ++u) {
+        const int ci = c00 + 32 * u + lane;
+        vv[u] = ci < nchunk ? __ldg(src + ci) : make_uint4(0u, 0u, 0u, 0u);
       }
-      int64_t pos = base + (incl - cnt);
-      while (m) {
-        const int e = __ffs(m) - 1;
-        m &= m - 1;
-        const uint32_t word = e < 4 ? (e < 2 ? v.x : v.y) : (e < 6 ? v.z : v.w);
-        const float x = bf16_bits_to_float((word >> (16 * (e & 1))) & 0xFFFFu);
-        col_idx[pos] = ci * 8 + e;
-        vals[pos] = __fsub_rn(x, copysignf(t, x));
-        ++pos;
+#pragma unroll
+      for (int u = 0; u < kDepth; ++u) {
+        const int ci = c00 + 32 * u + lane;
+        const uint4 v = vv[u];
+        uint32_t m = ci < nchunk ? outlier_mask8(v, tb) : 0u;
+        const uint32_t cnt = __popc(m);
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int64_t pos = base + (incl - cnt);
+        while (m) {
+          const int e = __ffs(m) - 1;
+          m &= m - 1;
+          const uint32_t word = e < 4 ? (e < 2 ? v.x : v.y) : (e < 6 ? v.z : v.w);
+          const float x = bf16_bits_to_float((word >> (16 * (e & 1))) & 0xFFFFu);
+          col_idx[pos] = ci * 8 + e;
+          vals[pos] = __fsub_rn(x, copysignf(t, x));
+          ++pos;
+        }
+        base += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
-      base += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
   }
 }
@@ -450,13 +461,13 @@ namespace fp4 {
 namespace {
 
 template <bool CODES>
-void launch_rows_outlier(int ch, int wpr, unsigned blocks, cudaStream_t s, const uint16_t* A, int64_t M, int K,
-                         int64_t lda, Ctrl* ctrl, const float* t, int32_t* row_cnt,
+void launch_rows_outlier(int ch, int wpr, unsigned blocks, unsigned threads, cudaStream_t s, const uint16_t* A,
+                         int64_t M, int K, int64_t lda, Ctrl* ctrl, const float* t, int32_t* row_cnt,
                          int32_t* scol, float* sval, uint16_t* A_c, int64_t ldac, uint8_t* codes, int64_t ldc,
                          float* scales) {
-#define FP4_ROWS_OUTLIER(CHV)                                                                                 \
-  rows_outlier_kernel<CHV, CODES><<<blocks, 256, 0, s>>>(A, M, K, lda, ctrl, t, row_cnt, scol, sval, A_c, ldac, \
-                                                         codes, ldc, scales, wpr)
+#define FP4_ROWS_OUTLIER(CHV)                                                                                     \
+  rows_outlier_kernel<CHV, CODES><<<blocks, threads, 0, s>>>(A, M, K, lda, ctrl, t, row_cnt, scol, sval, A_c, ldac, \
+                                                             codes, ldc, scales, wpr)
   switch (ch) {
     case 1: FP4_ROWS_OUTLIER(1); break;
     case 2: FP4_ROWS_OUTLIER(2); break;
@@ -507,22 +518,32 @@ fp4_status run_outlier_pipeline(const void* A, int64_t M, int64_t K, int64_t lda
                                                                              t_out);
   if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
 
-  // fused row pass: up to 4 chunks per lane (8 for rows longer than 8 warps x 4
-  // chunks), 1..8 warps per row (K <= 32768); persistent, 2 CTAs per SM
+  // fused row pass: ch chunks per lane and wpr warps per row, chosen to cover the
+  // row's 16-byte chunks with the least padding (ties: 4 chunks per lane;
+  // K <= 16384 fits 16 warps x 4 chunks); CTAs of about 8 warps, as many per
+  // SM as fit in 16 warps; persistent over row groups
   const int nchunk = int(K / 8);
-  int wpr = 1;
-  while (wpr < 8 && nchunk > 32 * 4 * wpr) wpr *= 2;
-  const int per_lane = (nchunk + 32 * wpr - 1) / (32 * wpr);
-  const int ch = per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : 8;
-  const int rows_per_cta = kRowWarps / wpr;
+  int ch = 1, wpr = (nchunk + 31) / 32, waste = wpr * 32 - nchunk;
+  for (int c : {2, 8, 4}) {
+    const int w = (nchunk + 32 * c - 1) / (32 * c);
+    const int x = w * 32 * c - nchunk;
+    if (w <= kMaxRowWarps && (wpr > kMaxRowWarps || x < waste || (x == waste && c == 4))) {
+      ch = c;
+      wpr = w;
+      waste = x;
+    }
+  }
+  const int rows_per_cta = wpr >= 8 ? 1 : 8 / wpr;
+  const int ctas_per_sm = kMaxRowWarps / (wpr * rows_per_cta) > 0 ? kMaxRowWarps / (wpr * rows_per_cta) : 1;
+  const unsigned threads = unsigned(32 * wpr * rows_per_cta);
   int64_t rblocks = (M + rows_per_cta - 1) / rows_per_cta;
-  if (rblocks > int64_t(sms) * 2) rblocks = int64_t(sms) * 2;
+  if (rblocks > int64_t(sms) * ctas_per_sm) rblocks = int64_t(sms) * ctas_per_sm;
   if (codes)
-    launch_rows_outlier<true>(ch, wpr, unsigned(rblocks), s, a, M, int(K), lda, ctrl, t_out, row_cnt, scol, sval,
-                              static_cast<uint16_t*>(A_clamped), ldac, codes, ldc, scales);
+    launch_rows_outlier<true>(ch, wpr, unsigned(rblocks), threads, s, a, M, int(K), lda, ctrl, t_out, row_cnt, scol,
+                              sval, static_cast<uint16_t*>(A_clamped), ldac, codes, ldc, scales);
   else
-    launch_rows_outlier<false>(ch, wpr, unsigned(rblocks), s, a, M, int(K), lda, ctrl, t_out, row_cnt, scol, sval,
-                               static_cast<uint16_t*>(A_clamped), ldac, nullptr, 0, nullptr);
+    launch_rows_outlier<false>(ch, wpr, unsigned(rblocks), threads, s, a, M, int(K), lda, ctrl, t_out, row_cnt, scol,
+                               sval, static_cast<uint16_t*>(A_clamped), ldac, nullptr, 0, nullptr);
   if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
   row_scan_kernel<<<1, 1024, 0, s>>>(row_cnt, M, row_ptr, nnz_out, ctrl, nnz_capacity, status);
   if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
