@@ -96,7 +96,7 @@ constexpr int kHotChunk = 32;   // TF32 values per 128-byte row: one pipeline st
 struct HotInfo {
   int hc;     // distinct nonzero columns of dA
   int hp;     // hc rounded up to a multiple of kHotChunk
-  int mode;   // 1: compensation on the tensor cores
+  int mode;   // 1: compensation on the tensor cores; 2: the same, packed (3 hc <= kHotChunk)
   int pad;
 };
 
@@ -144,6 +144,7 @@ __device__ void hot_scan(const uint32_t* bitmap, uint32_t* word_prefix, int32_t*
   const uint32_t excl = base + incl - c;
   if (t < nwords) word_prefix[t] = excl;
   const bool on = total > 0 && total <= uint32_t(kHotMax);
+  const bool packed = on && 3 * total <= uint32_t(kHotChunk);
   if (on) {
     uint32_t m = bits, h = excl;
     while (m) {
@@ -156,7 +157,7 @@ __device__ void hot_scan(const uint32_t* bitmap, uint32_t* word_prefix, int32_t*
     HotInfo hi;
     hi.hc = int(total);
     hi.hp = int((total + kHotChunk - 1) / kHotChunk) * kHotChunk;
-    hi.mode = on ? 1 : 0;
+    hi.mode = packed ? 2 : (on ? 1 : 0);
     hi.pad = 0;
     *info = hi;
   }
@@ -204,6 +205,9 @@ __global__ void __launch_bounds__(512) hot_mark_kernel(const int32_t* __restrict
 //     columns are distinct);
 //   the rest: one thread per output column j and 4 columns h of H:
 //     Q^T[j, h] = fl32(W[H[h], j] * s_W[j]), split; zero for h in [hc, hp).
+// Packed mode (3 hc <= 32): the three products sit side by side in the first 32
+// columns of the hi arrays, P_hi[i] = [P_hi | P_lo | P_hi | 0], Q_hi[j] =
+// [Q_hi | Q_hi | Q_lo | 0], so that one TF32 stage computes all of them.
 __global__ void __launch_bounds__(256) hot_build_kernel(
     const int32_t* __restrict__ rp, const int32_t* __restrict__ ci, const float* __restrict__ cv,
     const float* __restrict__ s_a, const uint16_t* __restrict__ W, int64_t ldw, const float* __restrict__ s_w,
@@ -232,8 +236,15 @@ __global__ void __launch_bounds__(256) hot_build_kernel(
       const int h = int(__ldg(word_prefix + (k >> 5)) + __popc(wd & ((1u << (k & 31)) - 1u)));
       float a, b;
       split_tf32(__fmul_rn(__ldg(cv + e), sa), a, b);
-      p_hi[int64_t(row) * kHotMax + h] = a;
-      p_lo[int64_t(row) * kHotMax + h] = b;
+      if (hi.mode == 2) {
+        float* pr = p_hi + int64_t(row) * kHotMax;
+        pr[h] = a;
+        pr[hi.hc + h] = b;
+        pr[2 * hi.hc + h] = a;
+      } else {
+        p_hi[int64_t(row) * kHotMax + h] = a;
+        p_lo[int64_t(row) * kHotMax + h] = b;
+      }
     }
     return;
   }
@@ -244,6 +255,24 @@ __global__ void __launch_bounds__(256) hot_build_kernel(
   const int j = (qb % nj) * 256 + threadIdx.x;
   if (j >= N) return;
   const float sw = __ldg(s_w + j);
+  if (hi.mode == 2) {
+    // packed: row j of Q_hi is [Q_hi | Q_hi | Q_lo | 0] over its first 32 columns
+    float* qr = q_hi + int64_t(j) * kHotMax;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int h = h0 + t;
+      if (h < hi.hc) {
+        float a, b;
+        split_tf32(__fmul_rn(bf16_bits_to_float(__ldg(W + int64_t(__ldg(hlist + h)) * ldw + j)), sw), a, b);
+        qr[h] = a;
+        qr[hi.hc + h] = a;
+        qr[2 * hi.hc + h] = b;
+      }
+    }
+    if (h0 == 0)
+      for (int x = 3 * hi.hc; x < kHotChunk; ++x) qr[x] = 0.0f;
+    return;
+  }
   float a[4], b[4];
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
@@ -344,9 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tiles = num_m * num_n;
   const int pair_id = int(blockIdx.x) / C::kCtas, npairs = int(gridDim.x) / C::kCtas;
   const int kblocks = (p.K / 2 + kBKBytes - 1) / kBKBytes;
-  // tensor-core compensation: 3 stages (hi*hi, hi*lo, lo*hi) per 32 columns of H
+  // tensor-core compensation: 3 stages (hi*hi, hi*lo, lo*hi) per 32 columns of
+  // H, or one stage holding all three products when they fit side by side
+  // (packed mode: the first stage's loads, chunk 0 of P_hi and Q_hi, are those)
   const bool hot = p.hot != nullptr && p.hot->mode != 0;
-  const int hot_stages = hot ? 3 * (p.hot->hp / kHotChunk) : 0;
+  const int hot_stages = hot ? (p.hot->mode == 2 ? 1 : 3 * (p.hot->hp / kHotChunk)) : 0;
   const int nstages = kblocks + hot_stages;
 
   if (warp == 0) {
