@@ -14,7 +14,8 @@ Metric: fwd + bwd TFLOP/s = sum over linears of 6 M K N / step time, with
 inputs resident in HBM and L2 flushed (256 MiB write) before every step.
 `e2e` is the same metric through the C ABI from pinned HOST buffers: the
 host->device copy of A, W, dY and the device->host copy of Y, dW and dX are inside
-the timed region.  `--impl reference` times the CPU oracle instead (bounded
+the timed region, on their own streams so that they overlap the kernels (the
+phases wait, by events, for their inputs to land).  `--impl reference` times the CPU oracle instead (bounded
 sample, single thread).  Under torchrun each rank runs an independent replica
 on its own GPU (the layer has no data-path exchange on one GPU's batch);
 value = work of all ranks / max-over-ranks time.
@@ -344,24 +345,61 @@ def run_gpu(args):
     bi = sum(h.numel() * 2 for h in uniq_hA.values()) + sum(h[1].numel() * 2 + h[2].numel() * 2 for h in host)
     bo = sum(y.numel() * 2 + d.numel() * 4 + x.numel() * 2 for y, d, x in zip(hY, hdW, hdX))
     e2e_ms = []
+    # Copies overlap the kernels as a user of the layer would run them: host to
+    # device on one stream (activations and weights first, output gradients
+    # last), the phases on the current stream as their inputs land (dgrad
+    # before wgrad), device to host on a third stream as each output is done.
+    s_c, s_in, s_out = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    acts = list(plan.acts.values())
+    nacts = len(acts)
+    idx = {name: i for i, name in enumerate(LinStep.PHASES)}
     for k in range(args.warmup + args.steps):
         flush.fill_(float(k))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        copied = set()
+        e0.record(s_c)
+        s_in.wait_event(e0)
+        s_out.wait_event(e0)
+        ev_a, ev_w, ev_g = {}, [], []
+        with torch.cuda.stream(s_in):
+            for i, l in enumerate(plan.lins):
+                if id(l.act) not in ev_a:
+                    l.act.A.copy_(host[i][0], non_blocking=True)
+                    ev_a[id(l.act)] = torch.cuda.Event()
+                    ev_a[id(l.act)].record(s_in)
+                l.W.copy_(host[i][1], non_blocking=True)
+                ev_w.append(torch.cuda.Event())
+                ev_w[-1].record(s_in)
+            for i, l in enumerate(plan.lins):
+                l.dY.copy_(host[i][2], non_blocking=True)
+                ev_g.append(torch.cuda.Event())
+                ev_g[-1].record(s_in)
+        for j, a in enumerate(acts):
+            s_c.wait_event(ev_a[id(a)])
+            plan.graphs[j].replay()
         for i, l in enumerate(plan.lins):
-            if id(host[i][0]) not in copied:
-                l.act.A.copy_(host[i][0], non_blocking=True)
-                copied.add(id(host[i][0]))
-            l.W.copy_(host[i][1], non_blocking=True)
-            l.dY.copy_(host[i][2], non_blocking=True)
-        for g in plan.graphs:
-            g.replay()
-        for i, l in enumerate(plan.lins):
-            hY[i].copy_(l.Y, non_blocking=True)
-            hdW[i].copy_(l.dW, non_blocking=True)
-            hdX[i].copy_(l.dX, non_blocking=True)
-        e1.record()
+            base = nacts + len(LinStep.PHASES) * i
+            s_c.wait_event(ev_w[i])
+            plan.graphs[base + idx["fp4_quantize_cols"]].replay()
+            plan.graphs[base + idx["fp4_linear_fwd"]].replay()
+            ev_y = torch.cuda.Event()
+            ev_y.record(s_c)
+            s_c.wait_event(ev_g[i])
+            plan.graphs[base + idx["fp4_linear_dgrad"]].replay()
+            ev_x = torch.cuda.Event()
+            ev_x.record(s_c)
+            plan.graphs[base + idx["fp4_linear_wgrad_dge"]].replay()
+            ev_w2 = torch.cuda.Event()
+            ev_w2.record(s_c)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_y)
+                hY[i].copy_(l.Y, non_blocking=True)
+                s_out.wait_event(ev_x)
+                hdX[i].copy_(l.dX, non_blocking=True)
+                s_out.wait_event(ev_w2)
+                hdW[i].copy_(l.dW, non_blocking=True)
+        s_c.wait_stream(s_out)
+        s_c.wait_stream(s_in)
+        e1.record(s_c)
         e1.synchronize()
         if k >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
