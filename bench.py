@@ -262,6 +262,24 @@ def dram_traffic(phase: str, workload: str):
     return e.get("bytes_per_launch")
 
 
+# ------------------------------------------------------------------ replicas
+
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over the ranks of the default process
+    group (the slowest replica sets the time); the values unchanged on one rank."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(world: int, flops_per_replica: float, ms_max: float) -> float:
+    """Whole-job TFLOP/s: every replica does the same work, the slowest sets the time."""
+    return world * flops_per_replica / (ms_max * 1e-3) / 1e12
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -406,10 +424,7 @@ def run_gpu(args):
     e2e_ms_mean = sum(e2e_ms) / len(e2e_ms)
 
     # ---- max over ranks
-    t = torch.tensor([ms_per_step, e2e_ms_mean], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max, e2e_max = float(t[0]), float(t[1])
+    ms_max, e2e_max = max_over_ranks([ms_per_step, e2e_ms_mean], "cuda")
 
     peaks, peak_src = load_peaks()
     fp4_peak = peaks["bf16_tflops"] * FP4_PER_BF16
@@ -439,8 +454,8 @@ def run_gpu(args):
     qnames = (ActStep.PHASE, "fp4_quantize_cols")
     quant_bytes = sum(amounts[n][0] for n in qnames)
     quant_ms = sum(kernels[n]["ms"] for n in qnames)
-    value = world * flops / (ms_max * 1e-3) / 1e12
-    e2e_value = world * flops / (e2e_max * 1e-3) / 1e12
+    value = job_throughput(world, flops, ms_max)
+    e2e_value = job_throughput(world, flops, e2e_max)
     line = {
         "metric": "FP4 linear fwd+bwd TFLOPS on 1 GB300, % of dense FP4 peak; quantize GB/s vs HBM",
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
