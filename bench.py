@@ -227,6 +227,44 @@ class StepPlan:
         if events is not None:
             events[len(self.graphs)].record()
 
+    def step(self, side):
+        """One step as a user of the layer runs it: the column quantization of
+        every W on the `side` stream while the row pipelines of the activations
+        run on the current one; then the forwards; then every dgrad on `side`
+        while the weight gradients run on the current stream."""
+        import torch
+        main = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(main)
+        side.wait_event(fork)
+        with torch.cuda.stream(side):
+            for l in self.lins:
+                l.fns()[0]()
+        for a in self.acts.values():
+            a.fn()()
+        main.wait_stream(side)
+        for l in self.lins:
+            l.fns()[1]()
+        fork2 = torch.cuda.Event()
+        fork2.record(main)
+        side.wait_event(fork2)
+        with torch.cuda.stream(side):
+            for l in self.lins:
+                l.fns()[3]()
+        for l in self.lins:
+            l.fns()[2]()
+        main.wait_stream(side)
+
+    def capture_step(self):
+        import torch
+        self.side = torch.cuda.Stream()
+        for _ in range(2):
+            self.step(self.side)
+        torch.cuda.synchronize()
+        self.step_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.step_graph):
+            self.step(self.side)
+
     def launches(self):
         return ActStep.LAUNCHES * len(self.acts) + sum(LinStep.LAUNCHES.values()) * len(self.lins)
 
@@ -325,21 +363,35 @@ def run_gpu(args):
         plan.run()
     torch.cuda.synchronize()
     plan.capture()
+    plan.capture_step()
     torch.cuda.synchronize()
     for _ in range(args.warmup):
         plan.replay()
+        plan.step_graph.replay()
     st, fl = fp4.fp4_device_status()
     if st != "FP4_OK":
         raise RuntimeError(f"device status after warm-up: {st} flags={fl}")
 
     # ---- device-resident timed region: L2 flush, then a short GPU-side head start
-    # so every replay of the step is queued before the first event fires
-    ncalls = len(plan.calls)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ncalls + 1)] for _ in range(args.steps)]
+    # so the step is queued before the first event fires.  The step is one CUDA
+    # graph (independent phases on two streams, see StepPlan.step).
+    ev_step = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        for k in range(args.steps):
+            flush.fill_(float(k))
+            torch.cuda._sleep(HEAD_START_CYCLES)
+            ev_step[k][0].record()
+            plan.step_graph.replay()
+            ev_step[k][1].record()
+        torch.cuda.synchronize()
+        # ---- per-phase pass (the roofline's kernel times): the same phases one
+        # after another, one graph per phase, events between them on the stream
+        # that launches them
+        ncalls = len(plan.calls)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ncalls + 1)] for _ in range(args.steps)]
         for k in range(args.steps):
             flush.fill_(float(k))
             torch.cuda._sleep(HEAD_START_CYCLES)
@@ -348,8 +400,9 @@ def run_gpu(args):
     st, fl = fp4.fp4_device_status()
     if st != "FP4_OK":
         raise RuntimeError(f"device status after timed steps: {st} flags={fl}")
-    step_ms = [ev[k][0].elapsed_time(ev[k][ncalls]) for k in range(args.steps)]
+    step_ms = [ev_step[k][0].elapsed_time(ev_step[k][1]) for k in range(args.steps)]
     ms_per_step = sum(step_ms) / len(step_ms)
+    seq_ms = sum(ev[k][0].elapsed_time(ev[k][ncalls]) for k in range(args.steps)) / args.steps
     phase_ms = {}
     for i, (name, _) in enumerate(plan.calls):
         phase_ms[name] = phase_ms.get(name, 0.0) + sum(ev[k][i].elapsed_time(ev[k][i + 1])
@@ -464,12 +517,14 @@ def run_gpu(args):
         "config": {"workload": args.workload, "linears": [[l.name, l.M, l.K, l.N, l.q] for l in work.linears],
                    "bwd": "weight gradient with DGE + input gradient dY W^T (BF16; the pages give no dgrad)",
                    "l2": "flushed before every step",
-                   "launch": "one CUDA graph per phase, replayed after a 0.2 ms GPU head start",
+                   "launch": "one CUDA graph per step (column quantization alongside the row pipeline, dgrad "
+                             "alongside wgrad, on two streams), replayed after a 0.2 ms GPU head start; kernel "
+                             "times from a second pass of one graph per phase",
                    "parallelism": f"replicas x{world}"},
         "fp4_peak_frac": round(value / world / fp4_peak, 4),
         "quantize": {"gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1), "frac_of_hbm": round(
             quant_bytes / (quant_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
-        "kernels": kernels, "nnz": nnz,
+        "kernels": kernels, "phases_one_after_another_ms": round(seq_ms, 5), "nnz": nnz,
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                 "ms_per_step": round(e2e_max, 5)},
