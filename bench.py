@@ -339,6 +339,8 @@ def run_gpu(args):
     from precision_gemm_row_gb300 import fp4lin as fp4
 
     work = wl.WORKLOADS[args.workload]
+    if args.fuse_shared_input:
+        work = wl.fuse_shared_inputs(work)
     host = []
     dev_inputs = []
     pinned_cache = {}
@@ -515,6 +517,7 @@ def run_gpu(args):
         "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp4_e2m1 fwd / bf16 wgrad + dgrad, fp32 accumulate", "data": "synthetic (seeded, LLaMA-shaped)",
         "config": {"workload": args.workload, "linears": [[l.name, l.M, l.K, l.N, l.q] for l in work.linears],
+                   "fused_shared_input": bool(args.fuse_shared_input),
                    "bwd": "weight gradient with DGE + input gradient dY W^T (BF16; the pages give no dgrad)",
                    "l2": "flushed before every step",
                    "launch": "one CUDA graph per step (column quantization alongside the row pipeline, dgrad "
@@ -639,6 +642,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=int, default=64, help="rows sampled by the oracle baseline")
+    ap.add_argument("--fuse-shared-input", action="store_true",
+                    help="linears reading the same activation run as one GEMM over their concatenated weights")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -28,7 +28,7 @@ import torch
 
 __all__ = [
     "LinearCase", "Workload", "WORKLOADS", "f32_to_bf16_bits", "bf16_bits_to_f32_view",
-    "draw_activation", "draw_weight", "draw_grad", "outlier_channels",
+    "draw_activation", "draw_weight", "draw_grad", "outlier_channels", "fuse_shared_inputs", "FusedWorkload",
 ]
 
 
@@ -166,3 +166,45 @@ WORKLOADS: Dict[str, Workload] = {
 }
 
 WORKLOAD_ORDER: List[str] = list(WORKLOADS)
+
+
+class FusedWorkload:
+    """A workload whose linears that read the same activation (and clamp
+    quantile) are one linear over their weights placed side by side: W_cat =
+    [W_1 | W_2 | ...] (K x sum N), dY_cat = [dY_1 | dY_2 | ...].  Only the layout
+    of the inputs changes: Y_cat = A W_cat holds each member's Y as a column
+    block, dW_cat each member's dW, and dY_cat W_cat^T = sum_i dY_i W_i^T is
+    the summed input gradient of the shared activation."""
+
+    def __init__(self, work: Workload):
+        self.base = work
+        self.key = work.key
+        self.seed = work.seed
+        groups: Dict[Tuple[str, float], List[LinearCase]] = {}
+        for lin in work.linears:
+            groups.setdefault((lin.act, lin.q), []).append(lin)
+        self.members: Dict[str, Tuple[LinearCase, ...]] = {}
+        fused = []
+        for lins in groups.values():
+            if len(lins) == 1:
+                f = lins[0]
+            else:
+                name = "+".join(l.name for l in lins)
+                f = dataclasses.replace(lins[0], name=name, N=sum(l.N for l in lins), weight_name=name)
+            self.members[f.name] = tuple(lins)
+            fused.append(f)
+        self.linears: Tuple[LinearCase, ...] = tuple(fused)
+        self.description = work.description + " (linears sharing an input fused along N)"
+
+    def activation(self, lin: LinearCase) -> np.ndarray:
+        return self.base.activation(self.members[lin.name][0])
+
+    def weight(self, lin: LinearCase) -> np.ndarray:
+        return np.concatenate([self.base.weight(l) for l in self.members[lin.name]], axis=1)
+
+    def grad(self, lin: LinearCase) -> np.ndarray:
+        return np.concatenate([self.base.grad(l) for l in self.members[lin.name]], axis=1)
+
+
+def fuse_shared_inputs(work: Workload) -> FusedWorkload:
+    return FusedWorkload(work)

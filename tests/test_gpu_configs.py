@@ -124,3 +124,52 @@ def test_full_size_linear(fp4, workload, linear):
     assert_bf16_compensated_close(host_bits(step.dX[torch.from_numpy(rows).cuda()]), dx_ref, dx_mag,
                                   bound=TC_SUM_BOUND)
     assert_no_device_flags(fp4)
+
+
+def test_fused_shared_input_linears_7b_layer(fp4):
+    """Linears reading the same activation as one GEMM over their weights side
+    by side (q/k/v: N = 12288, gate/up: N = 22016): every member's Y, column
+    codes and dW are its column block, and dX is the sum of the members' input
+    gradients; checked against the oracle member by member on sampled rows."""
+    import bench
+    base = wl.WORKLOADS["c3_llama7b_layer_8192tok"]
+    work = wl.fuse_shared_inputs(base)
+    fused = [l for l in work.linears if len(work.members[l.name]) > 1]
+    assert [l.N for l in fused] == [3 * 4096, 2 * 11008]
+    for lin in fused:
+        A_bits = work.activation(lin)
+        W_bits, dY_bits = work.weight(lin), work.grad(lin)
+        plan = bench.StepPlan(fp4, types.SimpleNamespace(linears=[lin]),
+                              [(dev_bf16(A_bits), dev_bf16(W_bits), dev_bf16(dY_bits))])
+        plan.run()
+        torch.cuda.synchronize()
+        assert_no_device_flags(fp4)
+        act, step = next(iter(plan.acts.values())), plan.lins[0]
+        rows, frows = _sample(lin.M, 5), _sample(lin.K, 6)
+        rp = act.out["row_ptr"].cpu().numpy().astype(np.int32)
+        ci, cv = act.out["col_idx"].cpu().numpy(), act.out["vals"].cpu().numpy()
+        a_codes, s_a = act.out["codes"].cpu().numpy(), act.out["scales"].cpu().numpy()
+        w_codes, s_w = step.w_codes.cpu().numpy(), step.s_w.cpu().numpy()
+        Y = host_bits(step.Y[torch.from_numpy(rows).cuda()])
+        dW = step.dW[torch.from_numpy(frows).cuda()].cpu().numpy()
+        dx_ref = np.zeros((rows.size, lin.K))
+        dx_mag = np.zeros((rows.size, lin.K))
+        c0 = 0
+        for m in work.members[lin.name]:
+            blk = slice(c0, c0 + m.N)
+            Wm, dYm = base.weight(m), base.grad(m)
+            cols = c0 + _sample(m.N, 7)
+            ref_w, ref_sw = orc.quantize_cols(orc.bf16_to_f32(Wm)[:, cols - c0])
+            assert np.array_equal(w_codes[cols], ref_w)
+            assert np.array_equal(s_w[cols].view(np.uint32), ref_sw.view(np.uint32))
+            y_ref = orc.linear_fwd(a_codes, s_a, w_codes[blk], s_w[blk], rp, ci, cv, Wm, rows=rows)
+            mag = orc.linear_fwd_magnitude(a_codes, s_a, w_codes[blk], s_w[blk], rp, ci, cv, Wm, rows=rows)
+            assert_bf16_compensated_close(Y[:, blk], y_ref, mag)
+            dw_ref = orc.wgrad_dge(A_bits, dYm, Wm, s_w[blk], 5.0, 3.0, rows=frows)
+            assert rel_frobenius(dW[:, blk], dw_ref) <= FROB_TOL
+            dx_ref += orc.linear_dgrad(dYm, Wm, rows=rows)
+            dx_mag += orc.linear_dgrad(dYm & np.uint16(0x7FFF), Wm & np.uint16(0x7FFF), rows=rows)
+            c0 += m.N
+        assert_bf16_compensated_close(host_bits(step.dX[torch.from_numpy(rows).cuda()]), dx_ref, dx_mag,
+                                      bound=TC_SUM_BOUND)
+        assert_no_device_flags(fp4)
