@@ -15,24 +15,48 @@
 // operands MN-major (the token dimension strided); its epilogue loads W and
 // s_W for each 32 x 32 block of dW, computes the factors and writes dW = G f'
 // once.
+#include <cmath>
+
 #include "bwd_gemm.cuh"
 
 namespace fp4 {
 namespace {
 
-// DGE factor f'(x) for the scaled weight magnitude x.  |u|^e uses the fast
-// power intrinsic (relative error a few fp32 ulps); u = 0 takes pw0, the limit
-// of |u|^e there: +inf for e < 0 (then clipped), 1 for e = 0, 0 for e > 0.
-// Written without branches: the interval is found by scaling x with 2/delta
-// (a power of two, so s and its fractional part are exact), and every case is
-// a select, so a warp never diverges over mixed magnitudes.
-__device__ __forceinline__ float dge_factor(float x, float inv_k, float expo, float clip, float pw0) {
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Constants of the DGE factor for one call.
+struct DgeConst {
+  float inv_k;        // 1/k
+  float expo;         // 1/k - 1
+  float log2_inv_k;   // log2(1/k)
+  float clip;
+  float f_mid;        // the factor at u = 0: min(clip, (1/k) lim |u|^expo), +inf, 1 or 0 before clipping
+};
+
+// DGE factor f'(x) for the scaled weight magnitude x.  (1/k)|u|^expo is taken
+// as 2^(expo log2 u + log2(1/k)) on the special-function unit (relative error
+// about 1e-6 at the largest exponents, far inside the 1e-5 bound of dW); u is
+// 0 or at least 2^-23 here, so flushing subnormals changes nothing, and u = 0
+// (an interval midpoint) takes the precomputed limit.  The interval is found
+// by scaling x with 2/delta (a power of two, so s and its fractional part are
+// exact), and every case is a select, so a warp never diverges over mixed
+// magnitudes.
+__device__ __forceinline__ float dge_factor(float x, const DgeConst& c) {
   const float two_over_delta = x < 2.0f ? 2.0f : (x < 4.0f ? 1.0f : 0.5f);
   const float s = x * two_over_delta;                        // interval [floor(s), floor(s) + 1)
   const float u = fabsf(fmaf(s - floorf(s), 2.0f, -1.0f));   // |2 (x - lo) / delta - 1|
-  const float pw = u > 0.0f ? __powf(u, expo) : pw0;
-  const float f = fminf(clip, inv_k * pw);
-  return x < 6.0f ? f : inv_k;
+  const float f = fminf(c.clip, ex2_approx(fmaf(c.expo, lg2_approx(u), c.log2_inv_k)));
+  const float fu = u > 0.0f ? f : c.f_mid;
+  return x < 6.0f ? fu : c.inv_k;
 }
 
 // dW[k, n] = G[k, n] * f'(|fl32(W[k, n] s_W[n])|), fp32.
@@ -43,7 +67,7 @@ struct DgeEpilogue {
   float* dW;
   int64_t lddw;
   int rows, cols;   // K, N
-  float inv_k, expo, clip, pw0;
+  DgeConst dge;
 
   // W rows row0..row0+31 (columns col0..col0+63: one 128-byte line per row)
   // and s_w[col0..col0+63] (two lines) into L2
@@ -70,10 +94,10 @@ struct DgeEpilogue {
     return pr;
   }
   __device__ __forceinline__ void store(const Pre& pr, int i, int grow, int gcol, float4 g) const {
-    const float f0 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(pr.w[i].x & 0xFFFFu), pr.sw.x)), inv_k, expo, clip, pw0);
-    const float f1 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(pr.w[i].x >> 16), pr.sw.y)), inv_k, expo, clip, pw0);
-    const float f2 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(pr.w[i].y & 0xFFFFu), pr.sw.z)), inv_k, expo, clip, pw0);
-    const float f3 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(pr.w[i].y >> 16), pr.sw.w)), inv_k, expo, clip, pw0);
+    const float f0 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(pr.w[i].x & 0xFFFFu), pr.sw.x)), dge);
+    const float f1 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(pr.w[i].x >> 16), pr.sw.y)), dge);
+    const float f2 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(pr.w[i].y & 0xFFFFu), pr.sw.z)), dge);
+    const float f3 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(pr.w[i].y >> 16), pr.sw.w)), dge);
     *reinterpret_cast<float4*>(dW + int64_t(grow) * lddw + gcol) = make_float4(g.x * f0, g.y * f1, g.z * f2, g.w * f3);
   }
 };
@@ -120,10 +144,13 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   e.lddw = lddw;
   e.rows = int(K);
   e.cols = int(N);
-  e.inv_k = 1.0f / dge_k;
-  e.expo = 1.0f / dge_k - 1.0f;
-  e.clip = dge_clip;
-  e.pw0 = e.expo < 0.0f ? INFINITY : (e.expo == 0.0f ? 1.0f : 0.0f);
+  e.dge.inv_k = 1.0f / dge_k;
+  e.dge.expo = 1.0f / dge_k - 1.0f;
+  e.dge.log2_inv_k = std::log2(1.0f / dge_k);
+  e.dge.clip = dge_clip;
+  // lim_{u -> 0} |u|^expo: +inf for expo < 0 (clipped), 1 for expo = 0, 0 for expo > 0
+  const float lim = e.dge.expo < 0.0f ? INFINITY : (e.dge.expo == 0.0f ? 1.0f : 0.0f);
+  e.dge.f_mid = std::fmin(dge_clip, e.dge.inv_k * lim);
   bwd::Shape s;
   s.R = int(K);
   s.C = int(N);
