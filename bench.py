@@ -300,6 +300,24 @@ def dram_traffic(phase: str, workload: str):
     return e.get("bytes_per_launch")
 
 
+def select_linears(wl, args):
+    """The workload, with shared-input linears fused (--fuse-shared-input) and
+    restricted to the linears named by --linear (all when none is named)."""
+    import types
+    work = wl.WORKLOADS[args.workload]
+    if args.fuse_shared_input:
+        work = wl.fuse_shared_inputs(work)
+    if args.linear:
+        names = {l.name for l in work.linears}
+        unknown = [n for n in args.linear if n not in names]
+        if unknown:
+            raise SystemExit(f"--linear {unknown}: not in {sorted(names)}")
+        keep = tuple(l for l in work.linears if l.name in args.linear)
+        work = types.SimpleNamespace(key=work.key, seed=work.seed, linears=keep, activation=work.activation,
+                                     weight=work.weight, grad=work.grad)
+    return work
+
+
 # ------------------------------------------------------------------ replicas
 
 def max_over_ranks(values, device):
@@ -338,9 +356,7 @@ def run_gpu(args):
         dist.barrier()
     from precision_gemm_row_gb300 import fp4lin as fp4
 
-    work = wl.WORKLOADS[args.workload]
-    if args.fuse_shared_input:
-        work = wl.fuse_shared_inputs(work)
+    work = select_linears(wl, args)
     host = []
     dev_inputs = []
     pinned_cache = {}
@@ -517,7 +533,7 @@ def run_gpu(args):
         "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp4_e2m1 fwd / bf16 wgrad + dgrad, fp32 accumulate", "data": "synthetic (seeded, LLaMA-shaped)",
         "config": {"workload": args.workload, "linears": [[l.name, l.M, l.K, l.N, l.q] for l in work.linears],
-                   "fused_shared_input": bool(args.fuse_shared_input),
+                   "fused_shared_input": bool(args.fuse_shared_input), "only_linears": args.linear or None,
                    "bwd": "weight gradient with DGE + input gradient dY W^T (BF16; the pages give no dgrad)",
                    "l2": "flushed before every step",
                    "launch": "one CUDA graph per step (column quantization alongside the row pipeline, dgrad "
@@ -644,6 +660,8 @@ def main():
     ap.add_argument("--cpu-budget", type=int, default=64, help="rows sampled by the oracle baseline")
     ap.add_argument("--fuse-shared-input", action="store_true",
                     help="linears reading the same activation run as one GEMM over their concatenated weights")
+    ap.add_argument("--linear", action="append", default=[],
+                    help="run only this linear of the workload (repeatable; default: all)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
