@@ -550,7 +550,7 @@ def run_gpu(args):
         "gpu_launches": args.steps * plan.launches(),
         "clocks": clocks.summary(),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:   # the CPU baseline is a single-GPU figure
         line["cpu_baseline"] = cpu_baseline(args.workload, 4 * args.cpu_budget)   # about 10 s of one core
     if world > 1:
         dist.barrier()
