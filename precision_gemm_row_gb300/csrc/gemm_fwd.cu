@@ -568,6 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           k = __ldg(p.ci + e);
           v = __ldg(p.cv + e);
         }
+        if (uint32_t(k) >= uint32_t(p.K)) {   // a column outside W: skipped and reported
+          atomicOr(p.status, FP4_FLAG_INTERNAL);
+          continue;
+        }
         const uint4* wr = reinterpret_cast<const uint4*>(p.W + int64_t(k) * p.ldw + col_base);
 #pragma unroll
         for (int g0 = 0; g0 < EC / 8; g0 += 5) {

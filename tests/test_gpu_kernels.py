@@ -406,6 +406,41 @@ def test_linear_fwd_scaled_and_compensated(fp4, M, N, K, q, workspace):
     assert_no_device_flags(fp4)
 
 
+@pytest.mark.parametrize("workspace", ["auto", None])
+@pytest.mark.parametrize("bad_col", [-1, 96])
+def test_linear_fwd_skips_and_reports_out_of_range_columns(fp4, workspace, bad_col):
+    """A dA entry whose column lies outside W (a corrupt caller CSR) is skipped by
+    both compensation paths and reported as FP4_ERR_INTERNAL; every other entry
+    still counts (Y equals the oracle's result without that entry)."""
+    M, N, K, q = 129, 264, 96, 0.9
+    A_bits = _t3_bits(M + 5, (M, K), 2.0)
+    W_bits = _normal_bits(N + 5, (K, N), 0.02)
+    t, _, _ = orc.quantile_threshold(A_bits, q)
+    A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
+    a_codes, s_a = orc.quantize_rows(A_c)
+    w_codes, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+    e = int(rp[M // 2])                       # first entry of a middle row
+    row = int(np.searchsorted(rp, e, side="right") - 1)
+    assert rp[row] <= e < rp[row + 1]
+    ci_bad = ci.copy()
+    ci_bad[e] = bad_col
+    keep = np.ones(ci.size, bool)
+    keep[e] = False
+    rp_ref = rp.copy()
+    rp_ref[row + 1:] -= 1
+    y_ref = orc.linear_fwd(a_codes, s_a, w_codes, s_w, rp_ref, ci[keep], cv[keep], W_bits)
+    mag = orc.linear_fwd_magnitude(a_codes, s_a, w_codes, s_w, rp_ref, ci[keep], cv[keep], W_bits)
+    d = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    csr = {"row_ptr": d(rp), "col_idx": d(ci_bad), "vals": d(cv)}
+    assert_no_device_flags(fp4)
+    yb = fp4.fp4_linear_fwd(d(a_codes), d(s_a), d(w_codes), d(s_w), K, csr=csr, W=dev_bf16(W_bits), out_type="bf16",
+                            workspace=workspace)
+    name, flags = fp4.fp4_device_status()
+    assert name == "FP4_ERR_INTERNAL" and flags & fp4.FLAG_INTERNAL, (name, flags)
+    assert_bf16_compensated_close(host_bits(yb), y_ref, mag)
+    assert_no_device_flags(fp4)
+
+
 def _hot_channel_bits(seed, M, K, n_hot, scale=20.0):
     """N(0,1) activations with n_hot seeded channels multiplied by `scale` (outliers gather there)."""
     rng = np.random.default_rng(seed)
