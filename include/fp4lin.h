@@ -243,8 +243,12 @@ size_t fp4_linear_fwd_workspace(int64_t M, int64_t N, int64_t K);
  *   s_w       device fp32 N
  *   M, N, K   M, N >= 1; 32 <= K <= 16384, K % 32 == 0; M, N < 2^31; N % 8 == 0
  *   dA_row_ptr, dA_col, dA_val  device CSR of dA (as from outlier_clamp_quantile),
- *             all three NULL for no compensation; the columns of a row must be
- *             distinct (the epilogue path is fastest when they ascend)
+ *             all three NULL for no compensation; row_ptr starts at 0 and does not
+ *             decrease, and entries [0, row_ptr[M]) of dA_col / dA_val are readable
+ *             (not checked: it would take a host synchronization); the columns of
+ *             a row must be distinct (the epilogue path is fastest when they
+ *             ascend); an entry whose column lies outside [0, K) is skipped and
+ *             reported as the device-side INTERNAL flag
  *   W         device BF16 K x ldw (the unquantized weight), required iff compensation
  *   Y         device, M x ldy elements of the output type; 16-byte aligned, ldy % 8 == 0
  *   y_type    fp4_out_type
@@ -254,7 +258,7 @@ size_t fp4_linear_fwd_workspace(int64_t M, int64_t N, int64_t K);
  * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE (non-NULL and too small),
  *         DEVICE_UNSUPPORTED, CUDA; device-side TIMEOUT flag if a pipeline wait
  *         runs out (about 1 s); device-side INTERNAL flag for a dA column
- *         outside [0, K) (the entry is skipped).
+ *         outside [0, K) (the entry is skipped, on both compensation paths).
  */
 fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_bytes, const float* s_a,
                           const uint8_t* w_codes_t, int64_t ldw_codes_bytes, const float* s_w,
