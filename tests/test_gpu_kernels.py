@@ -231,13 +231,15 @@ def test_fused_rows_outliers_every_finite_bf16_pattern(fp4, q):
 
 # ---------------------------------------------------------------- DGE weight gradient
 
-@pytest.mark.parametrize("M,K,N", [(64, 128, 256), (256, 512, 512), (200, 136, 264), (1000, 384, 520),
-                                   (1500, 1032, 520), (2048, 200, 264), (2304, 520, 520), (4100, 384, 136)])
+@pytest.mark.parametrize("M,K,N", [(1, 8, 8), (1, 200, 264), (64, 128, 256), (256, 512, 512), (200, 136, 264),
+                                   (1000, 384, 520), (1500, 1032, 520), (2048, 200, 264), (2304, 520, 520),
+                                   (4100, 384, 136)])
 @pytest.mark.parametrize("k,clip", [(5.0, 3.0), (1.0, 3.0)])
 @pytest.mark.parametrize("workspace", ["auto", None])
 def test_wgrad_dge(fp4, M, K, N, k, clip, workspace):
-    """M >= 2048 tokens runs the GEMM as CTA pairs (256-row dW tiles; K = 200, 520
-    and 384 leave partial pair tiles, N = 264 / 136 partial column tiles).  With a
+    """A single token (M = 1) and the smallest K, N; M >= 2048 tokens runs the GEMM
+    as CTA pairs (256-row dW tiles; K = 200, 520 and 384 leave partial pair
+    tiles, N = 264 / 136 partial column tiles).  With a
     workspace, these few-tile shapes with 2 or more 1024-token chunks (M = 1500
     and up) compute every tile as two halves of the token range."""
     A_bits = _normal_bits(M + 1, (M, K))
@@ -260,8 +262,9 @@ def _dgrad_ref(dY_bits, W_bits):
     return ref, mag
 
 
-@pytest.mark.parametrize("M,N,K", [(64, 128, 256), (200, 264, 136), (1000, 520, 392), (5, 8, 8), (129, 72, 1032),
-                                   (300, 1096, 264), (300, 2056, 264), (2304, 4104, 520), (513, 16384, 8)])
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (1, 2056, 264), (64, 128, 256), (200, 264, 136), (1000, 520, 392),
+                                   (5, 8, 8), (129, 72, 1032), (300, 1096, 264), (300, 2056, 264), (2304, 4104, 520),
+                                   (513, 16384, 8)])
 @pytest.mark.parametrize("out", ["bf16", "fp32"])
 @pytest.mark.parametrize("workspace", ["auto", None])
 def test_dgrad(fp4, M, N, K, out, workspace):
