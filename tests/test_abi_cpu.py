@@ -129,3 +129,28 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 64, 16, fake, 1, 20, None, 0, None) == 3
     assert L.fp4_quantize_cols(fake, 64, 12, 16, fake, 32, fake, fake, 1 << 10, None) == 2
     assert L.fp4_selftest_bounded_wait(0, None) == 1
+
+
+def _declared_arities():
+    """Number of parameters of every function include/fp4lin.h declares."""
+    text = open(os.path.join(ROOT, "include", "fp4lin.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(([^;{]*?)\)\s*;",
+                         text, flags=re.M | re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_header():
+    """Every ctypes prototype in the binding takes as many arguments as the C
+    declaration (a stale prototype would pass wrong values through the ABI)."""
+    fp4build.build()
+    from precision_gemm_row_gb300 import fp4lin
+    arities = _declared_arities()
+    assert len(arities) >= 12
+    for name, n in arities.items():
+        argtypes = getattr(fp4lin._lib, name).argtypes
+        assert argtypes is not None, name
+        assert len(argtypes) == n, (name, len(argtypes), n)
