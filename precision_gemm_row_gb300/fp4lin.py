@@ -363,3 +363,14 @@ def linear_forward(A: torch.Tensor, W: torch.Tensor, q: float, out_type: str = "
     Y = fp4_linear_fwd(o["codes"], o["scales"], w_codes_t, s_w, A.shape[1], csr=o, W=W, out_type=out_type,
                        stream=stream)
     return Y, dict(outlier=o, a_codes=o["codes"], s_a=o["scales"], w_codes_t=w_codes_t, s_w=s_w)
+
+
+def linear_backward(A: torch.Tensor, W: torch.Tensor, dY: torch.Tensor, s_w: torch.Tensor, dge_k: float = 5.0,
+                    dge_clip: float = 3.0, dx_dtype: torch.dtype = torch.bfloat16, stream=None):
+    """The backward of the quantized linear layer: the DGE-corrected weight
+    gradient dW (K x N, fp32) and the input gradient dX = dY W^T (M x K).
+    s_w: the column scales of W from the forward (linear_forward's "s_w").
+    Returns (dX, dW)."""
+    dW = fp4_linear_wgrad_dge(A, dY, W, s_w, dge_k, dge_clip, stream=stream)
+    dX = fp4_linear_dgrad(dY, W, out_dtype=dx_dtype, stream=stream)
+    return dX, dW

@@ -316,6 +316,28 @@ def test_split_tail_is_deterministic_and_matches_whole_tiles(fp4):
     assert_no_device_flags(fp4)
 
 
+def test_linear_forward_and_backward_conveniences(fp4):
+    """linear_forward / linear_backward chain the entry points of one layer step:
+    their results equal the individual calls' (bit for bit) and the oracle's."""
+    M, K, N, q = 200, 256, 264, 0.99
+    A_bits = _t3_bits(11, (M, K), 2.0)
+    W_bits = _normal_bits(12, (K, N), 0.02)
+    dY_bits = _normal_bits(13, (M, N), 1e-3)
+    A, W, dY = dev_bf16(A_bits), dev_bf16(W_bits), dev_bf16(dY_bits)
+    Y, inter = fp4.linear_forward(A, W, q)
+    dX, dW = fp4.linear_backward(A, W, dY, inter["s_w"])
+    assert dX.shape == (M, K) and dX.dtype == torch.bfloat16 and dW.shape == (K, N)
+    dW1 = fp4.fp4_linear_wgrad_dge(A, dY, W, inter["s_w"])
+    dX1 = fp4.fp4_linear_dgrad(dY, W)
+    assert torch.equal(dW.view(torch.int32), dW1.view(torch.int32))
+    assert torch.equal(dX.view(torch.int16), dX1.view(torch.int16))
+    _, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+    assert rel_frobenius(dW.cpu().numpy(), orc.wgrad_dge(A_bits, dY_bits, W_bits, s_w, 5.0, 3.0)) <= FROB_TOL
+    ref, mag = _dgrad_ref(dY_bits, W_bits)
+    assert_bf16_compensated_close(host_bits(dX), ref, mag, bound=TC_SUM_BOUND)
+    assert_no_device_flags(fp4)
+
+
 def test_dgrad_exact_on_integer_products(fp4):
     """Small integers: every product and partial sum is exact in fp32, so dX is
     the exact integer matrix bit for bit (checks operand order and tile
