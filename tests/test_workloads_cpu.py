@@ -74,3 +74,17 @@ def test_bench_linear_selection():
                                  linear=["q_proj"])
     with pytest.raises(SystemExit):
         bench.select_linears(wl, args)
+
+
+def test_reference_arm_line_on_the_small_workload():
+    """bench.py --impl reference times the oracle on the host; its JSON line
+    carries the contract's keys (checked on the 256 x 512 x 512 workload)."""
+    import bench
+    args = types.SimpleNamespace(workload="c1_single_linear_256x512x512", steps=1, warmup=3, cpu_budget=16)
+    line = bench.run_reference(args)
+    assert line["impl"] == "reference" and line["value"] > 0 and line["higher_is_better"] is True
+    assert line["unit"] == "TFLOP/s" and line["metric"].startswith("FP4 linear fwd+bwd TFLOPS")
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["steps"] == 1 and line["warmup"] == 3
