@@ -35,7 +35,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "c2_llama1.3b_mlp_up_8192x2048x5504"
+DEFAULT_WORKLOAD = "c4_llama13b_layer_16384tok"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP4_PER_BF16 = 13.5 / 2.25      # nominal dense FP4 : BF16 tensor rate
 L2_FLUSH_BYTES = 256 << 20
@@ -115,9 +115,9 @@ class ActStep:
     PHASE = "fp4_quantize_rows_outliers"
     LAUNCHES = 4   # histogram, fused row pass, row scan, CSR gather
 
-    def __init__(self, fp4, A, q):
+    def __init__(self, fp4, A, q, label=""):
         import torch
-        self.fp4, self.A, self.q = fp4, A, q
+        self.fp4, self.A, self.q, self.label = fp4, A, q, label
         M, K = A.shape
         cap = fp4.outlier_max_nnz(M, K, q)
         dev = A.device
@@ -199,12 +199,14 @@ class StepPlan:
         for lin, (A, W, dY) in zip(work.linears, device_inputs):
             key = (lin.act, lin.q)
             if key not in self.acts:
-                self.acts[key] = ActStep(fp4, A, lin.q)
+                self.acts[key] = ActStep(fp4, A, lin.q, lin.act)
             self.lins.append(LinStep(fp4, lin, self.acts[key], W, dY))
-        # (phase name, callable) in launch order
+        # (phase name, callable) in launch order, and what each call works on
         self.calls = [(ActStep.PHASE, a.fn()) for a in self.acts.values()]
+        self.labels = [a.label for a in self.acts.values()]
         for l in self.lins:
             self.calls += list(zip(LinStep.PHASES, l.fns()))
+            self.labels += [l.lin.name] * len(LinStep.PHASES)
 
     def run(self):
         for _, fn in self.calls:
@@ -286,15 +288,16 @@ KERNEL_SOURCES = {
 }
 
 
-def dram_traffic(phase: str, workload: str):
-    """Per-launch DRAM bytes of `phase` from the committed ncu summary, or None if
-    the kernel source changed since the capture (or none was taken)."""
+def dram_traffic(phase: str, workload: str, launch: str):
+    """Per-launch DRAM bytes of `phase` on `launch` (a linear or activation of the
+    workload) from the committed ncu summary, or None if the kernel source
+    changed since the capture (or none was taken)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    e = d.get(workload, {}).get(phase)
+    e = d.get(workload, {}).get(f"{phase}[{launch}]")
     if not e or e.get("source_hash") != _src_hash(KERNEL_SOURCES[phase]):
         return None
     return e.get("bytes_per_launch")
@@ -316,6 +319,18 @@ def select_linears(wl, args):
         work = types.SimpleNamespace(key=work.key, seed=work.seed, linears=keep, activation=work.activation,
                                      weight=work.weight, grad=work.grad)
     return work
+
+
+def arm_config(args, work, world: int):
+    """The workload as both arms report it."""
+    return {"workload": args.workload, "linears": [[l.name, l.M, l.K, l.N, l.q] for l in work.linears],
+            "fused_shared_input": bool(args.fuse_shared_input), "only_linears": args.linear or None,
+            "bwd": "weight gradient with DGE + input gradient dY W^T (BF16; the pages give no dgrad)",
+            "l2": "flushed before every step (256 MiB write); the inputs are larger than L2 as well",
+            "launch": "one CUDA graph per step (column quantization alongside the row pipeline, dgrad "
+                      "alongside wgrad, on two streams), replayed after a 0.2 ms GPU head start; kernel "
+                      "times from a second pass of one graph per phase",
+            "parallelism": f"replicas x{world}"}
 
 
 # ------------------------------------------------------------------ replicas
@@ -421,10 +436,11 @@ def run_gpu(args):
     step_ms = [ev_step[k][0].elapsed_time(ev_step[k][1]) for k in range(args.steps)]
     ms_per_step = sum(step_ms) / len(step_ms)
     seq_ms = sum(ev[k][0].elapsed_time(ev[k][ncalls]) for k in range(args.steps)) / args.steps
-    phase_ms = {}
+    phase_ms, call_ms = {}, []
     for i, (name, _) in enumerate(plan.calls):
-        phase_ms[name] = phase_ms.get(name, 0.0) + sum(ev[k][i].elapsed_time(ev[k][i + 1])
-                                                      for k in range(args.steps)) / args.steps
+        t = sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)) / args.steps
+        call_ms.append(t)
+        phase_ms[name] = phase_ms.get(name, 0.0) + t
 
     # ---- end to end through the C ABI from pinned host buffers
     hY = [torch.empty(l.Y.shape, dtype=l.Y.dtype).pin_memory() for l in plan.lins]
@@ -516,12 +532,31 @@ def run_gpu(args):
             ach, u, pk = per_s / 1e12, "TFLOP/s", peaks["bf16_tflops"]
         kernels[name] = {"ms": round(phase_ms[name], 5), "achieved": round(ach, 2), "unit": u, "peak": pk,
                          "frac": round(ach / pk, 4), "bound": "hbm" if unit == "B" else "tensor"}
-    dom = max(kernels, key=lambda n: kernels[n]["ms"])
-    kd = kernels[dom]
-    tr = dram_traffic(dom, args.workload)
-    roofline = {"bound": kd["bound"], "kernel": dom, "achieved": kd["achieved"], "peak": kd["peak"],
+    # roofline: the single launch (phase of one linear, or one activation's row
+    # call) with the longest time, its algorithmic work per launch / its time
+    per_call = []
+    for i, (name, _) in enumerate(plan.calls):
+        if name == ActStep.PHASE:
+            act = list(plan.acts.values())[i]
+            amount, unit, bound = act.algorithmic_bytes(), "B", "hbm"
+        else:
+            lin = plan.lins[(i - len(plan.acts)) // len(LinStep.PHASES)]
+            amount, unit, bound = lin.algorithmic()[name]
+        per_call.append((call_ms[i], name, plan.labels[i], amount, unit, bound))
+    ms_d, dom, dom_label, amount, unit, bound = max(per_call, key=lambda c: c[0])
+    per_s = amount / (ms_d * 1e-3)
+    if unit == "B":
+        ach, u, pk = per_s / 1e9, "GB/s", peaks["hbm_gbs"]
+    elif bound == "tensor_fp4":
+        ach, u, pk = per_s / 1e12, "TFLOP/s", fp4_peak
+    else:
+        ach, u, pk = per_s / 1e12, "TFLOP/s", peaks["bf16_tflops"]
+    tr = dram_traffic(dom, args.workload, dom_label)
+    roofline = {"bound": "hbm" if unit == "B" else "tensor", "kernel": dom, "launch": dom_label,
+                "achieved": round(ach, 2), "peak": pk,
                 "peak_source": f"{peak_src}" + (" x nominal FP4/BF16 ratio 6" if dom == "fp4_linear_fwd" else ""),
-                "unit": kd["unit"], "frac": kd["frac"], "traffic": tr}
+                "unit": u, "frac": round(ach / pk, 4), "traffic": tr, "launch_ms": round(ms_d, 5),
+                "work_per_launch": amount, "work_unit": "B" if unit == "B" else "FLOP"}
     qnames = (ActStep.PHASE, "fp4_quantize_cols")
     quant_bytes = sum(amounts[n][0] for n in qnames)
     quant_ms = sum(kernels[n]["ms"] for n in qnames)
@@ -532,14 +567,7 @@ def run_gpu(args):
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp4_e2m1 fwd / bf16 wgrad + dgrad, fp32 accumulate", "data": "synthetic (seeded, LLaMA-shaped)",
-        "config": {"workload": args.workload, "linears": [[l.name, l.M, l.K, l.N, l.q] for l in work.linears],
-                   "fused_shared_input": bool(args.fuse_shared_input), "only_linears": args.linear or None,
-                   "bwd": "weight gradient with DGE + input gradient dY W^T (BF16; the pages give no dgrad)",
-                   "l2": "flushed before every step",
-                   "launch": "one CUDA graph per step (column quantization alongside the row pipeline, dgrad "
-                             "alongside wgrad, on two streams), replayed after a 0.2 ms GPU head start; kernel "
-                             "times from a second pass of one graph per phase",
-                   "parallelism": f"replicas x{world}"},
+        "config": arm_config(args, work, world),
         "fp4_peak_frac": round(value / world / fp4_peak, 4),
         "quantize": {"gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1), "frac_of_hbm": round(
             quant_bytes / (quant_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
@@ -551,7 +579,7 @@ def run_gpu(args):
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:   # the CPU baseline is a single-GPU figure
-        line["cpu_baseline"] = cpu_baseline(args.workload, 4 * args.cpu_budget)   # about 10 s of one core
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_sample)   # two measured steps
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -567,85 +595,85 @@ import numpy as np
 from oracle import fp4_linear as orc
 from precision_gemm_row_gb300 import workloads as wl
 work = wl.WORKLOADS[sys.argv[2]]
-rows_sample = int(sys.argv[3])
+S = int(sys.argv[3])
 nsteps = int(sys.argv[4])
-inputs = [(lin, work.activation(lin), work.weight(lin), work.grad(lin)) for lin in work.linears]
-flops = sum(6 * lin.M * lin.K * lin.N for lin in work.linears)
+# the sub-problem of every linear: its first S tokens and first S output
+# columns, with the whole reduction length K (drawn once, outside the timing)
+inputs = []
+for lin in work.linears:
+    ms, ns = min(S, lin.M), min(S, lin.N)
+    A = work.activation(lin, rows=ms)
+    W = np.ascontiguousarray(work.weight(lin)[:, :ns])
+    dY = np.ascontiguousarray(work.grad(lin, rows=ms)[:, :ns])
+    inputs.append((lin, A, W, dY))
+flops = sum(6 * A.shape[0] * A.shape[1] * W.shape[1] for _, A, W, _ in inputs)
 steps = []
 for _ in range(nsteps):
-    total_est = 0.0
-    for lin, A_bits, W_bits, dY_bits in inputs:
-        t0 = time.perf_counter()
-        t, _, _ = orc.quantile_threshold(A_bits, lin.q)
-        A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
-        t1 = time.perf_counter()
-        rs = np.arange(min(rows_sample, lin.M))
-        a_codes_s, s_a_s = orc.quantize_rows(A_c[rs])
-        t2 = time.perf_counter()
-        w_codes, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
-        t3 = time.perf_counter()
-        a_full = np.zeros((lin.M, lin.K // 2), np.uint8)
-        a_full[rs] = a_codes_s
-        s_a_full = np.ones(lin.M, np.float32)
-        s_a_full[rs] = s_a_s
-        orc.linear_fwd(a_full, s_a_full, w_codes, s_w, rp, ci, cv, W_bits, rows=rs)
-        t4 = time.perf_counter()
-        ks = np.arange(min(rows_sample, lin.K))
-        orc.wgrad_dge(A_bits, dY_bits, W_bits, s_w, 5.0, 3.0, rows=ks)
-        t5 = time.perf_counter()
-        orc.f64_to_bf16(orc.linear_dgrad(dY_bits, W_bits, rows=rs))
-        t6 = time.perf_counter()
-        total_est += ((t1 - t0) + (t2 - t1) * lin.M / len(rs) + (t3 - t2) + (t4 - t3) * lin.M / len(rs)
-                      + (t5 - t4) * lin.K / len(ks) + (t6 - t5) * lin.M / len(rs))
-    steps.append(total_est)
+    t0 = time.perf_counter()
+    for lin, A, W, dY in inputs:
+        t, _, _ = orc.quantile_threshold(A, lin.q)
+        A_c, rp, ci, cv = orc.clamp_and_compensation(A, t)
+        a_codes, s_a = orc.quantize_rows(A_c)
+        w_codes, s_w = orc.quantize_cols(orc.bf16_to_f32(W))
+        orc.f64_to_bf16(orc.linear_fwd(a_codes, s_a, w_codes, s_w, rp, ci, cv, W))
+        orc.wgrad_dge(A, dY, W, s_w, 5.0, 3.0)
+        orc.f64_to_bf16(orc.linear_dgrad(dY, W))
+    steps.append(time.perf_counter() - t0)
 print(json.dumps(dict(steps=steps, flops=flops)))
 """
 
+ORACLE_SAMPLE = 256     # tokens x output columns of every linear's sub-problem
 
-def _oracle_steps(workload: str, rows_sample: int, nsteps: int):
+
+def _oracle_steps(workload: str, sample: int, nsteps: int):
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    r = subprocess.run([sys.executable, "-c", _ORACLE_SAMPLE, ROOT, workload, str(rows_sample), str(nsteps)],
+    r = subprocess.run([sys.executable, "-c", _ORACLE_SAMPLE, ROOT, workload, str(sample), str(nsteps)],
                        env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError("oracle baseline failed: " + r.stderr[-800:])
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def _sample_text(rows_sample: int) -> str:
-    return (f"per step: quantile + clamp + CSR of A and column quantization of W in full; row quantization and "
-            f"FP4 GEMM + epilogue and dgrad on the first {rows_sample} rows, DGE wgrad on the first {rows_sample} "
-            f"feature rows, each scaled linearly to the full size; one thread (OPENBLAS/OMP threads = 1)")
+def _sample_text(sample: int) -> str:
+    return (f"every linear of the workload on its first {sample} tokens x first {sample} output columns (the whole "
+            f"reduction length K): quantile + clamp + CSR + row codes of that activation slice, column codes of that "
+            f"weight slice, FP4 GEMM + epilogue, DGE weight gradient and input gradient, all measured (nothing "
+            f"extrapolated); value = 6 m K n summed over the sub-problems / measured time; one thread "
+            f"(OPENBLAS/OMP threads = 1)")
 
 
-def cpu_baseline(workload: str, rows_sample: int = 64):
+def cpu_baseline(workload: str, sample: int = ORACLE_SAMPLE, nsteps: int = 2):
     """The oracle, as it stands, timed in a fresh single-thread interpreter on a
-    bounded sample of one step of the workload (see _sample_text)."""
+    bounded sub-problem of every linear of the workload (see _sample_text)."""
     t0 = time.time()
-    d = _oracle_steps(workload, rows_sample, 1)
-    est = d["steps"][0]
-    return {"value": round(d["flops"] / est / 1e12, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": _sample_text(rows_sample), "est_step_s": round(est, 3), "wall_s": round(time.time() - t0, 1)}
+    d = _oracle_steps(workload, sample, nsteps)
+    step_s = statistics.median(d["steps"])
+    return {"value": round(d["flops"] / step_s / 1e12, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": _sample_text(sample), "sample_flops_per_step": d["flops"], "step_s": round(step_s, 6),
+            "steps": nsteps, "wall_s": round(time.time() - t0, 1)}
 
 
 def run_reference(args):
-    """`--impl reference`: the oracle on the host cores, W + K steps in one
-    process (inputs drawn once), median of the K timed steps."""
+    """`--impl reference`: the oracle on the host cores, W + K steps of the
+    bounded sub-problem in one process (inputs drawn once), each step measured;
+    ms_per_step is the median measured step time of what it ran."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
+    from precision_gemm_row_gb300 import workloads as wl
     t0 = time.time()
-    d = _oracle_steps(args.workload, args.cpu_budget, args.warmup + args.steps)
-    timed = d["steps"][args.warmup:]
-    est = statistics.median(timed)
-    v = round(d["flops"] / est / 1e12, 8)
-    cb = {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": _sample_text(args.cpu_budget),
-          "est_step_s": round(est, 3), "wall_s": round(time.time() - t0, 1)}
+    d = _oracle_steps(args.workload, args.cpu_sample, args.warmup + args.steps)
+    step_s = statistics.median(d["steps"][args.warmup:])
+    v = round(d["flops"] / step_s / 1e12, 8)
+    cb = {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": _sample_text(args.cpu_sample),
+          "sample_flops_per_step": d["flops"], "step_s": round(step_s, 6), "steps": args.steps,
+          "wall_s": round(time.time() - t0, 1)}
     return {"impl": "reference", "metric": "FP4 linear fwd+bwd TFLOPS on 1 GB300, % of dense FP4 peak; quantize GB/s "
             "vs HBM", "value": v, "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(est * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64/f32 (oracle)", "data": "synthetic (seeded, LLaMA-shaped)",
-            "config": {"workload": args.workload}, "cpu_baseline": cb,
+            "ms_per_step": round(step_s * 1e3, 3), "extrapolated": False, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (oracle)", "data": "synthetic (seeded, LLaMA-shaped)",
+            "config": arm_config(args, select_linears(wl, args), 1), "cpu_baseline": cb,
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -657,7 +685,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=int, default=64, help="rows sampled by the oracle baseline")
+    ap.add_argument("--cpu-sample", type=int, default=ORACLE_SAMPLE,
+                    help="tokens and output columns of every linear in the oracle's sub-problem")
     ap.add_argument("--fuse-shared-input", action="store_true",
                     help="linears reading the same activation run as one GEMM over their concatenated weights")
     ap.add_argument("--linear", action="append", default=[],

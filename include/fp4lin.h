@@ -27,6 +27,12 @@
  *    fp4_device_status reads; those calls still return FP4_OK.
  *  - Device: only compute capability 10.3 (GB300, sm_103a) is accepted;
  *    anything else returns FP4_ERR_DEVICE_UNSUPPORTED.
+ *  - Per-device state: on its first call on a device the library looks up
+ *    device addresses (its status word, the built-in scratch array of
+ *    fp4_quantize_cols_noalloc) and sets kernel attributes, and keeps them
+ *    for the life of the process.  Do not use the library on a device after
+ *    cudaDeviceReset (or any other teardown of that device's primary
+ *    context) in the same process: the kept addresses would be stale.
  */
 #ifndef FP4LIN_H
 #define FP4LIN_H

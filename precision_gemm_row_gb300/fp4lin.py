@@ -111,6 +111,21 @@ def _rowmajor(t: torch.Tensor, name: str, dtype: torch.dtype) -> int:
     return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), t.shape[1])
 
 
+def _vec(t: torch.Tensor, name: str, dtype: torch.dtype, n: int, device) -> None:
+    """A 1-D (or any contiguous) CUDA tensor of `dtype` with at least n elements on `device`."""
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous() or t.numel() < n or t.device != device:
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor of at least {n} elements on {device} "
+                         f"(got {t.dtype}, {tuple(t.shape)}, device {t.device})")
+
+
+def _mat(t: torch.Tensor, name: str, dtype: torch.dtype, rows: int, cols: int, device) -> int:
+    """A row-major CUDA matrix of `dtype`, at least rows x cols, on `device`; returns its leading dimension."""
+    ld = _rowmajor(t, name, dtype)
+    if t.shape[0] < rows or t.shape[1] < cols or t.device != device:
+        raise ValueError(f"{name} must be at least {rows} x {cols} on {device} (got {tuple(t.shape)} on {t.device})")
+    return ld
+
+
 def abi_version() -> int:
     return _lib.fp4_abi_version()
 
@@ -126,7 +141,10 @@ def fp4_quantize_rows(A: torch.Tensor, clamp_t: Optional[torch.Tensor] = None, c
         codes = torch.empty((M, K // 2), dtype=torch.uint8, device=A.device)
     if scales is None:
         scales = torch.empty((M,), dtype=torch.float32, device=A.device)
-    ldc = _rowmajor(codes, "codes", torch.uint8)
+    ldc = _mat(codes, "codes", torch.uint8, M, K // 2, A.device)
+    _vec(scales, "scales", torch.float32, M, A.device)
+    if clamp_t is not None:
+        _vec(clamp_t, "clamp_t", torch.float32, 1, A.device)
     _check("fp4_quantize_rows", _lib.fp4_quantize_rows(_p(A), M, K, lda, _p(clamp_t), _p(codes), ldc, _p(scales),
                                                        _s(stream)))
     return codes, scales
@@ -148,7 +166,9 @@ def fp4_quantize_cols(W: torch.Tensor, codes_t: Optional[torch.Tensor] = None, s
     ws_bytes = fp4_quantize_cols_workspace(N)
     if workspace is None:
         workspace = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=W.device)
-    ldc = _rowmajor(codes_t, "codes_t", torch.uint8)
+    ldc = _mat(codes_t, "codes_t", torch.uint8, N, K // 2, W.device)
+    _vec(scales, "scales", torch.float32, N, W.device)
+    _vec(workspace, "workspace", torch.uint8, ws_bytes, W.device)
     _check("fp4_quantize_cols", _lib.fp4_quantize_cols(_p(W), K, N, ldw, _p(codes_t), ldc, _p(scales), _p(workspace),
                                                        workspace.numel() * workspace.element_size(), _s(stream)))
     return codes_t, scales
@@ -160,7 +180,8 @@ def fp4_quantize_cols_noalloc(W: torch.Tensor, codes_t: torch.Tensor, scales: to
     this path is for callers that allocate nothing per call."""
     ldw = _rowmajor(W, "W", torch.bfloat16)
     K, N = W.shape
-    ldc = _rowmajor(codes_t, "codes_t", torch.uint8)
+    ldc = _mat(codes_t, "codes_t", torch.uint8, N, K // 2, W.device)
+    _vec(scales, "scales", torch.float32, N, W.device)
     _check("fp4_quantize_cols_noalloc", _lib.fp4_quantize_cols_noalloc(_p(W), K, N, ldw, _p(codes_t), ldc,
                                                                        _p(scales), _s(stream)))
     return codes_t, scales
@@ -197,12 +218,24 @@ def outlier_clamp_quantile(A: torch.Tensor, q: float, want_clamped: bool = False
     if want_clamped:
         o.setdefault("A_clamped", torch.empty_like(A))
     ac = o.get("A_clamped") if want_clamped else None
-    ldac = _rowmajor(ac, "A_clamped", torch.bfloat16) if ac is not None else 0
+    ldac = _mat(ac, "A_clamped", torch.bfloat16, M, K, dev) if ac is not None else 0
+    _check_outlier_outputs(o, M, cap, dev)
+    _vec(o["workspace"], "workspace", torch.uint8, ws_bytes, dev)
     ws = o["workspace"]
     _check("outlier_clamp_quantile", _lib.outlier_clamp_quantile(
         _p(A), M, K, lda, float(q), _p(o["t"]), _p(o["row_ptr"]), _p(o["col_idx"]), _p(o["vals"]),
         o["col_idx"].numel(), _p(o["nnz"]), _p(ac), ldac, _p(ws), ws.numel(), _s(stream)))
     return o
+
+
+def _check_outlier_outputs(o: Dict[str, torch.Tensor], M: int, cap: int, device) -> None:
+    _vec(o["t"], "t", torch.float32, 1, device)
+    _vec(o["row_ptr"], "row_ptr", torch.int32, M + 1, device)
+    _vec(o["col_idx"], "col_idx", torch.int32, cap, device)
+    _vec(o["vals"], "vals", torch.float32, cap, device)
+    _vec(o["nnz"], "nnz", torch.int64, 1, device)
+    if o["col_idx"].numel() != o["vals"].numel():
+        raise ValueError("col_idx and vals must have the same capacity")
 
 
 def fp4_quantize_rows_outliers(A: torch.Tensor, q: float, out: Optional[Dict[str, torch.Tensor]] = None,
@@ -223,7 +256,10 @@ def fp4_quantize_rows_outliers(A: torch.Tensor, q: float, out: Optional[Dict[str
     o.setdefault("scales", torch.empty((M,), dtype=torch.float32, device=dev))
     ws_bytes = outlier_clamp_quantile_workspace(M, K, o["col_idx"].numel())
     o.setdefault("workspace", torch.empty((ws_bytes,), dtype=torch.uint8, device=dev))
-    ldc = _rowmajor(o["codes"], "codes", torch.uint8)
+    ldc = _mat(o["codes"], "codes", torch.uint8, M, K // 2, dev)
+    _vec(o["scales"], "scales", torch.float32, M, dev)
+    _check_outlier_outputs(o, M, cap, dev)
+    _vec(o["workspace"], "workspace", torch.uint8, ws_bytes, dev)
     ws = o["workspace"]
     _check("fp4_quantize_rows_outliers", _lib.fp4_quantize_rows_outliers(
         _p(A), M, K, lda, float(q), _p(o["codes"]), ldc, _p(o["scales"]), _p(o["t"]), _p(o["row_ptr"]),
@@ -248,24 +284,32 @@ def fp4_linear_fwd(a_codes: torch.Tensor, s_a: Optional[torch.Tensor], w_codes_t
     cores when dA has few distinct columns); None forces the epilogue path; or a
     caller-owned CUDA uint8 tensor of at least fp4_linear_fwd_workspace(M, N, K) bytes.
     """
-    lda_c = _rowmajor(a_codes, "a_codes", torch.uint8)
-    ldw_c = _rowmajor(w_codes_t, "w_codes_t", torch.uint8)
+    dev = a_codes.device
     M, N = a_codes.shape[0], w_codes_t.shape[0]
+    lda_c = _mat(a_codes, "a_codes", torch.uint8, M, K // 2, dev)
+    ldw_c = _mat(w_codes_t, "w_codes_t", torch.uint8, N, K // 2, dev)
     yt = _OUT_TYPES[out_type]
+    if yt != FP4_OUT_RAW_ACC_FP32:
+        _vec(s_a, "s_a", torch.float32, M, dev)
+        _vec(s_w, "s_w", torch.float32, N, dev)
     if Y is None:
-        Y = torch.empty((M, N), dtype=torch.bfloat16 if yt == FP4_OUT_BF16 else torch.float32, device=a_codes.device)
-    ldy = _rowmajor(Y, "Y", torch.bfloat16 if yt == FP4_OUT_BF16 else torch.float32)
+        Y = torch.empty((M, N), dtype=torch.bfloat16 if yt == FP4_OUT_BF16 else torch.float32, device=dev)
+    ldy = _mat(Y, "Y", torch.bfloat16 if yt == FP4_OUT_BF16 else torch.float32, M, N, dev)
     rp = ci = cv = None
     ldw = 0
     ws, ws_bytes = None, 0
     if csr is not None:
         rp, ci, cv = csr["row_ptr"], csr["col_idx"], csr["vals"]
-        ldw = _rowmajor(W, "W", torch.bfloat16)
+        _vec(rp, "row_ptr", torch.int32, M + 1, dev)
+        _vec(ci, "col_idx", torch.int32, 0, dev)
+        _vec(cv, "vals", torch.float32, 0, dev)
+        ldw = _mat(W, "W", torch.bfloat16, K, N, dev)
         if isinstance(workspace, str):
             if workspace != "auto":
                 raise ValueError("workspace must be 'auto', None or a CUDA uint8 tensor")
             workspace = torch.empty(fp4_linear_fwd_workspace(M, N, K), dtype=torch.uint8, device=a_codes.device)
         if workspace is not None:
+            _vec(workspace, "workspace", torch.uint8, fp4_linear_fwd_workspace(M, N, K), dev)
             ws, ws_bytes = workspace, workspace.numel() * workspace.element_size()
     _check("fp4_linear_fwd", _lib.fp4_linear_fwd(
         _p(a_codes), lda_c, _p(s_a), _p(w_codes_t), ldw_c, _p(s_w), M, N, K, _p(rp), _p(ci), _p(cv), _p(W), ldw,
@@ -285,6 +329,7 @@ def _bwd_workspace(workspace, nbytes: int, device):
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
     if workspace is None:
         return None, 0
+    _vec(workspace, "workspace", torch.uint8, nbytes, device)
     return workspace, workspace.numel() * workspace.element_size()
 
 
@@ -303,13 +348,14 @@ def fp4_linear_wgrad_dge(A: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, s_w
                          workspace="auto", stream=None) -> torch.Tensor:
     """dW = (A^T dY) * f'(|W s_W|), fp32 (K x N).  workspace: see _bwd_workspace."""
     lda = _rowmajor(A, "A", torch.bfloat16)
-    lddy = _rowmajor(dY, "dY", torch.bfloat16)
-    ldw = _rowmajor(W, "W", torch.bfloat16)
     M, K = A.shape
     N = dY.shape[1]
+    lddy = _mat(dY, "dY", torch.bfloat16, M, N, A.device)
+    ldw = _mat(W, "W", torch.bfloat16, K, N, A.device)
+    _vec(s_w, "s_w", torch.float32, N, A.device)
     if dW is None:
         dW = torch.empty((K, N), dtype=torch.float32, device=A.device)
-    lddw = _rowmajor(dW, "dW", torch.float32)
+    lddw = _mat(dW, "dW", torch.float32, K, N, A.device)
     ws, ws_bytes = _bwd_workspace(workspace, fp4_linear_wgrad_dge_workspace(M, N, K), A.device)
     _check("fp4_linear_wgrad_dge", _lib.fp4_linear_wgrad_dge(
         _p(A), lda, _p(dY), lddy, _p(W), ldw, _p(s_w), M, N, K, float(dge_k), float(dge_clip), _p(dW), lddw,
@@ -321,16 +367,16 @@ def fp4_linear_dgrad(dY: torch.Tensor, W: torch.Tensor, out_dtype: torch.dtype =
                      dX: Optional[torch.Tensor] = None, workspace="auto", stream=None) -> torch.Tensor:
     """dX = dY W^T (M x K), BF16 or fp32; fp32 accumulation.  workspace: see _bwd_workspace."""
     lddy = _rowmajor(dY, "dY", torch.bfloat16)
-    ldw = _rowmajor(W, "W", torch.bfloat16)
     M, N = dY.shape
     K = W.shape[0]
     if W.shape[1] != N:
         raise ValueError(f"W must be K x {N} (got {tuple(W.shape)})")
+    ldw = _mat(W, "W", torch.bfloat16, K, N, dY.device)
     if dX is None:
         dX = torch.empty((M, K), dtype=out_dtype, device=dY.device)
     if dX.dtype not in (torch.bfloat16, torch.float32):
         raise ValueError(f"dX must be bfloat16 or float32 (got {dX.dtype})")
-    lddx = _rowmajor(dX, "dX", dX.dtype)
+    lddx = _mat(dX, "dX", dX.dtype, M, K, dY.device)
     dx_type = FP4_OUT_BF16 if dX.dtype == torch.bfloat16 else FP4_OUT_FP32
     ws, ws_bytes = _bwd_workspace(workspace, fp4_linear_dgrad_workspace(M, N, K), dY.device)
     _check("fp4_linear_dgrad", _lib.fp4_linear_dgrad(

@@ -56,14 +56,18 @@ def outlier_channels(seed: int, name: str, K: int, frac: float = 0.005) -> np.nd
     return np.sort(perm[:n_out])
 
 
-def draw_activation(seed: int, name: str, M: int, K: int, kind: str) -> np.ndarray:
-    """Activation A (M x K) as BF16 bits.
+def draw_activation(seed: int, name: str, M: int, K: int, kind: str, rows: int | None = None) -> np.ndarray:
+    """Activation A (M x K) as BF16 bits, or only its first `rows` rows.
 
     kind = "normal_x20"       N(0,1), 0.5 % of channels multiplied by 20
            "normal_redraw15"  N(0,1), 0.5 % of channels redrawn ~N(0, 15^2)
            "normal_4x20"      N(0,1), 4 channels multiplied by 20
            "student_t3"       Student-t, 3 degrees of freedom, per element
+
+    Every stream is consumed in row-major order, so the first `rows` rows are
+    the same values as the first rows of the whole draw.
     """
+    M = M if rows is None else min(M, rows)
     rng = _rng(seed, name)
     if kind == "student_t3":
         x = rng.standard_t(3, size=(M, K)).astype(np.float32)
@@ -89,8 +93,9 @@ def draw_weight(seed: int, name: str, K: int, N: int, std: float = 0.02) -> np.n
     return f32_to_bf16_bits(x)
 
 
-def draw_grad(seed: int, name: str, M: int, N: int, std: float = 1e-3) -> np.ndarray:
-    """Output gradient dY (M x N) as BF16 bits."""
+def draw_grad(seed: int, name: str, M: int, N: int, std: float = 1e-3, rows: int | None = None) -> np.ndarray:
+    """Output gradient dY (M x N) as BF16 bits, or only its first `rows` rows."""
+    M = M if rows is None else min(M, rows)
     x = _rng(seed, name).standard_normal(size=(M, N), dtype=np.float32) * np.float32(std)
     return f32_to_bf16_bits(x)
 
@@ -119,14 +124,14 @@ class Workload:
     description: str
     linears: Tuple[LinearCase, ...]
 
-    def activation(self, lin: LinearCase) -> np.ndarray:
-        return draw_activation(self.seed, lin.act, lin.M, lin.K, lin.act_kind)
+    def activation(self, lin: LinearCase, rows: int | None = None) -> np.ndarray:
+        return draw_activation(self.seed, lin.act, lin.M, lin.K, lin.act_kind, rows=rows)
 
     def weight(self, lin: LinearCase) -> np.ndarray:
         return draw_weight(self.seed, "W/" + (lin.weight_name or lin.name), lin.K, lin.N)
 
-    def grad(self, lin: LinearCase) -> np.ndarray:
-        return draw_grad(self.seed, "dY/" + lin.name, lin.M, lin.N)
+    def grad(self, lin: LinearCase, rows: int | None = None) -> np.ndarray:
+        return draw_grad(self.seed, "dY/" + lin.name, lin.M, lin.N, rows=rows)
 
 
 def _decoder(key: str, seed: int, desc: str, M: int, H: int, F: int) -> Workload:
@@ -196,14 +201,14 @@ class FusedWorkload:
         self.linears: Tuple[LinearCase, ...] = tuple(fused)
         self.description = work.description + " (linears sharing an input fused along N)"
 
-    def activation(self, lin: LinearCase) -> np.ndarray:
-        return self.base.activation(self.members[lin.name][0])
+    def activation(self, lin: LinearCase, rows: int | None = None) -> np.ndarray:
+        return self.base.activation(self.members[lin.name][0], rows=rows)
 
     def weight(self, lin: LinearCase) -> np.ndarray:
         return np.concatenate([self.base.weight(l) for l in self.members[lin.name]], axis=1)
 
-    def grad(self, lin: LinearCase) -> np.ndarray:
-        return np.concatenate([self.base.grad(l) for l in self.members[lin.name]], axis=1)
+    def grad(self, lin: LinearCase, rows: int | None = None) -> np.ndarray:
+        return np.concatenate([self.base.grad(l, rows=rows) for l in self.members[lin.name]], axis=1)
 
 
 def fuse_shared_inputs(work: Workload) -> FusedWorkload:

@@ -1,6 +1,8 @@
 """Helpers shared by the GPU parity tests: host <-> device transfer of BF16 bit
 patterns and the comparison rules (bit-exact, BF16 ulp distance, relative
 Frobenius error)."""
+import os
+
 import numpy as np
 import torch
 
@@ -64,3 +66,37 @@ def assert_bf16_compensated_close(got_bits: np.ndarray, y_ref: np.ndarray, magni
     bad = np.abs(got - y_ref) > allowed
     assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], y_ref[bad][:5])
     return int(np.count_nonzero(bf16_ulp_distance(got_bits, orc.f64_to_bf16(y_ref)) > BF16_ULP_TOL))
+
+
+def _golden_e2m1_x2() -> list:
+    """Twice the value of every E2M1 code (an integer), read from the golden
+    format table tests/golden/e2m1_codes.txt (written from the pages' bit layout)."""
+    vals = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", "e2m1_codes.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if line:
+                vals[int(line[0])] = int(round(2 * float(line[4])))
+    return [vals[c] for c in range(16)]
+
+
+def codes_to_int8_x2(packed: torch.Tensor) -> torch.Tensor:
+    """Packed E2M1 codes (R x C/2 uint8, element 2c in the low nibble) -> R x C int8
+    holding twice each value, on the tensors' device (test-side decode by table)."""
+    lut = torch.tensor(_golden_e2m1_x2(), dtype=torch.int8, device=packed.device)
+    lo = lut[(packed & 15).long()]
+    hi = lut[(packed >> 4).long()]
+    return torch.stack((lo, hi), dim=-1).reshape(packed.shape[0], 2 * packed.shape[1])
+
+
+def assert_raw_acc_equals_int_mm(raw: torch.Tensor, a_codes: torch.Tensor, w_codes_t: torch.Tensor):
+    """The whole M x N raw FP4 accumulator against torch._int_mm (cuBLASLt int8,
+    an independent library) on the x2 integer codes: 4 acc == (2 qA)(2 qW)^T
+    exactly (every value is an integer below 2^24, so fp32 holds it exactly)."""
+    a8 = codes_to_int8_x2(a_codes)
+    w8 = codes_to_int8_x2(w_codes_t)
+    ref = torch._int_mm(a8, w8.t())
+    got = raw.mul(4.0)
+    assert torch.equal(got, got.round()), "raw accumulator is not a multiple of 1/4"
+    bad = (got.to(torch.int32) != ref)
+    assert not bool(bad.any()), (int(bad.sum()), torch.nonzero(bad)[:5].tolist())

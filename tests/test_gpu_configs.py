@@ -6,8 +6,10 @@ Student-t stress case), run through the same launches bench.py times
 * CSR: every row's count against a full count of |A| > t; column indices and
   values bit-exact on sampled rows;
 * row codes / scales bit-exact on sampled rows; column codes / scales bit-exact
-  on sampled columns;
-* raw FP4 accumulators bit-exact, BF16 Y (1 ulp + fp32 sum bound) on sampled rows;
+  on every column;
+* the whole M x N raw FP4 accumulator against torch._int_mm (cuBLASLt int8) on
+  the x2 integer codes; raw accumulators bit-exact and BF16 Y (1 ulp + fp32 sum
+  bound) against the oracle, from the oracle's own codes, on sampled rows;
 * DGE weight gradient within 1e-5 relative Frobenius on sampled feature rows;
 * BF16 input gradient dY W^T within 1 ulp + the tensor-core sum bound on sampled rows.
 """
@@ -20,7 +22,7 @@ import torch
 from oracle import fp4_linear as orc
 from precision_gemm_row_gb300 import workloads as wl
 from tests.gpu_common import (FROB_TOL, TC_SUM_BOUND, assert_bf16_compensated_close, assert_no_device_flags,
-                              dev_bf16, host_bits, rel_frobenius)
+                              assert_raw_acc_equals_int_mm, dev_bf16, host_bits, rel_frobenius)
 
 pytestmark = pytest.mark.gpu
 
@@ -74,7 +76,6 @@ def test_full_size_linear(fp4, workload, linear):
     assert_no_device_flags(fp4)
     M, K, N = lin.M, lin.K, lin.N
     rows = _sample(M, 1)
-    cols = _sample(N, 2)
     frows = _sample(K, 3)
 
     # threshold over all of |A|
@@ -96,26 +97,25 @@ def test_full_size_linear(fp4, workload, linear):
     ref_a, ref_sa = orc.quantize_rows(A_c_s)
     assert np.array_equal(act.out["codes"][torch.from_numpy(rows).cuda()].cpu().numpy(), ref_a)
     assert np.array_equal(act.out["scales"].cpu().numpy()[rows].view(np.uint32), ref_sa.view(np.uint32))
-    # column quantization of W on sampled columns
+    # column quantization of W: every column against the oracle
     Wf = orc.bf16_to_f32(W_bits)
-    ref_w, ref_sw = orc.quantize_cols(Wf[:, cols])
-    assert np.array_equal(step.w_codes[torch.from_numpy(cols).cuda()].cpu().numpy(), ref_w)
-    assert np.array_equal(step.s_w.cpu().numpy()[cols].view(np.uint32), ref_sw.view(np.uint32))
-    # GEMM: raw accumulator (bit-exact) and compensated BF16 Y on sampled rows, from the GPU's own codes
-    a_codes = act.out["codes"].cpu().numpy()
-    w_codes = step.w_codes.cpu().numpy()
-    s_a = act.out["scales"].cpu().numpy()
-    s_w = step.s_w.cpu().numpy()
+    ref_w, ref_sw = orc.quantize_cols(Wf)
+    assert np.array_equal(step.w_codes.cpu().numpy(), ref_w)
+    assert np.array_equal(step.s_w.cpu().numpy().view(np.uint32), ref_sw.view(np.uint32))
+    # GEMM: the whole M x N raw accumulator against cuBLASLt int8 on the codes,
+    # and the sampled rows (raw and compensated BF16 Y) against the oracle, built
+    # from the oracle's own codes and scales
     raw = fp4.fp4_linear_fwd(act.out["codes"], None, step.w_codes, None, K, out_type="raw")
-    ref_raw = orc.gemm_raw(a_codes, w_codes, rows=rows).astype(np.float32)
+    assert_raw_acc_equals_int_mm(raw, act.out["codes"], step.w_codes)
+    ref_raw = orc.gemm_raw(ref_a, ref_w).astype(np.float32)
     assert np.array_equal(raw[torch.from_numpy(rows).cuda()].cpu().numpy().view(np.uint32), ref_raw.view(np.uint32))
-    rp32 = rp.astype(np.int32)
-    y_ref = orc.linear_fwd(a_codes, s_a, w_codes, s_w, rp32, ci_g, cv_g, W_bits, rows=rows)
-    mag = orc.linear_fwd_magnitude(a_codes, s_a, w_codes, s_w, rp32, ci_g, cv_g, W_bits, rows=rows)
+    del raw
+    y_ref = orc.linear_fwd(ref_a, ref_sa, ref_w, ref_sw, rp_s, ci_s, cv_s, W_bits)
+    mag = orc.linear_fwd_magnitude(ref_a, ref_sa, ref_w, ref_sw, rp_s, ci_s, cv_s, W_bits)
     y_gpu = host_bits(step.Y[torch.from_numpy(rows).cuda()])
     assert_bf16_compensated_close(y_gpu, y_ref, mag)
     # DGE weight gradient on sampled feature rows
-    dw_ref = orc.wgrad_dge(A_bits, dY_bits, W_bits, s_w, 5.0, 3.0, rows=frows)
+    dw_ref = orc.wgrad_dge(A_bits, dY_bits, W_bits, ref_sw, 5.0, 3.0, rows=frows)
     dw_gpu = step.dW[torch.from_numpy(frows).cuda()].cpu().numpy()
     assert rel_frobenius(dw_gpu, dw_ref) <= FROB_TOL
     # input gradient on sampled token rows
@@ -146,10 +146,15 @@ def test_fused_shared_input_linears_7b_layer(fp4):
         assert_no_device_flags(fp4)
         act, step = next(iter(plan.acts.values())), plan.lins[0]
         rows, frows = _sample(lin.M, 5), _sample(lin.K, 6)
-        rp = act.out["row_ptr"].cpu().numpy().astype(np.int32)
-        ci, cv = act.out["col_idx"].cpu().numpy(), act.out["vals"].cpu().numpy()
-        a_codes, s_a = act.out["codes"].cpu().numpy(), act.out["scales"].cpu().numpy()
+        # the oracle's threshold, CSR and row codes of the sampled rows
+        t, _, _ = orc.quantile_threshold(A_bits, lin.q)
+        A_c_s, rp_s, ci_s, cv_s = orc.clamp_and_compensation(A_bits[rows], t)
+        ref_a, ref_sa = orc.quantize_rows(A_c_s)
+        assert np.array_equal(act.out["codes"][torch.from_numpy(rows).cuda()].cpu().numpy(), ref_a)
         w_codes, s_w = step.w_codes.cpu().numpy(), step.s_w.cpu().numpy()
+        raw = fp4.fp4_linear_fwd(act.out["codes"], None, step.w_codes, None, lin.K, out_type="raw")
+        assert_raw_acc_equals_int_mm(raw, act.out["codes"], step.w_codes)
+        del raw
         Y = host_bits(step.Y[torch.from_numpy(rows).cuda()])
         dW = step.dW[torch.from_numpy(frows).cuda()].cpu().numpy()
         dx_ref = np.zeros((rows.size, lin.K))
@@ -158,14 +163,13 @@ def test_fused_shared_input_linears_7b_layer(fp4):
         for m in work.members[lin.name]:
             blk = slice(c0, c0 + m.N)
             Wm, dYm = base.weight(m), base.grad(m)
-            cols = c0 + _sample(m.N, 7)
-            ref_w, ref_sw = orc.quantize_cols(orc.bf16_to_f32(Wm)[:, cols - c0])
-            assert np.array_equal(w_codes[cols], ref_w)
-            assert np.array_equal(s_w[cols].view(np.uint32), ref_sw.view(np.uint32))
-            y_ref = orc.linear_fwd(a_codes, s_a, w_codes[blk], s_w[blk], rp, ci, cv, Wm, rows=rows)
-            mag = orc.linear_fwd_magnitude(a_codes, s_a, w_codes[blk], s_w[blk], rp, ci, cv, Wm, rows=rows)
+            ref_w, ref_sw = orc.quantize_cols(orc.bf16_to_f32(Wm))      # every column of the member
+            assert np.array_equal(w_codes[blk], ref_w)
+            assert np.array_equal(s_w[blk].view(np.uint32), ref_sw.view(np.uint32))
+            y_ref = orc.linear_fwd(ref_a, ref_sa, ref_w, ref_sw, rp_s, ci_s, cv_s, Wm)
+            mag = orc.linear_fwd_magnitude(ref_a, ref_sa, ref_w, ref_sw, rp_s, ci_s, cv_s, Wm)
             assert_bf16_compensated_close(Y[:, blk], y_ref, mag)
-            dw_ref = orc.wgrad_dge(A_bits, dYm, Wm, s_w[blk], 5.0, 3.0, rows=frows)
+            dw_ref = orc.wgrad_dge(A_bits, dYm, Wm, ref_sw, 5.0, 3.0, rows=frows)
             assert rel_frobenius(dW[:, blk], dw_ref) <= FROB_TOL
             dx_ref += orc.linear_dgrad(dYm, Wm, rows=rows)
             dx_mag += orc.linear_dgrad(dYm & np.uint16(0x7FFF), Wm & np.uint16(0x7FFF), rows=rows)

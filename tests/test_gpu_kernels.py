@@ -536,3 +536,44 @@ def test_linear_forward_pipeline_c1(fp4):
                                    ref["col_idx"], ref["vals"], W_bits)
     assert_bf16_compensated_close(host_bits(Y), ref["Y"], mag)
     assert_no_device_flags(fp4)
+
+
+# ---------------------------------------------------------------- binding checks
+
+def test_binding_rejects_undersized_or_mistyped_buffers(fp4):
+    """The C ABI cannot see buffer sizes, so the binding checks every tensor it
+    passes: an output too small, of the wrong dtype or on the wrong device is
+    refused before any launch (nothing is written)."""
+    K, N, M = 256, 64, 32
+    W = dev_bf16(_normal_bits(1, (K, N), 0.02))
+    A = dev_bf16(_normal_bits(2, (M, K)))
+    u8 = lambda *s: torch.zeros(s, dtype=torch.uint8, device="cuda")
+    f32 = lambda *s: torch.zeros(s, dtype=torch.float32, device="cuda")
+    bad_calls = [
+        lambda: fp4.fp4_quantize_cols(W, codes_t=u8(N - 1, K // 2)),
+        lambda: fp4.fp4_quantize_cols(W, codes_t=u8(N, K // 2 - 16)),
+        lambda: fp4.fp4_quantize_cols(W, scales=f32(N - 1)),
+        lambda: fp4.fp4_quantize_cols(W, scales=torch.zeros(N, dtype=torch.float16, device="cuda")),
+        lambda: fp4.fp4_quantize_cols(W, workspace=u8(8)),
+        lambda: fp4.fp4_quantize_cols_noalloc(W, u8(N, K // 2), f32(N - 8)),
+        lambda: fp4.fp4_quantize_cols_noalloc(W, u8(N, K // 2), torch.zeros(N)),            # host memory
+        lambda: fp4.fp4_quantize_rows(A, codes=u8(M - 1, K // 2)),
+        lambda: fp4.fp4_quantize_rows(A, scales=f32(M - 1)),
+        lambda: fp4.fp4_quantize_rows_outliers(A, 0.99, out={"codes": u8(M, K // 2 - 16)}),
+        lambda: fp4.fp4_quantize_rows_outliers(A, 0.99, out={"row_ptr": torch.zeros(M, dtype=torch.int32,
+                                                                                      device="cuda")}),
+        lambda: fp4.fp4_linear_wgrad_dge(A, dev_bf16(_normal_bits(3, (M, N))), W, f32(N - 1)),
+        lambda: fp4.fp4_linear_dgrad(dev_bf16(_normal_bits(3, (M, N))), W, dX=f32(M, K - 8)),
+    ]
+    for i, call in enumerate(bad_calls):
+        with pytest.raises(ValueError):
+            call()
+    codes, s_w = fp4.fp4_quantize_cols(W)
+    a_codes, s_a = fp4.fp4_quantize_rows(A)
+    with pytest.raises(ValueError):
+        fp4.fp4_linear_fwd(a_codes, s_a, codes, s_w, K, Y=torch.zeros((M, N - 8), dtype=torch.bfloat16,
+                                                                         device="cuda"))
+    with pytest.raises(ValueError):
+        fp4.fp4_linear_fwd(a_codes, s_a[: M - 1], codes, s_w, K)
+    torch.cuda.synchronize()
+    assert_no_device_flags(fp4)

@@ -161,3 +161,53 @@ def test_untransposed_weight_in_dgrad_is_caught(monkeypatch):
 
     monkeypatch.setattr(orc, "linear_dgrad", no_transpose)
     _expect_failure(pins.test_dgrad_is_the_adjoint_of_the_forward_product, 24, 24)
+
+
+def _magnitude_with(body):
+    """linear_fwd_magnitude rebuilt with one planted change in its compensation sum."""
+    def mag(a_codes, s_a, w_codes_t, s_w, row_ptr, col_idx, vals, W_bits, rows=None):
+        t1 = np.abs(orc.linear_fwd(a_codes, s_a, w_codes_t, s_w, rows=rows))
+        rows_ = np.arange(np.asarray(a_codes).shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+        W = orc.bf16_to_f32(W_bits).astype(np.float64)
+        rp = np.asarray(row_ptr, dtype=np.int64)
+        return body(t1, rows_, W, rp, np.asarray(col_idx, np.int64), np.asarray(vals, np.float64))
+    return mag
+
+
+def test_magnitude_with_signed_compensation_is_caught(monkeypatch):
+    def body(t1, rows, W, rp, ci, v):
+        for r, i in enumerate(rows):
+            t1[r] += v[rp[i]:rp[i + 1]] @ np.abs(W[ci[rp[i]:rp[i + 1]]])     # signed dA
+        return t1
+    monkeypatch.setattr(orc, "linear_fwd_magnitude", _magnitude_with(body))
+    _expect_failure(pins.test_fwd_magnitude_bruteforce_fractions)
+    _expect_failure(pins.test_fwd_magnitude_invariants)
+
+
+def test_magnitude_with_signed_weights_is_caught(monkeypatch):
+    def body(t1, rows, W, rp, ci, v):
+        for r, i in enumerate(rows):
+            t1[r] += np.abs(v[rp[i]:rp[i + 1]]) @ W[ci[rp[i]:rp[i + 1]]]     # signed W
+        return t1
+    monkeypatch.setattr(orc, "linear_fwd_magnitude", _magnitude_with(body))
+    _expect_failure(pins.test_fwd_magnitude_bruteforce_fractions)
+
+
+def test_magnitude_with_gemm_term_twice_is_caught(monkeypatch):
+    def body(t1, rows, W, rp, ci, v):
+        t1 = 2.0 * t1                                                       # GEMM term counted twice
+        for r, i in enumerate(rows):
+            t1[r] += np.abs(v[rp[i]:rp[i + 1]]) @ np.abs(W[ci[rp[i]:rp[i + 1]]])
+        return t1
+    monkeypatch.setattr(orc, "linear_fwd_magnitude", _magnitude_with(body))
+    _expect_failure(pins.test_fwd_magnitude_bruteforce_fractions)
+
+
+def test_magnitude_with_wrong_row_under_subset_is_caught(monkeypatch):
+    def body(t1, rows, W, rp, ci, v):
+        for r, i in enumerate(rows):
+            a, b = rp[r], rp[r + 1]                                          # position, not the row index
+            t1[r] += np.abs(v[a:b]) @ np.abs(W[ci[a:b]])
+        return t1
+    monkeypatch.setattr(orc, "linear_fwd_magnitude", _magnitude_with(body))
+    _expect_failure(pins.test_fwd_magnitude_invariants)

@@ -238,6 +238,61 @@ def test_compensation_term_is_dA_times_W():
     assert np.array_equal(y2, y0)
 
 
+def _magnitude_case(seed=21, M=5, K=32, N=6, q=0.8):
+    """A tiny compensated layer with several dA entries per row (Student-t A)."""
+    rng = np.random.default_rng(seed)
+    A_bits = wl.f32_to_bf16_bits(rng.standard_t(3, size=(M, K)).astype(np.float32))
+    W_bits = _bf16_matrix(rng, (K, N), 0.02)
+    t, _, _ = orc.quantile_threshold(A_bits, q)
+    A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
+    a_codes, s_a = orc.quantize_rows(A_c)
+    w_codes_t, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+    return A_bits, W_bits, a_codes, s_a, w_codes_t, s_w, rp, ci, cv
+
+
+def test_fwd_magnitude_bruteforce_fractions():
+    """|acc/(s_A s_W)| + sum_k |dA[i,k]| |W[k,j]| with exact rationals: the size
+    of the two terms the compensated output adds (the epilogue's fp32 rounding
+    is relative to it), from the decoded codes, the exact fp32 scales and the
+    exact BF16 weights."""
+    A_bits, W_bits, a_codes, s_a, w_codes_t, s_w, rp, ci, cv = _magnitude_case()
+    M, N, K = a_codes.shape[0], w_codes_t.shape[0], a_codes.shape[1] * 2
+    assert rp[-1] >= M        # several entries
+    mag = orc.linear_fwd_magnitude(a_codes, s_a, w_codes_t, s_w, rp, ci, cv, W_bits)
+    Wf = orc.bf16_to_f32(W_bits)
+
+    def dec(packed, r, k):
+        return Fraction(orc.e2m1_decode(int(packed[r, k // 2] >> (4 * (k % 2))) & 0xF))
+
+    for i in range(M):
+        for j in range(N):
+            acc = sum(dec(a_codes, i, k) * dec(w_codes_t, j, k) for k in range(K))
+            ref = abs(acc) / (Fraction(float(s_a[i])) * Fraction(float(s_w[j])))
+            for e in range(rp[i], rp[i + 1]):
+                ref += abs(Fraction(float(cv[e]))) * abs(Fraction(float(Wf[ci[e], j])))
+            assert abs(Fraction(float(mag[i, j])) - ref) <= Fraction(2.0 ** -50) * ref, (i, j)
+
+
+def test_fwd_magnitude_invariants():
+    """Triangle inequality (the magnitude bounds |Y|), independence of the signs
+    of dA, no compensation = |uncompensated Y|, and a row subset = those rows."""
+    A_bits, W_bits, a_codes, s_a, w_codes_t, s_w, rp, ci, cv = _magnitude_case(seed=22, M=8, K=64, N=10)
+    mag = orc.linear_fwd_magnitude(a_codes, s_a, w_codes_t, s_w, rp, ci, cv, W_bits)
+    Y = orc.linear_fwd(a_codes, s_a, w_codes_t, s_w, rp, ci, cv, W_bits)
+    assert np.all(np.abs(Y) <= mag * (1 + 1e-12))
+    flipped = orc.linear_fwd_magnitude(a_codes, s_a, w_codes_t, s_w, rp, ci, -cv, W_bits)
+    assert np.array_equal(flipped, mag)
+    empty = np.zeros(a_codes.shape[0] + 1, np.int32)
+    y0 = orc.linear_fwd(a_codes, s_a, w_codes_t, s_w)
+    assert np.array_equal(orc.linear_fwd_magnitude(a_codes, s_a, w_codes_t, s_w, empty, ci[:0], cv[:0], W_bits),
+                          np.abs(y0))
+    rows = [7, 2, 5]
+    assert np.array_equal(orc.linear_fwd_magnitude(a_codes, s_a, w_codes_t, s_w, rp, ci, cv, W_bits, rows=rows),
+                          mag[rows])
+    # the compensation's magnitude adds: every entry moves it up by |dA| |W|
+    assert np.all(mag >= np.abs(y0) - 1e-15)
+
+
 def test_forward_approximates_dense_product():
     # with the compensation added back, the FP4 layer approximates A @ W; the
     # error is bounded by the E2M1 rounding error of A_clamped and W.

@@ -33,8 +33,9 @@ def _rank_main(rank, world, port, out):
         dist.barrier()
 
         class Args:
-            workload = bench.DEFAULT_WORKLOAD
-            steps, warmup, cpu_budget = 1, 3, 1
+            workload = "c1_single_linear_256x512x512"
+            steps, warmup, cpu_sample = 1, 3, 16
+            fuse_shared_input, linear = False, []
         ref = bench.run_reference(Args) if rank != 0 else "rank 0 runs the oracle"
         out[rank] = (ms, ref)
     finally:

@@ -80,7 +80,8 @@ def test_reference_arm_line_on_the_small_workload():
     """bench.py --impl reference times the oracle on the host; its JSON line
     carries the contract's keys (checked on the 256 x 512 x 512 workload)."""
     import bench
-    args = types.SimpleNamespace(workload="c1_single_linear_256x512x512", steps=1, warmup=3, cpu_budget=16)
+    args = types.SimpleNamespace(workload="c1_single_linear_256x512x512", steps=1, warmup=3, cpu_sample=16,
+                                 fuse_shared_input=False, linear=[])
     line = bench.run_reference(args)
     assert line["impl"] == "reference" and line["value"] > 0 and line["higher_is_better"] is True
     assert line["unit"] == "TFLOP/s" and line["metric"].startswith("FP4 linear fwd+bwd TFLOPS")
@@ -88,3 +89,21 @@ def test_reference_arm_line_on_the_small_workload():
     assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["steps"] == 1 and line["warmup"] == 3
+    # measured, not extrapolated: the step time is what the sub-problem took, and
+    # the value is the sub-problem's work over that time
+    assert line["extrapolated"] is False
+    cb = line["cpu_baseline"]
+    assert line["ms_per_step"] == pytest.approx(cb["step_s"] * 1e3, abs=1e-3)
+    assert line["value"] == pytest.approx(cb["sample_flops_per_step"] / cb["step_s"] / 1e12, rel=2e-3)
+    assert cb["sample_flops_per_step"] == 6 * 16 * 512 * 16
+    assert line["config"]["workload"] == "c1_single_linear_256x512x512"
+    assert line["config"]["linears"] == [["linear", 256, 512, 512, 0.99]]
+
+
+def test_row_prefix_draws_equal_the_whole_draw():
+    """The oracle's sub-problem draws only the first rows of A and dY; every
+    activation kind gives the same values as the first rows of the full draw."""
+    for kind in ("normal", "normal_x20", "normal_redraw15", "normal_4x20", "student_t3"):
+        full = wl.draw_activation(7, "a", 96, 64, kind)
+        assert np.array_equal(wl.draw_activation(7, "a", 96, 64, kind, rows=10), full[:10]), kind
+    assert np.array_equal(wl.draw_grad(7, "g", 96, 40, rows=5), wl.draw_grad(7, "g", 96, 40)[:5])

@@ -4,8 +4,12 @@ regular one (fp4_quantize_cols with a caller workspace), through the C ABI.
 fp4_quantize_cols_noalloc serves callers that cannot give the library scratch
 memory; its column maxima live in a device array built into the library.  Two
 calls in a row on different inputs show that each call starts from a cleared
-array (no stale maxima leak from the previous call).  The file is collected
-last so that, under `-x`, every other test has already run if this one fails.
+array: the first call leaves large column maxima behind (values of scale 3),
+the second quantizes smaller values (scale 0.02) in the same columns, so a
+maximum left over from the first call would change the second call's scales
+and codes.  Both calls are also checked against the oracle.  The file is
+collected last so that, under `-x`, every other test has already run if this
+one fails.
 """
 import ctypes
 
@@ -33,7 +37,10 @@ def _weights(seed, K, N, std):
 
 
 def test_noalloc_matches_workspace_variant_on_two_calls(fp4):
-    cases = [(2048, 5504, 0.02, 0), (512, 264, 3.0, 1)]   # second call: larger values, fewer columns
+    from oracle import fp4_linear as orc
+    # first call: large values over 5504 columns; second: small values over the
+    # first 264 of the same columns (stale maxima would be larger than the new ones)
+    cases = [(2048, 5504, 3.0, 0), (512, 264, 0.02, 1)]
     for K, N, std, seed in cases:
         W = _weights(seed, K, N, std)
         ref_codes, ref_scales = fp4.fp4_quantize_cols(W)
@@ -46,6 +53,9 @@ def test_noalloc_matches_workspace_variant_on_two_calls(fp4):
         torch.cuda.synchronize()
         assert torch.equal(codes, ref_codes)
         assert torch.equal(scales.view(torch.int32), ref_scales.view(torch.int32))
+        o_codes, o_scales = orc.quantize_cols(W.float().cpu().numpy())
+        assert np.array_equal(codes.cpu().numpy(), o_codes)
+        assert np.array_equal(scales.cpu().numpy().view(np.uint32), o_scales.view(np.uint32))
     assert fp4.fp4_device_status() == ("FP4_OK", 0)
 
 
