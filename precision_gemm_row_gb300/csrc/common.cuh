@@ -213,6 +213,13 @@ __device__ __forceinline__ void fence_mbar_init_cluster() {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Relaxed arrive on an mbarrier of a CTA of the cluster: no release of this
+// thread's prior memory operations (for signals that order only tensor-memory
+// reads already completed by tcgen05.wait::ld, so outstanding global stores
+// are not waited for).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 // TMEM allocation for a CTA pair: one warp of each CTA executes it; both get the same columns.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols));
@@ -332,6 +339,16 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// (a, b) *= (x, y) as one packed fp32 multiply (each half rounded to nearest, as two fmul.rn).
+__device__ __forceinline__ void mul2_rn(float& a, float& b, float x, float y) {
+  uint64_t r;
+  const uint64_t ab = (uint64_t(__float_as_uint(b)) << 32) | __float_as_uint(a);
+  const uint64_t xy = (uint64_t(__float_as_uint(y)) << 32) | __float_as_uint(x);
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(ab), "l"(xy));
+  a = __uint_as_float(uint32_t(r));
+  b = __uint_as_float(uint32_t(r >> 32));
+}
 
 // Named barrier over `nthreads` threads (a multiple of 32) with id 1..15.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

@@ -38,6 +38,8 @@
 // then scales acc + P Q^T by 1/(s_A s_W), which equals acc/(s_A s_W) + dA W up to
 // fp32 rounding, and does no compensation work of its own.  Without a
 // workspace, or with more distinct columns, the epilogue forms the sum itself.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace fp4 {
@@ -300,6 +302,7 @@ struct FwdParams {
   const HotInfo* hot;   // null: no tensor-core compensation
   uint32_t* status;
   uint64_t wait_ns;
+  int fallback_only;    // run only when dA has more distinct columns than the tensor-core path takes
 };
 
 template <int BN, int NACC, bool PAIR>
@@ -309,6 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmPl, const __grid_constant__ CUtensorMap tmQh,
                    const __grid_constant__ CUtensorMap tmQl, const FwdParams p) {
   using C = FwdCfg<BN, NACC, PAIR>;
+  // as the fallback of the wide kernel: nothing to do unless dA has too many
+  // distinct columns for the tensor-core compensation (uniform over the grid)
+  if (p.fallback_only && !(p.hot->hc > kHotMax)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -513,9 +519,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this warp's column scales 1/s_W in its own shared-memory slice (no
       // cross-warp barrier, so a warp that gives up on a wait cannot strand others)
       __syncwarp();
-      for (int c = lane; c < EC; c += 32) {
-        const int col = nb * BN + c_base + c;
-        inv_sw_w[c] = (!raw && col < p.N) ? 1.0f / __ldg(p.s_w + col) : 1.0f;
+      {
+        // all of the lane's loads in flight at once, then the reciprocals
+        constexpr int kPer = (EC + 31) / 32;
+        float sw[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int c = lane + 32 * j, col = nb * BN + c_base + c;
+          sw[j] = (c < EC && !raw && col < p.N) ? __ldg(p.s_w + col) : 1.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+          if (lane + 32 * j < EC) inv_sw_w[lane + 32 * j] = 1.0f / sw[j];
       }
       __syncwarp();
       const int row = mrow0 + r_local;
@@ -672,6 +687,511 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Wide tiles: 256 x 480 per CTA pair.
+//
+// The tile's two column halves of 240 share every A stage: per K stage each CTA
+// loads its 128 rows of A (16 KB) and 120 rows of W^T for each half (2 x 15 KB),
+// and the leader issues one M = 256, N = 240 MMA per half.  Per SM that is
+// 46 KB per 960 clk of MMA work (48 B/clk), against 66 B/clk for 256 x 240
+// tiles, whose rate the L2 -> shared memory path could barely sustain.  The
+// accumulator takes all 480 TMEM columns (plus the 32 scale-factor columns),
+// so the next tile cannot start in a second buffer; instead each half has its
+// own full / empty barriers and, at a tile's ends, half 0 runs kWLag stages
+// ahead of half 1: the epilogue drains half 0 while the tensor core finishes
+// half 1, and drains half 1 while the tensor core starts the next tile's half 0.
+//
+// Work items (host-balanced, see wide_schedule): double tiles (two halves,
+// row blocks fastest), then single halves -- the last half of each row block
+// when the halves are odd in number, and the doubles of a partial last round
+// split in two, so that every pair ends within one half-tile of the others.
+// A half narrower than 240 columns (the right edge of W) runs an MMA of that
+// width, rounded up to 16; CTA r then loads its W^T rows from r x width / 2.
+constexpr int kWHalf = 240;          // columns per half (one MMA)
+constexpr int kWBRows = kWHalf / 2;  // W^T rows per CTA per half
+constexpr int kWStages = 4;
+constexpr int kWLag = 2;             // stages half 0 runs ahead of half 1 at a tile's ends
+constexpr int kWEpiWarps = 16;       // 4 per TMEM lane quadrant, each with a column group of each half
+constexpr int kWThreads = 64 + 32 * kWEpiWarps;
+
+struct WideCfg {
+  static constexpr int kAStage = kBM * kBKBytes;        // 16 KB
+  static constexpr int kBPart = kWBRows * kBKBytes;     // 15 KB
+  static constexpr int kBStage = 2 * kBPart;
+  static constexpr int kStageBytes = kAStage + kBStage;
+  static constexpr uint32_t kSfaCol = 2 * kWHalf;       // 480
+  static constexpr uint32_t kSfbCol = kSfaCol + 16;
+  static constexpr int kNumBars = 2 * kWStages + 4 + 1;
+  static constexpr int kBarBytes = 8 * kNumBars + 16;
+  static constexpr int kGroupCols = 64;                 // a warp's columns of a half: 64, 64, 64 and 48
+  static constexpr int kOutRowBytes = 32;               // staging: 16 BF16 or 8 fp32 columns a row
+  static constexpr int kOutBytes = 32 * kOutRowBytes;   // per warp
+  static constexpr int kInvSwBytes = kWEpiWarps * 2 * kGroupCols * 4;
+  static constexpr int kSmemBytes =
+      1024 + kWStages * kStageBytes + kWEpiWarps * kOutBytes + kBarBytes + kInvSwBytes;
+  static_assert(kSfbCol + 16 <= kTmemCols, "accumulator and scale factors exceed TMEM");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget exceeded");
+  static_assert(3 * kGroupCols < kWHalf && kWHalf - 3 * kGroupCols <= kGroupCols, "column groups");
+};
+
+struct WideSched {
+  int num_m;     // row blocks of 256
+  int num_nh;    // column halves of 240 (the last may be narrower)
+  int doubles;   // items [0, doubles): double tiles, row block fastest
+  int items;     // all items
+};
+
+// MMA width of a half whose first column is `rem` columns before the right edge.
+__host__ __device__ __forceinline__ int wide_half_width(int rem) {
+  return rem <= 0 ? 0 : (rem >= kWHalf ? kWHalf : (rem + 15) / 16 * 16);
+}
+
+__device__ __forceinline__ void wide_item(int i, const WideSched& s, int N, int& mb, int& n0, int& nh0, int& nh1) {
+  bool two = false;
+  if (i < s.doubles) {
+    mb = i % s.num_m;
+    n0 = (i / s.num_m) * (2 * kWHalf);
+    two = true;
+  } else {
+    int j = i - s.doubles;
+    const int odd = (s.num_nh & 1) ? s.num_m : 0;
+    if (j < odd) {                       // the last half of row block j
+      mb = j;
+      n0 = (s.num_nh - 1) * kWHalf;
+    } else {                             // one half of a split double
+      j -= odd;
+      const int d = s.doubles + (j >> 1);
+      mb = d % s.num_m;
+      n0 = (d / s.num_m) * (2 * kWHalf) + (j & 1) * kWHalf;
+    }
+  }
+  nh0 = wide_half_width(N - n0);
+  nh1 = two ? wide_half_width(N - n0 - kWHalf) : 0;
+}
+
+// Instruction descriptors with a run-time N (multiple of 16; M = 256).
+__device__ __forceinline__ uint32_t idesc_mxf4_pair_n(int n) {
+  return (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (1u << 23) | (uint32_t(256 >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t idesc_tf32_pair_n(int n) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(256 >> 4) << 24);
+}
+
+// The 4 MMAs of one half of one stage (K = 256 E2M1 values, or 32 TF32 values),
+// into accumulator columns 240 H .. : straight-line code, so that the single
+// issuing thread keeps the tensor pipe fed (a version with a per-MMA branch
+// between the kinds and a per-MMA accumulate flag ran at about 60 % of the
+// instruction rate).
+template <int H>
+__device__ __forceinline__ void wide_issue(uint32_t tmem, uint32_t a0, uint32_t b0, uint32_t idesc, uint32_t sfa,
+                                           uint32_t sfb, bool fp4, bool first) {
+  const uint32_t d = tmem + uint32_t(H * kWHalf);
+  const uint32_t bb = b0 + uint32_t(H * WideCfg::kBPart);
+  if (fp4) {
+    mma_mxf4_pair(d, smem_desc_sw128(a0, 16, 1024), smem_desc_sw128(bb, 16, 1024), idesc, sfa, sfb, first ? 0u : 1u);
+#pragma unroll
+    for (int k = 1; k < kBKBytes / kMmaKBytes; ++k)
+      mma_mxf4_pair(d, smem_desc_sw128(a0 + k * kMmaKBytes, 16, 1024), smem_desc_sw128(bb + k * kMmaKBytes, 16, 1024),
+                    idesc, sfa, sfb, 1u);
+  } else {
+#pragma unroll
+    for (int k = 0; k < kBKBytes / kMmaKBytes; ++k)
+      mma_tf32_pair(d, smem_desc_sw128(a0 + k * kMmaKBytes, 16, 1024), smem_desc_sw128(bb + k * kMmaKBytes, 16, 1024),
+                    idesc, 1u);
+  }
+}
+
+__global__ void __launch_bounds__(kWThreads, 1)
+    fp4_fwd_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmPh,
+                        const __grid_constant__ CUtensorMap tmPl, const __grid_constant__ CUtensorMap tmQh,
+                        const __grid_constant__ CUtensorMap tmQl, const FwdParams p, const WideSched sc) {
+  using C = WideCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kWStages * C::kAStage;
+  uint8_t* sOut = smem + kWStages * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + kWEpiWarps * C::kOutBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  float* inv_sw_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + C::kBarBytes);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kWStages;
+  const uint32_t accf0 = empty0 + 8 * kWStages;   // per half: accumulator half ready
+  const uint32_t acce0 = accf0 + 16;              // per half: accumulator half drained
+  const uint32_t done_bar = acce0 + 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (p.hot) {
+      prefetch_tmap(&tmPh);
+      prefetch_tmap(&tmPl);
+      prefetch_tmap(&tmQh);
+      prefetch_tmap(&tmQl);
+    }
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(accf0 + 8 * h, 1);
+      mbar_init(acce0 + 8 * h, 2 * kWEpiWarps);   // every epilogue warp of both CTAs
+    }
+    mbar_init(done_bar, 1);
+    fence_mbar_init_cluster();
+  }
+  if (warp == 1) tmem_alloc_for<true>(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  cta_sync<true>();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp >= 2 && warp < 6) {  // unit block scales: every scale byte = 0x7F (2^0)
+    const uint32_t lb = uint32_t((warp & 3) * 32) << 16;
+    tmem_st8_fill(tmem + lb + C::kSfaCol, 0x7F7F7F7Fu);
+    tmem_st8_fill(tmem + lb + C::kSfaCol + 8, 0x7F7F7F7Fu);
+    tmem_st8_fill(tmem + lb + C::kSfbCol, 0x7F7F7F7Fu);
+    tmem_st8_fill(tmem + lb + C::kSfbCol + 8, 0x7F7F7F7Fu);
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  cta_sync<true>();
+  tc_fence_after();
+
+  // with more distinct dA columns than the tensor-core path takes, the
+  // fallback kernel (launched after this one) does the whole product
+  const bool skip = p.rp != nullptr && p.hot != nullptr && p.hot->hc > kHotMax;
+  const bool hot = !skip && p.hot != nullptr && p.hot->mode != 0;
+  const int hot_stages = hot ? (p.hot->mode == 2 ? 1 : 3 * (p.hot->hp / kHotChunk)) : 0;
+  const int kblocks = (p.K / 2 + kBKBytes - 1) / kBKBytes;
+  const int nstages = kblocks + hot_stages;
+  const int items = skip ? 0 : sc.items;
+  const int pair_id = int(blockIdx.x) >> 1, npairs = int(gridDim.x) >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs)
+    int stage = 0;
+    uint32_t phase = 0, issued = 0;
+    bool ok = true;
+    for (int it = pair_id; it < items && ok; it += npairs) {
+      int mb, n0, nh0, nh1;
+      wide_item(it, sc, p.N, mb, n0, nh0, nh1);
+      const int arow = mb * (2 * kBM) + int(rank) * kBM;
+      const int b0row = n0 + int(rank) * (nh0 >> 1);
+      const int b1row = n0 + kWHalf + int(rank) * (nh1 >> 1);
+      const uint32_t bytes = 2u * uint32_t(C::kAStage + (nh0 ? C::kBPart : 0) + (nh1 ? C::kBPart : 0));
+      for (int kb = 0; kb < nstages; ++kb) {
+        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t fb = full0 + 8 * stage;
+          if (rank == 0) mbar_arrive_expect_tx(fb, bytes);
+          const uint32_t da = smem_u32(sA + stage * C::kAStage), db = smem_u32(sB + stage * C::kBStage);
+          if (kb < kblocks) {
+            tma_load_2d_to<true>(da, &tmA, fb, kb * kBKBytes, arow);
+            if (nh0) tma_load_2d_to<true>(db, &tmB, fb, kb * kBKBytes, b0row);
+            if (nh1) tma_load_2d_to<true>(db + C::kBPart, &tmB, fb, kb * kBKBytes, b1row);
+          } else {
+            // 32 columns of H: P part x Q part, pairs (hi, hi), (hi, lo), (lo, hi)
+            const int hs = kb - kblocks, chunk = hs / 3, pr = hs - 3 * chunk;
+            const int x = chunk * kHotChunk;
+            tma_load_2d_to<true>(da, pr == 2 ? &tmPl : &tmPh, fb, x, arow);
+            const CUtensorMap* q = pr == 1 ? &tmQl : &tmQh;
+            if (nh0) tma_load_2d_to<true>(db, q, fb, x, b0row);
+            if (nh1) tma_load_2d_to<true>(db + C::kBPart, q, fb, x, b1row);
+          }
+        }
+        __syncwarp();
+        ++issued;
+        if (++stage == kWStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    for (int s = 0; s < kWStages; ++s) {
+      const uint32_t n_s = issued / kWStages + (uint32_t(s) < issued % kWStages ? 1u : 0u);
+      if (n_s > 0 && !mbar_wait(empty0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
+        atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    }
+  } else if (warp == 1 && rank == 0) {
+    // ------------------------------------------------ MMA issuer (leader CTA)
+    int s0 = 0, s1 = 0;          // ring slot of the next half-0 and half-1 stage
+    uint32_t ph0 = 0;            // phase of the next half-0 stage's full barrier
+    uint32_t accph = 0;
+    bool ok = true;
+    const uint32_t sfa = tmem + C::kSfaCol, sfb = tmem + C::kSfbCol;
+    const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+    for (int it = pair_id; it < items && ok; it += npairs) {
+      int mb, n0, nh0, nh1;
+      wide_item(it, sc, p.N, mb, n0, nh0, nh1);
+      const uint32_t f0 = idesc_mxf4_pair_n(nh0), f1 = idesc_mxf4_pair_n(nh1);
+      const uint32_t t0 = idesc_tf32_pair_n(nh0), t1 = idesc_tf32_pair_n(nh1);
+      const int L = nstages < kWLag ? nstages : kWLag;
+      const int s_end = nstages - L > L ? nstages - L : L;
+      // stage kb of this tile: its full barrier (half 0 only), then lane 0 issues
+#define FP4_WIDE_FULL()                                   \
+  if (!mbar_wait(full0 + 8 * s0, ph0, p.wait_ns)) {       \
+    ok = false;                                           \
+    break;                                                \
+  }                                                       \
+  tc_fence_after();
+#define FP4_WIDE_ADV0()   \
+  if (++s0 == kWStages) { \
+    s0 = 0;               \
+    ph0 ^= 1u;            \
+  }
+#define FP4_WIDE_ADV1() \
+  if (++s1 == kWStages) s1 = 0;
+      if (!mbar_wait(acce0, accph ^ 1u, p.wait_ns)) {   // half 0 drained
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int kb = 0; kb < L; ++kb) {
+        FP4_WIDE_FULL()
+        if (lane == 0 && nh0)
+          wide_issue<0>(tmem, a_base + s0 * C::kAStage, b_base + s0 * C::kBStage, kb < kblocks ? f0 : t0, sfa, sfb,
+                        kb < kblocks, kb == 0);
+        __syncwarp();
+        FP4_WIDE_ADV0()
+      }
+      if (!ok) break;
+      if (!mbar_wait(acce0 + 8, accph ^ 1u, p.wait_ns)) {   // half 1 drained
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int kb = 0; kb < L; ++kb) {
+        if (lane == 0) {
+          if (nh1)
+            wide_issue<1>(tmem, a_base + s1 * C::kAStage, b_base + s1 * C::kBStage, kb < kblocks ? f1 : t1, sfa, sfb,
+                          kb < kblocks, kb == 0);
+          commit_to<true>(empty0 + 8 * s1, 0x3);   // the stage is free in both CTAs
+        }
+        __syncwarp();
+        FP4_WIDE_ADV1()
+      }
+      for (int kb = L; kb < s_end; ++kb) {   // both halves of a stage back to back
+        FP4_WIDE_FULL()
+        if (lane == 0) {
+          const uint32_t a0 = a_base + s0 * C::kAStage, b0 = b_base + s0 * C::kBStage;
+          const bool fp4s = kb < kblocks;
+          if (nh0) wide_issue<0>(tmem, a0, b0, fp4s ? f0 : t0, sfa, sfb, fp4s, false);
+          if (nh1) wide_issue<1>(tmem, a0, b0, fp4s ? f1 : t1, sfa, sfb, fp4s, false);
+          commit_to<true>(empty0 + 8 * s0, 0x3);
+        }
+        __syncwarp();
+        FP4_WIDE_ADV0()
+        FP4_WIDE_ADV1()
+      }
+      if (!ok) break;
+      for (int kb = s_end; kb < nstages; ++kb) {   // half 0 finishes first
+        FP4_WIDE_FULL()
+        if (lane == 0 && nh0)
+          wide_issue<0>(tmem, a_base + s0 * C::kAStage, b_base + s0 * C::kBStage, kb < kblocks ? f0 : t0, sfa, sfb,
+                        kb < kblocks, kb == 0);
+        __syncwarp();
+        FP4_WIDE_ADV0()
+      }
+      if (!ok) break;
+      if (lane == 0) commit_to<true>(accf0, 0x3);        // half 0 of the accumulator is ready
+      __syncwarp();
+      for (int kb = s_end; kb < nstages; ++kb) {
+        if (lane == 0) {
+          if (nh1)
+            wide_issue<1>(tmem, a_base + s1 * C::kAStage, b_base + s1 * C::kBStage, kb < kblocks ? f1 : t1, sfa, sfb,
+                          kb < kblocks, kb == 0);
+          commit_to<true>(empty0 + 8 * s1, 0x3);
+        }
+        __syncwarp();
+        FP4_WIDE_ADV1()
+      }
+      if (lane == 0) commit_to<true>(accf0 + 8, 0x3);    // half 1 is ready
+      __syncwarp();
+      accph ^= 1u;
+#undef FP4_WIDE_FULL
+#undef FP4_WIDE_ADV0
+#undef FP4_WIDE_ADV1
+    }
+    if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    if (lane == 0) commit_to<true>(done_bar, 0x1);
+    __syncwarp();
+    if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+  } else if (warp >= 2) {
+    // ------------------------------------------------ epilogue (both CTAs, own 128 rows)
+    // 16 warps; warp w owns TMEM lanes 32 (w % 4) .. +31 (one output row per
+    // thread) and column group (w - 2) / 4 of each half: columns 64 g .. of the
+    // half, 64 wide (48 for the last).  Per half, for BF16 output: read the
+    // group's columns, scale and round them into at most 32 packed registers,
+    // release the half, then store.  TMEM is held for the arithmetic alone, about
+    // 16 x 64 values a thread-warp, which the tensor core's other half covers.
+    constexpr int GC = C::kGroupCols;
+    const int e = warp - 2;
+    const int g = e >> 2, q = warp & 3;
+    const int gw = g < 3 ? GC : kWHalf - 3 * GC;   // this warp's columns of a half
+    float* inv_sw_w = inv_sw_s + e * 2 * GC;
+    uint8_t* out_s = sOut + e * C::kOutBytes;
+    uint8_t* orow = out_s + lane * C::kOutRowBytes;
+    const uint32_t lane_base = uint32_t(q * 32) << 16;
+    const bool raw = (p.y_type == FP4_OUT_RAW_ACC_FP32);
+    const bool bf16_out = (p.y_type == FP4_OUT_BF16);
+    uint32_t accph = 0;
+    bool ok = true;
+    for (int it = pair_id; it < items && ok; it += npairs) {
+      int mb, n0, nh0, nh1;
+      wide_item(it, sc, p.N, mb, n0, nh0, nh1);
+      const int row0 = mb * (2 * kBM) + int(rank) * kBM + q * 32;
+      const int row = row0 + lane;
+      // the row's scale and this warp's column scales of both halves, all loads
+      // in flight at once, before the first wait
+      float sw[4];
+      const float sa = (row < p.M && !raw) ? __ldg(p.s_a + row) : 1.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {   // column c = lane + 32 j of [half 0 group | half 1 group]
+        const int c = lane + 32 * j, h = c >= GC, cc = c - h * GC;
+        const int col = n0 + h * kWHalf + g * GC + cc;
+        sw[j] = (cc < gw && !raw && col < p.N) ? __ldg(p.s_w + col) : 1.0f;
+      }
+      const float inv_sa = 1.0f / sa;
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) inv_sw_w[lane + 32 * j] = 1.0f / sw[j];
+      __syncwarp();
+      int ncols[2], col_base[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int nhh = h ? nh1 : nh0;
+        ncols[h] = nhh - g * GC < 0 ? 0 : (nhh - g * GC > gw ? gw : nhh - g * GC);   // multiple of 16
+        col_base[h] = n0 + h * kWHalf + g * GC;
+      }
+      if (bf16_out) {
+        // both halves into registers, each released as soon as it is read; the
+        // stores follow (a store burst between the halves would delay half 1,
+        // while after both they overlap the next tile's main loop)
+        uint32_t pk[2][GC / 2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(accf0 + 8 * h, accph, p.wait_ns))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tcol = uint32_t(h * kWHalf + g * GC);
+#pragma unroll
+          for (int c0 = 0; c0 < GC; c0 += 16) {
+            if (c0 < ncols[h]) {   // warp-uniform
+              uint32_t r[16];
+              tmem_ld8(tmem + lane_base + tcol + c0, *reinterpret_cast<uint32_t(*)[8]>(r));
+              tmem_ld8(tmem + lane_base + tcol + c0 + 8, *reinterpret_cast<uint32_t(*)[8]>(r + 8));
+              tmem_wait_ld();
+#pragma unroll
+              for (int t = 0; t < 8; ++t) {
+                float y0 = __uint_as_float(r[2 * t]), y1 = __uint_as_float(r[2 * t + 1]);
+                mul2_rn(y0, y1, inv_sa, inv_sa);
+                const float2 w = *reinterpret_cast<const float2*>(inv_sw_w + h * GC + c0 + 2 * t);
+                mul2_rn(y0, y1, w.x, w.y);
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
+                pk[h][c0 / 2 + t] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+            }
+          }
+          // the half may be overwritten: its TMEM reads completed at tcgen05.wait::ld
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(acce0 + 8 * h, 0));
+        }
+        if (!ok) break;
+        // stores, 16 columns at a time through the warp's staging rows: each lane
+        // writes its row (32 bytes), then the warp stores the block row-major in
+        // 16-byte pieces, two lanes to a row
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int c0 = 0; c0 < GC; c0 += 16) {
+            if (c0 < ncols[h]) {
+              __syncwarp();
+              *reinterpret_cast<uint4*>(orow) =
+                  make_uint4(pk[h][c0 / 2], pk[h][c0 / 2 + 1], pk[h][c0 / 2 + 2], pk[h][c0 / 2 + 3]);
+              *reinterpret_cast<uint4*>(orow + 16) =
+                  make_uint4(pk[h][c0 / 2 + 4], pk[h][c0 / 2 + 5], pk[h][c0 / 2 + 6], pk[h][c0 / 2 + 7]);
+              __syncwarp();
+#pragma unroll
+              for (int rr = 0; rr < 2; ++rr) {   // 64 pieces: piece i is row i / 2, bytes 16 (i % 2) ..
+                const int i = lane + 32 * rr;
+                const int grow = row0 + (i >> 1), gcol = col_base[h] + c0 + 8 * (i & 1);
+                const uint4 v = *reinterpret_cast<const uint4*>(out_s + 16 * i);
+                if (grow < p.M && gcol < p.N)
+                  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.Y) + int64_t(grow) * p.ldy + gcol) = v;
+              }
+            }
+          }
+        }
+      } else {
+        // fp32 or the raw accumulator: 8 columns (32 bytes a row) at a time,
+        // stored while the half is held
+        for (int h = 0; h < 2; ++h) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait(accf0 + 8 * h, accph, p.wait_ns))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tcol = uint32_t(h * kWHalf + g * GC);
+          for (int c0 = 0; c0 < ncols[h]; c0 += 8) {   // warp-uniform
+            uint32_t r[8];
+            tmem_ld8(tmem + lane_base + tcol + c0, r);
+            tmem_wait_ld();
+            float y[8];
+#pragma unroll
+            for (int t = 0; t < 8; t += 2) {
+              y[t] = __uint_as_float(r[t]);
+              y[t + 1] = __uint_as_float(r[t + 1]);
+              if (!raw) {
+                mul2_rn(y[t], y[t + 1], inv_sa, inv_sa);
+                const float2 w = *reinterpret_cast<const float2*>(inv_sw_w + h * GC + c0 + t);
+                mul2_rn(y[t], y[t + 1], w.x, w.y);
+              }
+            }
+            __syncwarp();
+            *reinterpret_cast<float4*>(orow) = make_float4(y[0], y[1], y[2], y[3]);
+            *reinterpret_cast<float4*>(orow + 16) = make_float4(y[4], y[5], y[6], y[7]);
+            __syncwarp();
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const int i = lane + 32 * rr;
+              const int grow = row0 + (i >> 1), gcol = col_base[h] + c0 + 4 * (i & 1);
+              const uint4 v = *reinterpret_cast<const uint4*>(out_s + 16 * i);
+              if (grow < p.M && gcol < p.N)
+                *reinterpret_cast<uint4*>(static_cast<float*>(p.Y) + int64_t(grow) * p.ldy + gcol) = v;
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(acce0 + 8 * h, 0));
+        }
+        if (!ok) break;
+      }
+      accph ^= 1u;
+    }
+    if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+  }
+
+  // neither CTA leaves or frees TMEM while its partner may still signal it
+  __syncwarp();
+  tc_fence_before();
+  cta_sync<true>();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_for<true>(tmem, kTmemCols);
+  }
+}
+
 constexpr int kFwdBN = 240;
 constexpr int kFwdAcc = 2;
 
@@ -774,6 +1294,91 @@ fp4_status launch_fwd(const CUtensorMap& tmA, const CUtensorMap& tmY, const uint
 }  // namespace
 }  // namespace fp4
 
+
+namespace fp4 {
+namespace {
+// Half-tiles of the busiest pair when items [0, doubles) are double tiles and
+// [doubles, doubles + singles) single halves, dealt round robin to `pairs`.
+int64_t wide_makespan(int64_t doubles, int64_t singles, int64_t pairs) {
+  int64_t worst = 0;
+  for (int64_t p = 0; p < pairs && p < doubles + singles; ++p) {
+    const int64_t nd = p < doubles ? (doubles - 1 - p) / pairs + 1 : 0;
+    // items i in [doubles, doubles + singles) with i = p (mod pairs)
+    const int64_t first = doubles + ((p - doubles) % pairs + pairs) % pairs;
+    const int64_t ns = first < doubles + singles ? (doubles + singles - 1 - first) / pairs + 1 : 0;
+    worst = std::max(worst, 2 * nd + ns);
+  }
+  return worst;
+}
+
+// Work list of the wide kernel: all double tiles, or the last partial round of
+// them split into single halves when that shortens the busiest pair's list.
+WideSched wide_schedule(int64_t M, int64_t N, int64_t pairs) {
+  WideSched s;
+  s.num_m = int((M + 2 * kBM - 1) / (2 * kBM));
+  s.num_nh = int((N + kWHalf - 1) / kWHalf);
+  const int64_t d0 = int64_t(s.num_m) * (s.num_nh / 2);
+  const int64_t s0 = (s.num_nh & 1) ? s.num_m : 0;
+  const int64_t r = d0 % pairs;
+  int64_t split = 0;
+  if (r && wide_makespan(d0 - r, s0 + 2 * r, pairs) < wide_makespan(d0, s0, pairs)) split = r;
+  s.doubles = int(d0 - split);
+  s.items = int(d0 - split + s0 + 2 * split);
+  return s;
+}
+
+fp4_status launch_fwd_wide(const CUtensorMap& tmA, const uint8_t* w_codes_t,
+                           int64_t ldw_codes_bytes, const float* q_hi, const float* q_lo, const float* p_hi,
+                           const float* p_lo, FwdParams p, int sms, cudaStream_t cs) {
+  using C = WideCfg;
+  fp4_status st;
+  CUtensorMap tmB, tmPh = tmA, tmPl = tmA, tmQh = tmA, tmQl = tmA;   // compensation maps unused without p.hot
+  if ((st = encode_tmap_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_codes_t, uint64_t(p.K / 2), uint64_t(p.N),
+                           uint64_t(ldw_codes_bytes), kBKBytes, kWBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK)
+    return st;
+  if (p.hot) {
+    const uint32_t row_bytes = kHotMax * 4;
+    if ((st = encode_tmap_2d(&tmPh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p_hi, kHotMax, uint64_t(p.M), row_bytes,
+                             kHotChunk, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
+        (st = encode_tmap_2d(&tmPl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p_lo, kHotMax, uint64_t(p.M), row_bytes,
+                             kHotChunk, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
+        (st = encode_tmap_2d(&tmQh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q_hi, kHotMax, uint64_t(p.N), row_bytes,
+                             kHotChunk, kWBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK ||
+        (st = encode_tmap_2d(&tmQl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q_lo, kHotMax, uint64_t(p.N), row_bytes,
+                             kHotChunk, kWBRows, CU_TENSOR_MAP_SWIZZLE_128B)) != FP4_OK)
+      return st;
+  }
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(fp4_fwd_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+      return FP4_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  const int64_t pairs = sms / 2;
+  const WideSched sc = wide_schedule(p.M, p.N, pairs);
+  const int grid = int(2 * (sc.items < pairs ? sc.items : pairs));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kWThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = cs;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, fp4_fwd_wide_kernel, tmA, tmB, tmPh, tmPl, tmQh, tmQl, p, sc) != cudaSuccess)
+    return launch_status();
+  return launch_status();
+}
+}  // namespace
+}  // namespace fp4
+
 FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_bytes, const float* s_a,
                                   const uint8_t* w_codes_t, int64_t ldw_codes_bytes, const float* s_w, int64_t M,
                                   int64_t N, int64_t K, const int32_t* dA_row_ptr, const int32_t* dA_col,
@@ -862,6 +1467,20 @@ FP4_API fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_byte
   p.hot = hot_info;
   p.status = status_word();
   p.wait_ns = kWaitLimitNs;
+  p.fallback_only = 0;
+  // K >= 4096, without compensation or with it on the tensor cores: the wide
+  // kernel (256 x 480 pair tiles; below 16 K stages a tile is too short to
+  // hide the drain of its single accumulator, and the double-buffered 240-wide
+  // kernel is faster).  The tensor-core path is decided on the device (the
+  // distinct dA columns are counted there), so with a workspace the 240-wide
+  // kernel follows as a fallback that does the product only when dA has more
+  // than kHotMax distinct columns (the wide kernel then does nothing), forming
+  // the compensation on its CUDA cores; otherwise that kernel does it all.
+  if (K >= 4096 && (!comp || use_hot)) {
+    st = launch_fwd_wide(tmA, w_codes_t, ldw_codes_bytes, q_hi, q_lo, p_hi, p_lo, p, sms, cs);
+    if (st != FP4_OK || !comp) return st;
+    p.fallback_only = 1;
+  }
   // CTA pairs once the K loop is long enough (16 FP4 stages, K >= 4096) for the
   // pair's lighter stages to outweigh its shared accumulator hand-off
   if (K >= 4096) return launch_fwd<true>(tmA, tmY, w_codes_t, ldw_codes_bytes, q_hi, q_lo, p_hi, p_lo, p, sms, cs);

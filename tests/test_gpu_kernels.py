@@ -577,3 +577,36 @@ def test_binding_rejects_undersized_or_mistyped_buffers(fp4):
         fp4.fp4_linear_fwd(a_codes, s_a[: M - 1], codes, s_w, K)
     torch.cuda.synchronize()
     assert_no_device_flags(fp4)
+
+
+# ---------------------------------------------------------------- wide pair tiles (K >= 4096)
+
+@pytest.mark.parametrize("M,N,K", [(37, 8, 4096), (300, 240, 4096), (256, 480, 5120), (129, 1000, 4096),
+                                   (1000, 5120, 4096), (8192, 4800, 4096), (512, 13824, 4096)])
+def test_wide_gemm_raw_and_scaled(fp4, M, N, K):
+    """The 256 x 480 pair-tile kernel that runs K >= 4096: a half narrower than 240
+    (N = 8, 1000, 13824), a single half (N = 240), odd numbers of halves, partial
+    pair rows (M = 37, 129, 1000), and a schedule that splits the last round of
+    double tiles into single halves (M = 8192, N = 4800: 320 doubles on 76 pairs).
+    The raw accumulator is checked against the oracle on small shapes and in full
+    against torch._int_mm; BF16 output without compensation within 1 ulp."""
+    from tests.gpu_common import assert_raw_acc_equals_int_mm
+    a = _random_codes(M * 3 + N, M, K)
+    w = _random_codes(N * 5 + K, N, K)
+    da, dw = torch.from_numpy(a).cuda(), torch.from_numpy(w).cuda()
+    raw = fp4.fp4_linear_fwd(da, None, dw, None, K, out_type="raw")
+    assert_raw_acc_equals_int_mm(raw, da, dw)
+    rows = np.unique(np.concatenate([np.arange(min(M, 3)), np.random.default_rng(M).choice(M, min(M, 24), replace=False),
+                                     [M - 1]]))
+    ref = orc.gemm_raw(a, w, rows=rows).astype(np.float32)
+    got = raw[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    rng = np.random.default_rng(K + N)
+    s_a = (rng.uniform(0.05, 4.0, M)).astype(np.float32)
+    s_w = (rng.uniform(0.05, 4.0, N)).astype(np.float32)
+    yb = fp4.fp4_linear_fwd(da, torch.from_numpy(s_a).cuda(), dw, torch.from_numpy(s_w).cuda(), K, out_type="bf16")
+    y_ref = orc.linear_fwd(a, s_a, w, s_w, rows=rows)
+    assert bf16_ulp_distance(host_bits(yb[torch.from_numpy(rows).cuda()]), orc.f64_to_bf16(y_ref)).max() <= BF16_ULP_TOL
+    yf = fp4.fp4_linear_fwd(da, torch.from_numpy(s_a).cuda(), dw, torch.from_numpy(s_w).cuda(), K, out_type="fp32")
+    np.testing.assert_allclose(yf[torch.from_numpy(rows).cuda()].cpu().numpy(), y_ref, rtol=2.0 ** -21, atol=0)
+    assert_no_device_flags(fp4)
