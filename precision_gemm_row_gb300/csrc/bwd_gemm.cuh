@@ -212,7 +212,7 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
       const int bcol = nb * kBN + int(rank) * C::kBCols;       // this CTA's rows of Q
       const int lb_end = w.c1 * kChunkStages < lblocks ? w.c1 * kChunkStages : lblocks;
       for (int lb = w.c0 * kChunkStages; lb < lb_end; ++lb) {
-        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
+        if (!mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -249,7 +249,7 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
     // have landed and no commit is still on its way) before the CTA may exit
     for (int s = 0; s < kStages; ++s) {
       const uint32_t n_s = issued / kStages + (uint32_t(s) < issued % kStages ? 1u : 0u);
-      if (n_s > 0 && !mbar_wait(empty0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
+      if (n_s > 0 && !mbar_wait_warp(empty0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
         atomicOr(p.status, FP4_FLAG_TIMEOUT);
     }
   } else if (warp == 1 && rank == 0) {
@@ -265,14 +265,14 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
       for (int ch = w.c0; ch < w.c1 && ok; ++ch) {
         const int lb0 = ch * kChunkStages;
         const int lb1 = lb0 + kChunkStages < lblocks ? lb0 + kChunkStages : lblocks;
-        if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
+        if (!mbar_wait_warp(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + uint32_t(acc * kBN);
         for (int lb = lb0; lb < lb1; ++lb) {
-          if (!mbar_wait(full0 + 8 * stage, phase, p.wait_ns)) {
+          if (!mbar_wait_warp(full0 + 8 * stage, phase, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -312,7 +312,7 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
     if (lane == 0) commit_to<PAIR>(done_bar, 0x1);
     __syncwarp();
-    if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    if (!mbar_wait_warp(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   } else if (warp >= 2) {
     // ------------------------------------------------ chunk promotion + epilogue (own 128 rows)
     const int ew = warp - 2;

@@ -83,6 +83,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// mbar_wait by every lane of a warp, with one verdict for the whole warp (a lane
+// that gave up at the limit while another saw the phase complete would otherwise
+// leave the warp divergent before its next warp-wide operation).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity, limit_ns));
+}
+
 // 2-D tiled TMA load global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
                                             int32_t c1) {
@@ -428,6 +435,20 @@ __device__ __forceinline__ uint32_t clamp_pair(uint32_t w, uint32_t tb2) {
 // Two E2M1 codes (one byte) of the fp32 products x * s of a BF16 pair.
 __device__ __forceinline__ uint32_t quantize_pair(uint32_t w, float s) {
   return e2m1x2_encode(__fmul_rn(__uint_as_float(w << 16), s), __fmul_rn(__uint_as_float(w & 0xFFFF0000u), s));
+}
+
+// Eight codes of a 16-byte chunk of BF16 values (no clamp), the products x * s
+// formed two at a time by the packed fp32 multiply (each rounded as fmul.rn).
+__device__ __forceinline__ uint32_t quantize8_packed(const uint4 v, float s) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+    mul2_rn(lo, hi, s, s);
+    out |= e2m1x2_encode(lo, hi) << (8 * i);
+  }
+  return out;
 }
 
 // Eight codes of a 16-byte chunk of BF16 values, element 0 in the lowest nibble;

@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int arow = mb * kTileM + int(rank) * kBM;           // this CTA's 128 rows of A
       const int brow = nb * BN + int(rank) * C::kBRows;         // this CTA's part of the tile's B rows
       for (int kb = 0; kb < nstages; ++kb) {
-        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
+        if (!mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // loads have landed and no commit is still on its way) before the CTA may exit
     for (int s = 0; s < C::kStages; ++s) {
       const uint32_t n_s = issued / C::kStages + (uint32_t(s) < issued % C::kStages ? 1u : 0u);
-      if (n_s > 0 && !mbar_wait(empty0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
+      if (n_s > 0 && !mbar_wait_warp(empty0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
         atomicOr(p.status, FP4_FLAG_TIMEOUT);
     }
   } else if (warp == 1 && rank == 0) {
@@ -447,14 +447,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sfa = tmem + C::kSfaCol, sfb = tmem + C::kSfbCol;
     const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
     for (int tile = pair_id; tile < tiles && ok; tile += npairs) {
-      if (!mbar_wait(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
+      if (!mbar_wait_warp(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem + uint32_t(acc * BN);
       for (int kb = 0; kb < nstages; ++kb) {
-        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_ns)) {
+        if (!mbar_wait_warp(full0 + 8 * stage, phase, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every MMA issued by this thread must finish before TMEM is released
     if (lane == 0) commit_to<PAIR>(done_bar, 0x1);
     __syncwarp();
-    if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    if (!mbar_wait_warp(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue (both CTAs, own 128 rows)
     constexpr int EC = C::kEpiCols;
@@ -884,7 +884,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       const int b1row = n0 + kWHalf + int(rank) * (nh1 >> 1);
       const uint32_t bytes = 2u * uint32_t(C::kAStage + (nh0 ? C::kBPart : 0) + (nh1 ? C::kBPart : 0));
       for (int kb = 0; kb < nstages; ++kb) {
-        if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
+        if (!mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -917,7 +917,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
     for (int s = 0; s < kWStages; ++s) {
       const uint32_t n_s = issued / kWStages + (uint32_t(s) < issued % kWStages ? 1u : 0u);
-      if (n_s > 0 && !mbar_wait(empty0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
+      if (n_s > 0 && !mbar_wait_warp(empty0 + 8 * s, (n_s - 1) & 1u, p.wait_ns) && lane == 0)
         atomicOr(p.status, FP4_FLAG_TIMEOUT);
     }
   } else if (warp == 1 && rank == 0) {
@@ -937,7 +937,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       const int s_end = nstages - L > L ? nstages - L : L;
       // stage kb of this tile: its full barrier (half 0 only), then lane 0 issues
 #define FP4_WIDE_FULL()                                   \
-  if (!mbar_wait(full0 + 8 * s0, ph0, p.wait_ns)) {       \
+  if (!mbar_wait_warp(full0 + 8 * s0, ph0, p.wait_ns)) {  \
     ok = false;                                           \
     break;                                                \
   }                                                       \
@@ -949,7 +949,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   }
 #define FP4_WIDE_ADV1() \
   if (++s1 == kWStages) s1 = 0;
-      if (!mbar_wait(acce0, accph ^ 1u, p.wait_ns)) {   // half 0 drained
+      if (!mbar_wait_warp(acce0, accph ^ 1u, p.wait_ns)) {   // half 0 drained
         ok = false;
         break;
       }
@@ -963,7 +963,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         FP4_WIDE_ADV0()
       }
       if (!ok) break;
-      if (!mbar_wait(acce0 + 8, accph ^ 1u, p.wait_ns)) {   // half 1 drained
+      if (!mbar_wait_warp(acce0 + 8, accph ^ 1u, p.wait_ns)) {   // half 1 drained
         ok = false;
         break;
       }
@@ -1023,7 +1023,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if (!ok && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
     if (lane == 0) commit_to<true>(done_bar, 0x1);
     __syncwarp();
-    if (!mbar_wait(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    if (!mbar_wait_warp(done_bar, 0, p.wait_ns) && lane == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
   } else if (warp >= 2) {
     // ------------------------------------------------ epilogue (both CTAs, own 128 rows)
     // 16 warps; warp w owns TMEM lanes 32 (w % 4) .. +31 (one output row per

@@ -4,20 +4,14 @@
 // threshold (A_clamped), and dA = A - A_clamped is kept as a sparse matrix that
 // is nonzero only where clamping happened.
 //
-// Kernels (all HBM-bound, no spin-waits):
-//  1. histogram_select: one 32768-bin histogram of the 15-bit BF16 magnitude
-//     pattern per CTA in shared memory, merged into a global histogram; the
-//     last CTA to finish (atomic ticket) scans it for the exact k-th order
-//     statistic t.
-//  2. rows_outlier: one row per warp (or several warps for long rows), held in
-//     registers: counts |A| > t per 16-byte chunk and writes the row's count
-//     and its first kRowSlots entries (column, A - sign(A) t), in column order,
-//     into fixed per-row slots (no atomics); optionally writes A_clamped, and
-//     in the fused variant also the row's E2M1 codes and scale (the clamp
-//     applied), so A is read once here.
-//  3. row_scan: scan of the per-row counts -> row_ptr (one CTA, coalesced tiles).
-//  4. gather: copies every row's slots to its CSR position; a row with more
-//     than kRowSlots entries is read again from A and emitted in full.
+// One cooperative kernel does it all (rowcall_kernel, below; HBM-bound): a
+// pilot histogram of every 64th row gives a floor under the threshold, a full
+// pass histograms only the magnitudes above the floor (a second pass fills in
+// the rest when the pilot misleads), every CTA selects the exact k-th order
+// statistic t, a row pass writes the row codes / scales, A_clamped on request
+// and each row's first kRowSlots entries (column, A - sign(A) t) into per-row
+// slots, and row_ptr and the CSR follow from per-CTA totals.  Its three or four
+// grid barriers are bounded waits.
 #include <cmath>
 
 #include "common.cuh"
@@ -26,27 +20,32 @@ namespace fp4 {
 namespace {
 
 constexpr int kBins = 32768;
-constexpr int kHistThreads = 1024;
 
-constexpr int kRowSlots = 16;  // entries per row kept by the row pass (more are re-read from A)
+constexpr int kRowSlots = 32;  // entries per row kept by the row pass (more are re-read from A)
 
 struct Ctrl {
-  uint32_t done;          // CTAs finished with the histogram
+  uint32_t unused;
   uint32_t t_bits;        // 15-bit magnitude pattern of t
   unsigned long long nnz_expect; // number of |A| > t from the histogram
 };
 
 struct WsLayout {
-  size_t hist, ctrl, cnt, scol, sval, total;
+  size_t hist, hist2, ctrl, fctrl, cta_total, cnt, scol, sval, total;
 };
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+constexpr int kMaxCtas = 1024;   // CTA totals of the fused row call (one CTA per SM)
+
+// The histograms and both control blocks come first: one memset clears them.
 WsLayout ws_layout(int64_t M) {
   WsLayout L;
   size_t off = 0;
   L.hist = off; off += round256(size_t(kBins) * 4);
+  L.hist2 = off; off += round256(size_t(kBins) * 4);
   L.ctrl = off; off += round256(sizeof(Ctrl));
+  L.fctrl = off; off += 256;
+  L.cta_total = off; off += round256(size_t(kMaxCtas) * 8);
   L.cnt = off; off += round256(size_t(M) * 4);
   L.scol = off; off += round256(size_t(M) * kRowSlots * 4);
   L.sval = off; off += round256(size_t(M) * kRowSlots * 4);
@@ -54,116 +53,6 @@ WsLayout ws_layout(int64_t M) {
   return L;
 }
 
-__global__ void __launch_bounds__(kHistThreads, 1)
-    histogram_select_kernel(const uint16_t* __restrict__ A, int64_t M, int K, int64_t lda, int64_t k_rank,
-                            uint32_t* __restrict__ ghist, Ctrl* __restrict__ ctrl, float* __restrict__ t_out) {
-  extern __shared__ uint32_t hist[];  // kBins counters
-  __shared__ uint32_t part[kHistThreads];
-  __shared__ int is_last;
-  for (int b = threadIdx.x; b < kBins; b += kHistThreads) hist[b] = 0;
-  __syncthreads();
-
-  const int cpr = K >> 3;  // 16-byte chunks per row
-  const int64_t total = M * cpr;
-  const bool dense = (lda == K);
-  const int64_t stride = int64_t(gridDim.x) * kHistThreads;
-  constexpr int kU = 8;  // loads in flight per thread
-  for (int64_t g0 = int64_t(blockIdx.x) * kHistThreads + threadIdx.x; g0 < total; g0 += stride * kU) {
-    uint4 v[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int64_t g = g0 + u * stride;
-      if (g < total) {
-        const uint4* p;
-        if (dense) {
-          p = reinterpret_cast<const uint4*>(A) + g;
-        } else {
-          const int64_t r = g / cpr;
-          p = reinterpret_cast<const uint4*>(A + r * lda) + (g - r * cpr);
-        }
-        v[u] = __ldcs(p);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (g0 + u * stride < total) {
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          atomicAdd(&hist[w[i] & 0x7FFFu], 1u);
-          atomicAdd(&hist[(w[i] >> 16) & 0x7FFFu], 1u);
-        }
-      }
-    }
-  }
-  __syncthreads();
-  for (int b = threadIdx.x; b < kBins; b += kHistThreads) {
-    const uint32_t c = hist[b];
-    if (c) atomicAdd(ghist + b, c);
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = (atomicAdd(&ctrl->done, 1u) == gridDim.x - 1);
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-
-  // Exact order statistic: the smallest bin b with cumulative count >= k_rank.
-  // The merged histogram comes into this CTA's shared memory with coalesced
-  // 16-byte loads; thread t then owns bins 32 t .. 32 t + 31 (summed in a
-  // lane-skewed order, so a warp's 32 reads fall in 32 different banks).
-  constexpr int kPer = kBins / kHistThreads;  // 32 bins per thread
-#pragma unroll
-  for (int j = 0; j < kBins / 4 / kHistThreads; ++j) {
-    const int i4 = threadIdx.x + j * kHistThreads;
-    reinterpret_cast<uint4*>(hist)[i4] = __ldcg(reinterpret_cast<const uint4*>(ghist) + i4);
-  }
-  __syncthreads();
-  const int b0 = threadIdx.x * kPer;
-  uint32_t sum = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) sum += hist[b0 + ((i + threadIdx.x) & (kPer - 1))];
-  // inclusive scan of the 1024 partial sums: within each warp by shuffles, then
-  // over the 32 warp totals (counts fit 32 bits: n < 2^32)
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  uint32_t x = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) part[wid] = x;
-  __syncthreads();
-  if (wid == 0) {
-    uint32_t wv = part[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, wv, o);
-      if (lane >= o) wv += y;
-    }
-    part[lane] = wv;
-  }
-  __syncthreads();
-  const uint64_t incl = uint64_t(x) + (wid ? part[wid - 1] : 0u);
-  const uint64_t excl = incl - sum;
-  if (excl < uint64_t(k_rank) && uint64_t(k_rank) <= incl) {
-    uint64_t run = excl;
-    int sel = b0 + kPer - 1;
-    for (int i = 0; i < kPer; ++i) {
-      run += hist[b0 + i];
-      if (run >= uint64_t(k_rank)) {
-        sel = b0 + i;
-        break;
-      }
-    }
-    const uint64_t n = uint64_t(M) * uint64_t(K);
-    ctrl->t_bits = uint32_t(sel);
-    ctrl->nnz_expect = n - run;
-    *t_out = bf16_bits_to_float(uint32_t(sel));
-  }
-}
-
-constexpr int kMaxRowWarps = 16;   // warps per CTA of the row pass
 
 // 8-bit mask of the elements of a 16-byte BF16 chunk whose magnitude pattern exceeds tb.
 __device__ __forceinline__ uint32_t outlier_mask8(const uint4 v, uint32_t tb) {
@@ -177,236 +66,530 @@ __device__ __forceinline__ uint32_t outlier_mask8(const uint4 v, uint32_t tb) {
   return m;
 }
 
-// Each row is handled by `wpr` warps; lane l of warp w holds the row's 16-byte
-// chunks ci = l + 32 (w + wpr c), c < CH, in registers.  Column order of the
-// entries is chunk-slot c first, then warp, then lane, which is what the
-// offsets below follow.  A CTA holds blockDim.x / 32 / wpr rows.
-template <int CH, bool CODES>
-__global__ void __launch_bounds__(512, 1) rows_outlier_kernel(
-    const uint16_t* __restrict__ A, int64_t M, int K, int64_t lda, Ctrl* ctrl, const float* __restrict__ t_ptr,
-    int32_t* __restrict__ row_cnt, int32_t* __restrict__ scol, float* __restrict__ sval, uint16_t* __restrict__ A_c,
-    int64_t ldac, uint8_t* __restrict__ codes, int64_t ldc, float* __restrict__ scales, int wpr) {
-  __shared__ uint32_t red[kMaxRowWarps];
-  __shared__ uint32_t tcnt[kMaxRowWarps][CH];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rows_per_cta = int(blockDim.x >> 5) / wpr;
-  const int r_in_cta = warp / wpr, w_in_row = warp % wpr;
-  const int wrow0 = r_in_cta * wpr;  // first warp of this row
-  const int nchunk = K >> 3;
-  const uint32_t tb = ctrl->t_bits;
-  const uint32_t tb2 = tb | (tb << 16);
-  const float t = *t_ptr;
-  // persistent over row groups; the next group's chunks are loaded before the
-  // current group is processed, so every warp keeps one row's loads in flight
-  const int64_t gstride = int64_t(gridDim.x) * rows_per_cta;
-  uint4 v[CH];
-  {
-    const int64_t row = int64_t(blockIdx.x) * rows_per_cta + r_in_cta;
-    const uint4* src = reinterpret_cast<const uint4*>(A + (row < M ? row : 0) * lda);
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int ci = lane + 32 * (w_in_row + wpr * c);
-      v[c] = (row < M && ci < nchunk) ? __ldcs(src + ci) : make_uint4(0u, 0u, 0u, 0u);
+// ---------------------------------------------------------------------------
+// The fused row call: threshold, clamp, CSR of dA and (optionally) the row
+// codes / scales and A_clamped in ONE cooperative kernel (one CTA of 512
+// threads per SM, all resident; grid barriers are bounded waits).
+//
+//  1. pilot: every 64th row of each CTA's row block in a full 32768-bin
+//     histogram, merged into g_pilot;                          -- barrier
+//  2. every CTA derives the same floor F from the pilot: the sample's
+//     magnitude with 4x the requested exceedance (plus 16) above it, so t >= F
+//     unless the sample misleads (then step 4 fills the rest in);
+//  3. main pass over the CTA's rows: a histogram of the magnitudes >= F only
+//     (a chunk whose 8 magnitudes are all below F costs three packed maxima,
+//     no atomics), merged into g_main;                          -- barrier
+//  4. every CTA selects t = the largest bin b with #{|A| >= b} >= n - k + 1
+//     (the k-th smallest); if the bins >= F hold fewer than n - k + 1 values,
+//     a second pass counts the magnitudes < F, and t is selected over all bins;
+//  5. row pass over the CTA's rows in reverse order (the rows read last in
+//     step 3 are still in L2): one warp per row, absmax of the clamped row and
+//     the outlier count, then codes, scale, A_clamped and the row's first
+//     kRowSlots entries (column order) into its slots;          -- barrier
+//  6. row_ptr from the per-CTA totals and a block scan; the slots (or, for a
+//     longer row, A read again) go to their CSR positions.
+constexpr int kRThreads = 512;
+constexpr int kRWarps = kRThreads / 32;
+constexpr int kPilotStride = 64;
+constexpr int kRU = 8;   // 16-byte loads in flight per lane (row pass, two sweeps)
+constexpr int kHU = 16;  // 16-byte loads in flight per lane (histogram passes)
+
+struct FCtrl {
+  uint32_t bar_count;   // CTAs arrived at the current grid barrier
+  uint32_t bar_gen;     // barrier generation
+};
+
+struct RowCallParams {
+  const uint16_t* A;
+  int64_t M;
+  int K;
+  int64_t lda;
+  int64_t k_rank;          // 1-based rank of t among |A| ascending
+  int64_t n_pilot;         // values in the pilot sample (every kPilotStride-th row of each CTA's block)
+  uint32_t* g_pilot;       // 32768 bins, zeroed
+  uint32_t* g_main;        // 32768 bins, zeroed
+  FCtrl* fctrl;            // zeroed
+  Ctrl* ctrl;              // t_bits and nnz_expect for the caller-visible checks
+  int64_t* cta_total;      // one per CTA
+  int32_t* row_cnt;
+  int32_t* scol;
+  float* sval;
+  float* t_out;
+  int32_t* row_ptr;
+  int32_t* col_idx;
+  float* vals;
+  int64_t cap;
+  int64_t* nnz_out;
+  uint16_t* A_c;
+  int64_t ldac;
+  uint8_t* codes;
+  int64_t ldc;
+  float* scales;
+  uint32_t* status;
+  uint64_t wait_ns;
+};
+
+// Grid barrier over co-resident CTAs (sense by generation), bounded: false when
+// the limit ran out (the caller records FP4_FLAG_TIMEOUT and stops).
+__device__ bool grid_sync(FCtrl* c, uint64_t limit_ns) {
+  __syncthreads();
+  int ok = 1;
+  if (threadIdx.x == 0) {
+    volatile uint32_t* gen = &c->bar_gen;
+    const uint32_t g = *gen;
+    __threadfence();
+    if (atomicAdd(&c->bar_count, 1u) == gridDim.x - 1) {
+      c->bar_count = 0u;
+      __threadfence();
+      atomicAdd(&c->bar_gen, 1u);
+    } else {
+      const uint64_t t0 = global_timer_ns();
+      while (*gen == g) {
+        if (global_timer_ns() - t0 > limit_ns) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
     }
+    __threadfence();
   }
-  for (int64_t row0 = int64_t(blockIdx.x) * rows_per_cta; row0 < M; row0 += gstride) {
-    const int64_t row = row0 + r_in_cta;
-    const bool active = row < M;
-    uint4 vn[CH];
-    {
-      const int64_t nrow = row + gstride;
-      const uint4* nsrc = reinterpret_cast<const uint4*>(A + (nrow < M ? nrow : 0) * lda);
+  return __syncthreads_and(ok) != 0;
+}
+
+// Counts the magnitude patterns in [lo, hi) of rows r (r_begin <= r < r_end,
+// r - r_begin a multiple of `stride`, one warp per row) into hist (shared).
+__device__ void rows_histogram(const RowCallParams& p, int64_t r_begin, int64_t r_end, int stride, uint32_t lo,
+                               uint32_t hi, uint32_t* hist) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunk = p.K >> 3;
+  for (int64_t row = r_begin + int64_t(warp) * stride; row < r_end; row += int64_t(kRWarps) * stride) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.A + row * p.lda);
+    for (int c00 = 0; c00 < nchunk; c00 += 32 * kHU) {   // every lane takes every step
+      uint4 v[kHU];
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int ci = lane + 32 * (w_in_row + wpr * c);
-        vn[c] = (nrow < M && ci < nchunk) ? __ldcs(nsrc + ci) : make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < kHU; ++u) {
+        const int c = c00 + 32 * u + lane;
+        v[u] = c < nchunk ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
       }
-    }
-    uint32_t msk[CH], excl[CH];
-    uint32_t mx = 0;
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      // one packed maximum per chunk serves the row's absmax and the outlier test
-      const uint32_t m2 = chunk_maxmag(v[c]);
-      if (CODES) mx = bf2_max(mx, m2);
-      const uint32_t g = bf2_gt_mask(m2, tb2);
-      msk[c] = 0;
-      excl[c] = 0;
-      uint32_t tot = 0;
-      if (__any_sync(0xFFFFFFFFu, g != 0)) {  // rare: some lane has an outlier in this slot
-        msk[c] = g ? outlier_mask8(v[c], tb) : 0u;
-        const uint32_t n = __popc(msk[c]);
-        uint32_t incl = n;
+      for (int u = 0; u < kHU; ++u) {
+        if (c00 + 32 * u + lane >= nchunk) continue;
+        const uint32_t m2 = chunk_maxmag(v[u]);
+        if (max(m2 & 0xFFFFu, m2 >> 16) < lo) continue;   // all 8 below the range: no atomics
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-        excl[c] = incl - n;
-      }
-      if (lane == 0) tcnt[warp][c] = tot;
-    }
-    if (CODES) {
-      const uint32_t mb = warp_max_bits(mx);
-      if (lane == 0) red[warp] = mb;
-    }
-    __syncthreads();
-    if (active && w_in_row == 0 && lane == 0) {
-      uint32_t total = 0;
-      for (int c = 0; c < CH; ++c)
-        for (int w = 0; w < wpr; ++w) total += tcnt[wrow0 + w][c];
-      row_cnt[row] = int32_t(total);
-    }
-    if (active) {
-      // the row's first kRowSlots entries go to its slots; a longer row is
-      // emitted again from A by the gather pass
-      uint32_t off = 0;
-#pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        uint32_t pos = off + excl[c];
-        for (int w = 0; w < w_in_row; ++w) pos += tcnt[wrow0 + w][c];
-        uint32_t m = msk[c];
-        if (m && pos < uint32_t(kRowSlots)) {
-          const int ci = lane + 32 * (w_in_row + wpr * c);
-          const uint4 vc = v[c];
-          while (m && pos < uint32_t(kRowSlots)) {  // set bits in ascending column order
-            const int e = __ffs(m) - 1;
-            m &= m - 1;
-            const uint32_t word = e < 4 ? (e < 2 ? vc.x : vc.y) : (e < 6 ? vc.z : vc.w);
-            const float x = bf16_bits_to_float((word >> (16 * (e & 1))) & 0xFFFFu);
-            scol[row * kRowSlots + pos] = ci * 8 + e;
-            sval[row * kRowSlots + pos] = __fsub_rn(x, copysignf(t, x));
-            ++pos;
-          }
-        }
-        for (int w = 0; w < wpr; ++w) off += tcnt[wrow0 + w][c];
-      }
-    }
-    if (active && A_c) {
-      uint4* dst = reinterpret_cast<uint4*>(A_c + row * ldac);
-#pragma unroll
-      for (int c = 0; c < CH; ++c) {
-        const int ci = lane + 32 * (w_in_row + wpr * c);
-        if (ci < nchunk) {
-          const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-          uint32_t cw[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
-            cw[i] = (((lo & 0x7FFFu) > tb) ? ((lo & 0x8000u) | tb) : lo) |
-                    ((((hi & 0x7FFFu) > tb) ? ((hi & 0x8000u) | tb) : hi) << 16);
-          }
-          dst[ci] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t k0 = w[i] & 0x7FFFu, k1 = (w[i] >> 16) & 0x7FFFu;
+          if (k0 >= lo && k0 < hi) atomicAdd(hist + k0, 1u);
+          if (k1 >= lo && k1 < hi) atomicAdd(hist + k1, 1u);
         }
       }
     }
-    if (CODES) {
-      uint32_t amax_bits = 0;
-      for (int i = 0; i < wpr; ++i) amax_bits = max(amax_bits, red[wrow0 + i]);
-      // max over min(|x|, t) = min(max |x|, t)
-      const float sc = scale_from_absmax(bf16_bits_to_float(min(amax_bits, tb)));
-      if (active) {
-        if (w_in_row == 0 && lane == 0) scales[row] = sc;
-        uint32_t* dst = reinterpret_cast<uint32_t*>(codes + row * ldc);
-#pragma unroll
-        for (int c = 0; c < CH; ++c) {
-          const int ci = lane + 32 * (w_in_row + wpr * c);
-          if (ci < nchunk) dst[ci] = quantize8<true>(v[c], sc, tb2);   // the clamp is a no-op without outliers
-        }
-      }
-    }
-    __syncthreads();  // tcnt / red are reused by the next row group
-#pragma unroll
-    for (int c = 0; c < CH; ++c) v[c] = vn[c];
   }
 }
 
-// row_ptr[0] = 0, row_ptr[i+1] = sum of counts of rows <= i, in tiles of 4096
-// rows (coalesced loads); checks the total against the histogram's count.
-__global__ void __launch_bounds__(1024) row_scan_kernel(const int32_t* __restrict__ row_cnt, int64_t M,
-                                                       int32_t* __restrict__ row_ptr, int64_t* __restrict__ nnz_out,
-                                                       const Ctrl* __restrict__ ctrl, int64_t cap,
-                                                       uint32_t* __restrict__ status) {
-  __shared__ long long wsum[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  long long carry = 0;
-  if (tid == 0) row_ptr[0] = 0;
-  for (int64_t base = 0; base < M; base += 4096) {
-    const int64_t idx = base + 4 * tid;
-    int c[4];
-    if (idx + 3 < M) {
-      const int4 q = *reinterpret_cast<const int4*>(row_cnt + idx);
-      c[0] = q.x; c[1] = q.y; c[2] = q.z; c[3] = q.w;
-    } else {
+// Zeroes hist[lo, hi) (shared), histograms the CTA's rows into it and adds the
+// nonzero bins to g (global).
+__device__ void histogram_phase(const RowCallParams& p, int64_t r0, int64_t r1, int stride, uint32_t lo,
+                                uint32_t hi, uint32_t* hist, uint32_t* g) {
+  for (uint32_t b = lo + threadIdx.x; b < hi; b += kRThreads) hist[b] = 0u;
+  __syncthreads();
+  rows_histogram(p, r0, r1, stride, lo, hi, hist);
+  __syncthreads();
+  for (uint32_t b = lo + threadIdx.x; b < hi; b += kRThreads) {
+    const uint32_t c = hist[b];
+    if (c) atomicAdd(g + b, c);
+  }
+}
+
+// Over bins [lo, 32768) of g (global, complete there): finds the largest bin b
+// with suffix(b) = sum of bins >= b at least `target`.  Returns b, or -1 when
+// suffix(lo) < target; *total = suffix(lo), *above = suffix(b + 1).  Uniform
+// over the CTA (uses `scratch`: kBins words of shared memory).
+__device__ int suffix_select(const uint32_t* g, uint32_t lo, uint64_t target, uint32_t* scratch, uint64_t* total,
+                             uint64_t* above) {
+  __shared__ int sel;
+  __shared__ unsigned long long sel_above;
+  constexpr int kPer = kBins / kRThreads;   // 64 bins a thread
+  {
+    // all of a thread's loads in flight at once, then the stores (a load-then-store
+    // loop would wait out one L2 round trip per 16 bytes)
+    constexpr int kLd = kBins / 4 / kRThreads;   // 16
+    uint4 v[kLd];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) c[i] = (idx + i < M) ? row_cnt[idx + i] : 0;
+    for (int j = 0; j < kLd; ++j) {
+      const int i = threadIdx.x + j * kRThreads;
+      v[j] = (4u * uint32_t(i) + 3u < lo) ? make_uint4(0u, 0u, 0u, 0u) : __ldcg(reinterpret_cast<const uint4*>(g) + i);
     }
-    const long long s0 = c[0], s1 = s0 + c[1], s2 = s1 + c[2], s3 = s2 + c[3];
-    long long x = s3;
+#pragma unroll
+    for (int j = 0; j < kLd; ++j) reinterpret_cast<uint4*>(scratch)[threadIdx.x + j * kRThreads] = v[j];
+  }
+  if (threadIdx.x == 0) sel = -1;
+  __syncthreads();
+  // bins below lo are not counted (a partially covered word had them zeroed above only if fully below)
+  const int b0 = threadIdx.x * kPer;
+  unsigned long long sum = 0;
+  for (int i = 0; i < kPer; ++i) {
+    const int b = b0 + ((i + threadIdx.x) & (kPer - 1));
+    if (uint32_t(b) >= lo) sum += scratch[b];
+  }
+  // suffix sums over the 512 partial sums (from the top), one thread per partial
+  unsigned long long suf = 0;   // sum of partials of threads > this one
+  {
+    // a simple two-level scan: each warp sums its 32 partials, then warps from the top
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    unsigned long long x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_down_sync(0xFFFFFFFFu, x, o);
+      if (lane + o < 32) x += y;
+    }
+    // x = sum of partials lane..31 of this warp
+    __shared__ unsigned long long wsum[kRWarps];
+    if (lane == 0) wsum[wid] = x;
+    __syncthreads();
+    unsigned long long higher = 0;
+    for (int w = wid + 1; w < kRWarps; ++w) higher += wsum[w];
+    suf = higher + x - sum;   // partials strictly above this thread
+    if (threadIdx.x == 0) *total = higher + x;
+  }
+  // the crossing: suffix at the top of this thread's range is suf, at its bottom suf + sum
+  if (suf < target && suf + sum >= target) {
+    unsigned long long run = suf;
+    for (int i = kPer - 1; i >= 0; --i) {
+      const int b = b0 + i;
+      const unsigned long long c = uint32_t(b) >= lo ? scratch[b] : 0u;
+      if (run + c >= target) {
+        sel = b;
+        sel_above = run;
+        break;
+      }
+      run += c;
+    }
+  }
+  __syncthreads();
+  *above = sel_above;
+  const int r = sel;
+  __syncthreads();
+  return r;
+}
+
+// The row's entries in chunk j (lane's 16-byte chunk c = column chunk): the warp
+// numbers them in column order (chunk index c ascending across the lanes) and
+// writes those with position < kRowSlots into the row's slots.  `pos` (warp-
+// uniform) is the number of entries in earlier chunks; every lane must call.
+__device__ __noinline__ void emit_slots(const RowCallParams& p, int64_t row, int c, bool valid, const uint4 v,
+                                        uint32_t tbits, float t, uint32_t& pos) {
+  const int lane = threadIdx.x & 31;
+  uint32_t m = valid ? outlier_mask8(v, tbits) : 0u;
+  const uint32_t nm = __popc(m);
+  if (!__any_sync(0xFFFFFFFFu, nm != 0)) return;
+  uint32_t incl = nm;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t ps = pos + incl - nm;
+  while (m && ps < uint32_t(kRowSlots)) {   // set bits in ascending column order
+    const int e = __ffs(m) - 1;
+    m &= m - 1;
+    const uint32_t word = e < 4 ? (e < 2 ? v.x : v.y) : (e < 6 ? v.z : v.w);
+    const float x = bf16_bits_to_float((word >> (16 * (e & 1))) & 0xFFFFu);
+    p.scol[row * kRowSlots + ps] = c * 8 + e;
+    p.sval[row * kRowSlots + ps] = __fsub_rn(x, copysignf(t, x));
+    ++ps;
+  }
+  pos += __shfl_sync(0xFFFFFFFFu, incl, 31);
+}
+
+// Codes and A_clamped of one 16-byte chunk; `has` says whether some value of the
+// chunk exceeds t (without one the clamp changes nothing and is skipped).
+__device__ __noinline__ void chunk_outputs_clamped(uint32_t* cdst, uint4* adst, int c, const uint4 v, float sc,
+                                                 uint32_t tb2) {
+  if (cdst) cdst[c] = quantize8<true>(v, sc, tb2);
+  if (adst) adst[c] = make_uint4(clamp_pair(v.x, tb2), clamp_pair(v.y, tb2), clamp_pair(v.z, tb2), clamp_pair(v.w, tb2));
+}
+// (the rare paths are out of line: a fully unrolled row pass with them inlined
+// outgrew the instruction cache)
+__device__ __forceinline__ void chunk_outputs(uint32_t* cdst, uint4* adst, int c, const uint4 v, float sc, uint32_t tb2,
+                                              bool has) {
+  if (has) {
+    chunk_outputs_clamped(cdst, adst, c, v, sc, tb2);
+    return;
+  }
+  if (cdst) cdst[c] = quantize8_packed(v, sc);
+  if (adst) adst[c] = v;
+}
+
+__device__ __noinline__ uint32_t count_outliers(const uint4 v, uint32_t tbits) { return __popc(outlier_mask8(v, tbits)); }
+
+// Scale, row count and slots of one row from its absmax pattern and count
+// (warp-uniform); lane 0 writes them.  Returns the scale.
+__device__ __forceinline__ float row_scale(const RowCallParams& p, int64_t row, uint32_t amax_bits, uint32_t cnt,
+                                           uint32_t tbits) {
+  // max over min(|x|, t) = min(max |x|, t)
+  const float sc = scale_from_absmax(bf16_bits_to_float(min(amax_bits, tbits)));
+  if ((threadIdx.x & 31) == 0) {
+    if (p.scales) p.scales[row] = sc;
+    p.row_cnt[row] = int32_t(cnt);
+  }
+  return sc;
+}
+
+// One row held in registers (CH 16-byte chunks a lane, c = 32 j + lane): one read
+// of A.  Every lane of the warp calls; returns the row's outlier count.
+template <int CH>
+__device__ uint32_t row_pass_regs(const RowCallParams& p, int64_t row, int nchunk, uint32_t tbits, float t) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t tb2 = tbits | (tbits << 16);
+  const uint4* src = reinterpret_cast<const uint4*>(p.A + row * p.lda);
+  uint4 v[CH];
+#pragma unroll
+  for (int j = 0; j < CH; ++j) {
+    const int c = 32 * j + lane;
+    v[j] = c < nchunk ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  uint32_t mx = 0, cnt = 0, ob = 0;   // ob bit j: chunk j holds a value above t
+#pragma unroll
+  for (int j = 0; j < CH; ++j) {
+    const uint32_t m2 = chunk_maxmag(v[j]);   // zero chunks (past the row) add nothing
+    mx = bf2_max(mx, m2);
+    if (bf2_gt_mask(m2, tb2)) {
+      ob |= 1u << j;
+      cnt += count_outliers(v[j], tbits);
+    }
+  }
+  const uint32_t amax_bits = warp_max_bits(mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+  const float sc = row_scale(p, row, amax_bits, cnt, tbits);
+  uint32_t* cdst = p.codes ? reinterpret_cast<uint32_t*>(p.codes + row * p.ldc) : nullptr;
+  uint4* adst = p.A_c ? reinterpret_cast<uint4*>(p.A_c + row * p.ldac) : nullptr;
+  uint32_t pos = 0;
+#pragma unroll
+  for (int j = 0; j < CH; ++j) {
+    const int c = 32 * j + lane;
+    const bool has = (ob >> j) & 1u;
+    if (c < nchunk) chunk_outputs(cdst, adst, c, v[j], sc, tb2, has);
+    if (cnt != 0 && pos < uint32_t(kRowSlots)) {   // warp-uniform
+      if (__any_sync(0xFFFFFFFFu, has)) emit_slots(p, row, c, has, v[j], tbits, t, pos);
+    }
+  }
+  return cnt;
+}
+
+// A row too wide for registers: absmax and count in a first sweep over A, then
+// codes, A_clamped and slots in a second (the row is then in L1 / L2).
+__device__ uint32_t row_pass_two_sweeps(const RowCallParams& p, int64_t row, int nchunk, uint32_t tbits, float t) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t tb2 = tbits | (tbits << 16);
+  const uint4* src = reinterpret_cast<const uint4*>(p.A + row * p.lda);
+  uint32_t mx = 0, cnt = 0;
+  uint64_t ob = 0;   // bit g: this lane's chunk 32 g + lane holds a value above t (g < 64: K <= 16384)
+  for (int c00 = 0; c00 < nchunk; c00 += 32 * kRU) {   // every lane takes every step
+    uint4 v[kRU];
+#pragma unroll
+    for (int u = 0; u < kRU; ++u) {
+      const int c = c00 + 32 * u + lane;
+      v[u] = c < nchunk ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kRU; ++u) {
+      const uint32_t m2 = chunk_maxmag(v[u]);
+      mx = bf2_max(mx, m2);
+      if (bf2_gt_mask(m2, tb2)) {
+        ob |= 1ull << (c00 / 32 + u);
+        cnt += count_outliers(v[u], tbits);
+      }
+    }
+  }
+  const uint32_t amax_bits = warp_max_bits(mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+  const float sc = row_scale(p, row, amax_bits, cnt, tbits);
+  uint32_t* cdst = p.codes ? reinterpret_cast<uint32_t*>(p.codes + row * p.ldc) : nullptr;
+  uint4* adst = p.A_c ? reinterpret_cast<uint4*>(p.A_c + row * p.ldac) : nullptr;
+  uint32_t pos = 0;
+  for (int c00 = 0; c00 < nchunk; c00 += 32 * kRU) {   // every lane takes every step (warp-wide scans)
+    uint4 v[kRU];
+#pragma unroll
+    for (int u = 0; u < kRU; ++u) {
+      const int c = c00 + 32 * u + lane;
+      v[u] = c < nchunk ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kRU; ++u) {
+      const int c = c00 + 32 * u + lane;
+      const bool has = (ob >> (c00 / 32 + u)) & 1ull;
+      if (c < nchunk) chunk_outputs(cdst, adst, c, v[u], sc, tb2, has);
+      if (cnt != 0 && pos < uint32_t(kRowSlots)) {   // warp-uniform
+        if (__any_sync(0xFFFFFFFFu, has)) emit_slots(p, row, c, has, v[u], tbits, t, pos);
+      }
+    }
+  }
+  return cnt;
+}
+
+__global__ void __launch_bounds__(kRThreads, 1) rowcall_kernel(const RowCallParams p) {
+  extern __shared__ uint32_t hist[];   // kBins words
+  __shared__ uint64_t s_above;
+  __shared__ unsigned long long red64[kRWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t n = p.M * int64_t(p.K);
+  const int64_t r0 = p.M * blockIdx.x / gridDim.x, r1 = p.M * (blockIdx.x + 1) / gridDim.x;
+  const uint64_t e_rank = uint64_t(n - p.k_rank + 1);   // t is the e_rank-th largest magnitude
+  bool ok = true;
+
+  // ---- 1-2: pilot histogram and the floor F
+  uint32_t F = 0;
+  const bool use_pilot = e_rank * 4 <= uint64_t(n);   // q > 0.75: the threshold sits in the tail
+  if (use_pilot) {
+    histogram_phase(p, r0, r1, kPilotStride, 0u, uint32_t(kBins), hist, p.g_pilot);
+    ok = grid_sync(p.fctrl, p.wait_ns);
+    if (ok) {
+      const uint64_t n_pilot = uint64_t(p.n_pilot);
+      uint64_t dummy = 0;
+      const double want = 4.0 * double(e_rank) * double(n_pilot) / double(n) + 16.0;
+      if (n_pilot >= 4096 && want < double(n_pilot)) {
+        const int f = suffix_select(p.g_pilot, 0u, uint64_t(want), hist, &dummy, &dummy);
+        F = f < 0 ? 0u : uint32_t(f);
+      }
+    }
+  }
+  // ---- 3-4: histogram of the magnitudes >= F, then t
+  int tb = -1;
+  uint64_t nnz_expect = 0;
+  if (ok) {
+    histogram_phase(p, r0, r1, 1, F, uint32_t(kBins), hist, p.g_main);
+    ok = grid_sync(p.fctrl, p.wait_ns);
+  }
+  if (ok) {
+    uint64_t tot = 0, above = 0;
+    tb = suffix_select(p.g_main, F, e_rank, hist, &tot, &above);
+    if (threadIdx.x == 0) s_above = above;
+    __syncthreads();
+    if (tb < 0 && F > 0) {   // the pilot misled: count the magnitudes below F as well
+      histogram_phase(p, r0, r1, 1, 0u, F, hist, p.g_main);
+      ok = grid_sync(p.fctrl, p.wait_ns);
+      if (ok) {
+        tb = suffix_select(p.g_main, 0u, e_rank, hist, &tot, &above);
+        if (threadIdx.x == 0) s_above = above;
+        __syncthreads();
+      }
+    }
+    nnz_expect = s_above;
+  }
+  if (!ok) {   // a grid barrier ran out: report, produce nothing
+    if (threadIdx.x == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    return;
+  }
+  if (tb < 0) {   // cannot happen with a complete histogram: report, produce nothing
+    if (threadIdx.x == 0) atomicOr(p.status, FP4_FLAG_INTERNAL);
+    return;
+  }
+  const uint32_t tbits = uint32_t(tb);
+  const float t = bf16_bits_to_float(tbits);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *p.t_out = t;
+    p.ctrl->t_bits = tbits;
+    p.ctrl->nnz_expect = nnz_expect;
+  }
+
+  // ---- 5: row pass, one warp per row, the CTA's rows in reverse order
+  const int nchunk = p.K >> 3;
+  const int per_lane = (nchunk + 31) / 32;
+  long long cta_cnt = 0;
+  for (int64_t i = warp; r1 - 1 - i >= r0; i += kRWarps) {
+    const int64_t row = r1 - 1 - i;
+    uint32_t cnt;
+    if (per_lane <= 4) cnt = row_pass_regs<4>(p, row, nchunk, tbits, t);
+    else if (per_lane <= 8) cnt = row_pass_regs<8>(p, row, nchunk, tbits, t);
+    else if (per_lane <= 16) cnt = row_pass_regs<16>(p, row, nchunk, tbits, t);
+    else if (per_lane <= 20) cnt = row_pass_regs<20>(p, row, nchunk, tbits, t);
+    else cnt = row_pass_two_sweeps(p, row, nchunk, tbits, t);
+    cta_cnt += cnt;
+  }
+  // the CTA's total
+  if (lane == 0) red64[warp] = (unsigned long long)cta_cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long s = 0;
+    for (int w = 0; w < kRWarps; ++w) s += red64[w];
+    p.cta_total[blockIdx.x] = int64_t(s);
+  }
+  if (!grid_sync(p.fctrl, p.wait_ns)) {
+    if (threadIdx.x == 0) atomicOr(p.status, FP4_FLAG_TIMEOUT);
+    return;
+  }
+
+  // ---- 6: row_ptr and the gather
+  __shared__ long long s_base;
+  {
+    long long b = 0;
+    for (int c = threadIdx.x; c < int(blockIdx.x); c += kRThreads) b += __ldcg(p.cta_total + c);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(0xFFFFFFFFu, b, o);
+    if (lane == 0) red64[warp] = (unsigned long long)b;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      long long s = 0;
+      for (int w = 0; w < kRWarps; ++w) s += (long long)red64[w];
+      s_base = s;
+    }
+    __syncthreads();
+  }
+  const long long base = s_base;
+  // row_ptr[r0] is also the previous CTA's last value; writing it here (the same
+  // number) lets the gather below read only this CTA's own entries
+  if (threadIdx.x == 0 && (r0 < r1 || blockIdx.x == 0)) p.row_ptr[r0] = int32_t(base);
+  // block scan of the counts of rows r0 .. r1 - 1, kRThreads at a time
+  long long carry = 0;
+  for (int64_t tile = r0; tile < r1; tile += kRThreads) {
+    const int64_t row = tile + threadIdx.x;
+    const long long c = row < r1 ? __ldcg(p.row_cnt + row) : 0;
+    long long x = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const long long y = __shfl_up_sync(0xFFFFFFFFu, x, o);
       if (lane >= o) x += y;
     }
-    if (lane == 31) wsum[warp] = x;
     __syncthreads();
-    if (warp == 0) {
-      long long w = wsum[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(0xFFFFFFFFu, w, o);
-        if (lane >= o) w += y;
-      }
-      wsum[lane] = w;
+    if (lane == 31) red64[warp] = (unsigned long long)x;
+    __syncthreads();
+    long long before = 0, tile_total = 0;
+    for (int w = 0; w < kRWarps; ++w) {
+      if (w < warp) before += (long long)red64[w];
+      tile_total += (long long)red64[w];
     }
-    __syncthreads();
-    const long long excl = carry + (warp ? wsum[warp - 1] : 0) + x - s3;
-    const long long incl4[4] = {s0, s1, s2, s3};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (idx + i < M) row_ptr[idx + i + 1] = int32_t(excl + incl4[i]);
-    carry += wsum[31];
-    __syncthreads();
+    if (row < r1) p.row_ptr[row + 1] = int32_t(base + carry + before + x);
+    carry += tile_total;
   }
-  if (tid == 0) {
-    if (nnz_out) *nnz_out = carry;
-    if (carry > cap) atomicOr(status, FP4_FLAG_CAPACITY);
-    else if (uint64_t(carry) != ctrl->nnz_expect) atomicOr(status, FP4_FLAG_INTERNAL);
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
+    const long long total = base + carry;
+    if (p.nnz_out) *p.nnz_out = total;
+    if (total > p.cap) atomicOr(p.status, FP4_FLAG_CAPACITY);
+    else if (uint64_t(total) != p.ctrl->nnz_expect) atomicOr(p.status, FP4_FLAG_INTERNAL);
   }
-}
-
-// One warp per row: the row's slots to its CSR position, or, for a row with
-// more than kRowSlots entries, the row read again from A and emitted in column
-// order (a warp prefix over the lanes' 16-byte chunks).
-__global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__ row_cnt,
-                                                    const int32_t* __restrict__ row_ptr, int64_t M,
-                                                    const int32_t* __restrict__ scol, const float* __restrict__ sval,
-                                                    const uint16_t* __restrict__ A, int K, int64_t lda,
-                                                    const Ctrl* __restrict__ ctrl, const float* __restrict__ t_ptr,
-                                                    int32_t* __restrict__ col_idx, float* __restrict__ vals,
-                                                    int64_t cap) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp_global = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  const uint32_t tb = ctrl->t_bits;
-  const float t = *t_ptr;
-  const int nchunk = K >> 3;
-  for (int64_t row = warp_global; row < M; row += nwarps) {
-    const int32_t n = row_cnt[row];
-    const int64_t dst = row_ptr[row];
-    if (dst + n > cap) continue;   // flagged by the scan
-    if (n <= kRowSlots) {
-      if (lane < n) {
-        col_idx[dst + lane] = scol[row * kRowSlots + lane];
-        vals[dst + lane] = sval[row * kRowSlots + lane];
+  __syncthreads();   // this CTA's row_ptr entries are visible to all its threads
+  if (p.cap == 0) return;
+  // gather: the row's slots to its CSR position, or the row read again from A
+  for (int64_t row = r0 + warp; row < r1; row += kRWarps) {
+    const int32_t nr = __ldcg(p.row_cnt + row);
+    const int64_t dst = p.row_ptr[row];
+    if (nr == 0 || dst + nr > p.cap) continue;   // beyond the capacity: flagged above
+    if (nr <= kRowSlots) {
+      if (lane < nr) {
+        p.col_idx[dst + lane] = __ldcg(p.scol + row * kRowSlots + lane);
+        p.vals[dst + lane] = __ldcg(p.sval + row * kRowSlots + lane);
       }
       continue;
     }
-    const uint4* src = reinterpret_cast<const uint4*>(A + row * lda);
-    int64_t base = dst;
+    const uint4* src = reinterpret_cast<const uint4*>(p.A + row * p.lda);
+    int64_t b = dst;
     constexpr int kDepth = 4;   // 32-chunk groups loaded before any is scanned
-    for (int c00 = 0; c00 < nchunk; c00 += 32 * kDepth) {
+    for (int c00 = 0; c00 < nchunk; c00 += 32 * kDepth) {   // every lane takes every step
       uint4 vv[kDepth];
 #pragma unroll
       for (int u = 0; u < kDepth; ++u) {
@@ -417,25 +600,25 @@ __global__ void __launch_bounds__(256) gather_kernel(const int32_t* __restrict__
       for (int u = 0; u < kDepth; ++u) {
         const int ci = c00 + 32 * u + lane;
         const uint4 v = vv[u];
-        uint32_t m = ci < nchunk ? outlier_mask8(v, tb) : 0u;
-        const uint32_t cnt = __popc(m);
-        uint32_t incl = cnt;
+        uint32_t m = ci < nchunk ? outlier_mask8(v, tbits) : 0u;
+        const uint32_t nm = __popc(m);
+        uint32_t incl = nm;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
           if (lane >= o) incl += y;
         }
-        int64_t pos = base + (incl - cnt);
+        int64_t ps = b + (incl - nm);
         while (m) {
           const int e = __ffs(m) - 1;
           m &= m - 1;
           const uint32_t word = e < 4 ? (e < 2 ? v.x : v.y) : (e < 6 ? v.z : v.w);
           const float x = bf16_bits_to_float((word >> (16 * (e & 1))) & 0xFFFFu);
-          col_idx[pos] = ci * 8 + e;
-          vals[pos] = __fsub_rn(x, copysignf(t, x));
-          ++pos;
+          p.col_idx[ps] = ci * 8 + e;
+          p.vals[ps] = __fsub_rn(x, copysignf(t, x));
+          ++ps;
         }
-        base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        b += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
     }
   }
@@ -460,25 +643,10 @@ FP4_API size_t outlier_clamp_quantile_workspace(int64_t M, int64_t K, int64_t nn
 namespace fp4 {
 namespace {
 
-template <bool CODES>
-void launch_rows_outlier(int ch, int wpr, unsigned blocks, unsigned threads, cudaStream_t s, const uint16_t* A,
-                         int64_t M, int K, int64_t lda, Ctrl* ctrl, const float* t, int32_t* row_cnt,
-                         int32_t* scol, float* sval, uint16_t* A_c, int64_t ldac, uint8_t* codes, int64_t ldc,
-                         float* scales) {
-#define FP4_ROWS_OUTLIER(CHV)                                                                                     \
-  rows_outlier_kernel<CHV, CODES><<<blocks, threads, 0, s>>>(A, M, K, lda, ctrl, t, row_cnt, scol, sval, A_c, ldac, \
-                                                             codes, ldc, scales, wpr)
-  switch (ch) {
-    case 1: FP4_ROWS_OUTLIER(1); break;
-    case 2: FP4_ROWS_OUTLIER(2); break;
-    case 4: FP4_ROWS_OUTLIER(4); break;
-    default: FP4_ROWS_OUTLIER(8); break;
-  }
-#undef FP4_ROWS_OUTLIER
-}
-
-// Histogram + threshold, fused row pass (CSR staging, optional A_clamped, optional
-// codes / scales), row scan and gather.  Arguments are validated by the callers.
+// The fused row call (rowcall_kernel): threshold, clamp, CSR staging, optional
+// A_clamped and codes / scales, row_ptr and gather in one cooperative launch of
+// one CTA per SM, after one memset of the histograms and control blocks.
+// Arguments are validated by the callers.
 fp4_status run_outlier_pipeline(const void* A, int64_t M, int64_t K, int64_t lda, double q, float* t_out,
                                 int32_t* row_ptr, int32_t* col_idx, float* vals, int64_t nnz_capacity,
                                 int64_t* nnz_out, void* A_clamped, int64_t ldac, uint8_t* codes, int64_t ldc,
@@ -488,73 +656,68 @@ fp4_status run_outlier_pipeline(const void* A, int64_t M, int64_t K, int64_t lda
   if (st != FP4_OK) return st;
   const WsLayout L = ws_layout(M);
   auto* ws = static_cast<uint8_t*>(workspace);
-  auto* ghist = reinterpret_cast<uint32_t*>(ws + L.hist);
-  auto* ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
-  auto* row_cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
-  auto* scol = reinterpret_cast<int32_t*>(ws + L.scol);
-  auto* sval = reinterpret_cast<float*>(ws + L.sval);
-  uint32_t* status = status_word();
-  const auto* a = static_cast<const uint16_t*>(A);
-
   const int64_t n = M * K;
-  const int64_t k_rank = n - outlier_max_nnz(M, K, q);
-  if (cudaMemsetAsync(ws, 0, L.cnt, s) != cudaSuccess) return FP4_ERR_CUDA;  // histogram + control block
+  if (cudaMemsetAsync(ws, 0, L.cta_total, s) != cudaSuccess) return FP4_ERR_CUDA;
 
-  static bool attr_set[64] = {false};
+  static int ctas_per_sm[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  const size_t hist_smem = size_t(kBins) * 4;
-  if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(histogram_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(hist_smem)) !=
-        cudaSuccess)
+  const size_t smem = size_t(kBins) * 4;
+  if (dev < 0 || dev >= 64) return FP4_ERR_CUDA;
+  if (!ctas_per_sm[dev]) {
+    if (cudaFuncSetAttribute(rowcall_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
       return FP4_ERR_CUDA;
-    attr_set[dev] = true;
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, rowcall_kernel, kRThreads, smem) != cudaSuccess || nb < 1)
+      return FP4_ERR_CUDA;
+    ctas_per_sm[dev] = nb;
   }
-  const int64_t chunks = n / 8;
-  int64_t hblocks = (chunks + kHistThreads * 8 - 1) / (kHistThreads * 8);
-  if (hblocks > sms) hblocks = sms;
-  if (hblocks < 1) hblocks = 1;
-  histogram_select_kernel<<<unsigned(hblocks), kHistThreads, hist_smem, s>>>(a, M, int(K), lda, k_rank, ghist, ctrl,
-                                                                             t_out);
-  if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
-
-  // fused row pass: ch chunks per lane and wpr warps per row, chosen to cover the
-  // row's 16-byte chunks with the least padding (ties: 4 chunks per lane;
-  // K <= 16384 fits 16 warps x 4 chunks); CTAs of about 8 warps, as many per
-  // SM as fit in 16 warps; persistent over row groups
-  const int nchunk = int(K / 8);
-  int ch = 1, wpr = (nchunk + 31) / 32, waste = wpr * 32 - nchunk;
-  for (int c : {2, 8, 4}) {
-    const int w = (nchunk + 32 * c - 1) / (32 * c);
-    const int x = w * 32 * c - nchunk;
-    if (w <= kMaxRowWarps && (wpr > kMaxRowWarps || x < waste || (x == waste && c == 4))) {
-      ch = c;
-      wpr = w;
-      waste = x;
-    }
+  RowCallParams prm;
+  prm.A = static_cast<const uint16_t*>(A);
+  prm.M = M;
+  prm.K = int(K);
+  prm.lda = lda;
+  prm.k_rank = n - outlier_max_nnz(M, K, q);
+  prm.g_pilot = reinterpret_cast<uint32_t*>(ws + L.hist);
+  prm.g_main = reinterpret_cast<uint32_t*>(ws + L.hist2);
+  prm.fctrl = reinterpret_cast<FCtrl*>(ws + L.fctrl);
+  prm.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+  prm.cta_total = reinterpret_cast<int64_t*>(ws + L.cta_total);
+  prm.row_cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
+  prm.scol = reinterpret_cast<int32_t*>(ws + L.scol);
+  prm.sval = reinterpret_cast<float*>(ws + L.sval);
+  prm.t_out = t_out;
+  prm.row_ptr = row_ptr;
+  prm.col_idx = col_idx;
+  prm.vals = vals;
+  prm.cap = nnz_capacity;
+  prm.nnz_out = nnz_out;
+  prm.A_c = static_cast<uint16_t*>(A_clamped);
+  prm.ldac = ldac;
+  prm.codes = codes;
+  prm.ldc = ldc;
+  prm.scales = scales;
+  prm.status = status_word();
+  prm.wait_ns = kWaitLimitNs;
+  // one CTA per SM (every CTA resident: the grid barriers need it)
+  int grid = sms < kMaxCtas ? sms : kMaxCtas;
+  prm.n_pilot = 0;
+  for (int c = 0; c < grid; ++c) {
+    const int64_t a = M * c / grid, b = M * (c + 1) / grid;
+    prm.n_pilot += (b - a + kPilotStride - 1) / kPilotStride * K;
   }
-  const int rows_per_cta = wpr >= 8 ? 1 : 8 / wpr;
-  const int ctas_per_sm = kMaxRowWarps / (wpr * rows_per_cta) > 0 ? kMaxRowWarps / (wpr * rows_per_cta) : 1;
-  const unsigned threads = unsigned(32 * wpr * rows_per_cta);
-  int64_t rblocks = (M + rows_per_cta - 1) / rows_per_cta;
-  if (rblocks > int64_t(sms) * ctas_per_sm) rblocks = int64_t(sms) * ctas_per_sm;
-  if (codes)
-    launch_rows_outlier<true>(ch, wpr, unsigned(rblocks), threads, s, a, M, int(K), lda, ctrl, t_out, row_cnt, scol,
-                              sval, static_cast<uint16_t*>(A_clamped), ldac, codes, ldc, scales);
-  else
-    launch_rows_outlier<false>(ch, wpr, unsigned(rblocks), threads, s, a, M, int(K), lda, ctrl, t_out, row_cnt, scol,
-                               sval, static_cast<uint16_t*>(A_clamped), ldac, nullptr, 0, nullptr);
-  if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
-  row_scan_kernel<<<1, 1024, 0, s>>>(row_cnt, M, row_ptr, nnz_out, ctrl, nnz_capacity, status);
-  if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
-  if (nnz_capacity > 0) {
-    int64_t gblocks = (M + 7) / 8;
-    if (gblocks > int64_t(sms) * 8) gblocks = int64_t(sms) * 8;
-    gather_kernel<<<unsigned(gblocks), 256, 0, s>>>(row_cnt, row_ptr, M, scol, sval, a, int(K), lda, ctrl, t_out,
-                                                    col_idx, vals, nnz_capacity);
-    if (launch_status() != FP4_OK) return FP4_ERR_CUDA;
-  }
-  return FP4_OK;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kRThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, rowcall_kernel, prm) != cudaSuccess) return launch_status();
+  return launch_status();
 }
 
 fp4_status validate_outlier_args(const void* A, int64_t M, int64_t K, int64_t lda, double q, const float* t_out,

@@ -610,3 +610,36 @@ def test_wide_gemm_raw_and_scaled(fp4, M, N, K):
     yf = fp4.fp4_linear_fwd(da, torch.from_numpy(s_a).cuda(), dw, torch.from_numpy(s_w).cuda(), K, out_type="fp32")
     np.testing.assert_allclose(yf[torch.from_numpy(rows).cuda()].cpu().numpy(), y_ref, rtol=2.0 ** -21, atol=0)
     assert_no_device_flags(fp4)
+
+
+def test_outlier_pilot_misled_by_its_sample(fp4):
+    """The row call draws a floor under the threshold from every 64th row of each
+    CTA's row block (a pilot).  Here exactly those rows hold values 100 times
+    larger, so the floor lands above the true threshold and the call must count
+    the magnitudes below it in a second pass; t, the CSR and the codes stay
+    bit-exact."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, K, q = 32 * sms, 512, 0.999
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    sampled = np.zeros(M, bool)
+    for b in range(sms):
+        r0, r1 = M * b // sms, M * (b + 1) // sms
+        sampled[r0:r1:64] = True
+    x[sampled] *= np.float32(100.0)
+    A_bits = wl.f32_to_bf16_bits(x)
+    o = fp4.fp4_quantize_rows_outliers(dev_bf16(A_bits), q)
+    t, t_bits, k = orc.quantile_threshold(A_bits, q)
+    A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
+    # the true threshold lies among the large rows, and with 4x the exceedance
+    # the pilot's floor is above it (the second pass is needed)
+    assert float(o["t"].item()) == float(t)
+    assert np.array_equal(o["row_ptr"].cpu().numpy(), rp)
+    nnz = int(o["nnz"].item())
+    assert nnz == rp[-1]
+    assert np.array_equal(o["col_idx"][:nnz].cpu().numpy(), ci)
+    assert np.array_equal(o["vals"][:nnz].cpu().numpy().view(np.uint32), cv.view(np.uint32))
+    ref_codes, ref_s = orc.quantize_rows(A_c)
+    assert np.array_equal(o["codes"].cpu().numpy(), ref_codes)
+    assert np.array_equal(o["scales"].cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
+    assert_no_device_flags(fp4)
