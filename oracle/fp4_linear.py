@@ -41,6 +41,8 @@ R3 the sign of a value that rounds to zero is kept (code 0x8); R4 a zero or
    R11 accumulation and outputs in fp32 / BF16 (the pages' FP16 output is the
    authors' emulation detail); R12 element 2c of a row goes in the low nibble;
    R16 the input gradient (absent from the pages) is dY W^T with the BF16 W.
+R17 the FP8 weight gradient for communication is E4M3 with one per-tensor
+   scale from the caller, round half to even, saturating at 448.
 
 Precision: fp64 wherever the pages fix no precision.  The quantizer itself
 works in fp32 because its definition (R1) is an fp32 division and multiply.
@@ -400,6 +402,65 @@ def wgrad_dge(A_bits, dY_bits, W_bits, s_w, k: float, clip: float,
     W = bf16_to_f32(np.asarray(W_bits)[np.ix_(rows, cols)])
     x = np.abs(W * np.asarray(s_w, dtype=np.float32)[cols][None, :]).astype(np.float64)
     return (G * dge_derivative(x, k, clip)).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) weight gradient, for gradient communication
+# --------------------------------------------------------------------------
+# Page 1, mixed-precision passage: the framework communicates gradients in FP8.
+# The pages name neither the FP8 variant nor its scaling.  Reading R17: E4M3
+# (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no infinities, the
+# all-ones pattern S.1111.111 is NaN, so the largest finite magnitude is
+# 1.75 * 2^8 = 448), one per-tensor fp32 scale s supplied by the caller
+# (code = E4M3(fl32(dW * s)), dW ~ decode(code) / s), round half to the even
+# mantissa, magnitudes above 448 saturate to 448, and max |dW| is returned so
+# the caller can form the next step's scale (delayed per-tensor scaling).
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one E4M3 byte from its bit fields (NaN for S.1111.111)."""
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** -6          # subnormal: 0.m x 2^(1 - 7)
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def e4m3_encode(y: np.ndarray) -> np.ndarray:
+    """E4M3 byte of each finite y (fp32 or fp64): nearest value, ties to the
+    even mantissa, |y| above 448 gives 448, the sign kept for values that round
+    to zero.  Works on the binary exponent, so every step is exact in fp64."""
+    y = np.asarray(y, dtype=np.float64)
+    assert np.all(np.isfinite(y)), "finite inputs only"
+    a = np.abs(y)
+    _, ex = np.frexp(a)                             # a = f 2^ex, f in [0.5, 1)
+    e = np.maximum(ex - 1, -6)                      # unbiased exponent, subnormals share -6
+    q = np.rint(a * np.exp2(3 - e))                 # mantissa units of 2^(e-3), half to even
+    # q in [8, 16] for normals (16: carried into the next binade), [0, 8] below 2^-6
+    carry = q >= 16
+    e = np.where(carry, e + 1, e)
+    q = np.where(carry, 8, q)
+    normal = q >= 8
+    mag = np.where(normal, ((e + 7) << 3) + (q - 8), q).astype(np.int64)
+    # the magnitude pattern grows with the value, so past 448 (0x7E) it is cut
+    # to 448 (0x7F would be NaN)
+    mag = np.minimum(mag, 0x7E)
+    return (mag | np.where(np.signbit(y), 0x80, 0)).astype(np.uint8)
+
+
+def wgrad_dge_fp8(dW32: np.ndarray, scale: float) -> Tuple[np.ndarray, np.float32]:
+    """E4M3 codes of fl32(dW * scale) and max |dW| (fp32), per reading R17.
+
+    dW32 is the fp32 weight gradient (wgrad_dge); the product with the
+    per-tensor scale is one fp32 multiply, rounded to nearest."""
+    dW32 = np.asarray(dW32, dtype=np.float32)
+    y = dW32 * np.float32(scale)
+    return e4m3_encode(y), np.float32(np.max(np.abs(dW32))) if dW32.size else np.float32(0)
 
 
 # --------------------------------------------------------------------------

@@ -211,3 +211,43 @@ def test_magnitude_with_wrong_row_under_subset_is_caught(monkeypatch):
         return t1
     monkeypatch.setattr(orc, "linear_fwd_magnitude", _magnitude_with(body))
     _expect_failure(pins.test_fwd_magnitude_invariants)
+
+
+def test_e4m3_ties_away_and_missing_saturation_are_caught(monkeypatch):
+    real = orc.e4m3_encode
+
+    def ties_away(y):
+        y = np.asarray(y, dtype=np.float64)
+        c = real(y)
+        # where y sits exactly halfway between two codes, take the larger magnitude
+        lo = np.array([abs(orc.e4m3_decode(int(v))) for v in c.ravel()]).reshape(c.shape)
+        nxt = np.array([abs(orc.e4m3_decode(int(v & 0x7F) + 1)) if (v & 0x7F) < 0x7E else np.inf
+                        for v in c.ravel()]).reshape(c.shape)
+        tie = np.abs(y) == (lo + nxt) / 2
+        return np.where(tie, c + 1, c).astype(np.uint8)
+
+    monkeypatch.setattr(orc, "e4m3_encode", ties_away)
+    _expect_failure(pins.test_e4m3_golden_ties_and_saturation)
+    _expect_failure(pins.test_e4m3_encode_exact_rational_on_values_midpoints_and_neighbours)
+
+    def no_saturation(y):
+        c = real(y)
+        big = np.abs(np.asarray(y, dtype=np.float64)) > 464.0
+        return np.where(big, c | 0x7F, c).astype(np.uint8)
+
+    monkeypatch.setattr(orc, "e4m3_encode", no_saturation)
+    _expect_failure(pins.test_e4m3_golden_ties_and_saturation)
+    _expect_failure(pins.test_e4m3_encode_exact_rational_on_values_midpoints_and_neighbours)
+    monkeypatch.setattr(orc, "e4m3_encode", real)
+
+
+def test_e4m3_wrong_exponent_bias_is_caught(monkeypatch):
+    real = orc.e4m3_decode
+    monkeypatch.setattr(orc, "e4m3_decode", lambda c: real(c) * 2.0)       # bias 6 instead of 7
+    _expect_failure(pins.test_e4m3_decode_closed_form)
+    monkeypatch.setattr(orc, "e4m3_decode", real)
+    real_enc = orc.e4m3_encode
+    monkeypatch.setattr(orc, "e4m3_encode", lambda y: real_enc(np.asarray(y, dtype=np.float64) / 2.0))
+    _expect_failure(pins.test_e4m3_encode_exact_rational_on_values_midpoints_and_neighbours)
+    _expect_failure(pins.test_e4m3_encode_matches_torch_float8_in_range)
+    monkeypatch.setattr(orc, "e4m3_encode", real_enc)

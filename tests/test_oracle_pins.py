@@ -522,3 +522,93 @@ def test_dgrad_sampled_rows_cols_match_full():
     full = orc.linear_dgrad(dY_bits, W_bits)
     rows, cols = [0, 7, 19], [11, 2]
     assert np.array_equal(orc.linear_dgrad(dY_bits, W_bits, rows=rows, cols=cols), full[np.ix_(rows, cols)])
+
+
+# ---------------------------------------------------------------- E4M3 (FP8 weight gradient)
+
+def _e4m3_values_exact():
+    """Finite non-negative E4M3 values as exact rationals, indexed by code 0..126:
+    subnormals m/8 2^-6, normals (1 + m/8) 2^(e-7), e = 1..15 (code 127 is NaN)."""
+    vals = []
+    for c in range(127):
+        e, m = c >> 3, c & 7
+        vals.append(Fraction(m, 8) * Fraction(1, 64) if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7))
+    return vals
+
+
+def _e4m3_nearest_exact(y: float) -> int:
+    """Nearest finite E4M3 value by exact rational distance, ties to the even
+    mantissa, magnitudes past 448 saturated, the sign bit from y."""
+    vals = _e4m3_values_exact()
+    mag = abs(Fraction(float(y)))
+    if mag >= vals[-1]:
+        c = 126
+    else:
+        hi = next(i for i, v in enumerate(vals) if v >= mag)
+        lo = max(hi - 1, 0)
+        dlo, dhi = mag - vals[lo], vals[hi] - mag
+        c = lo if dlo < dhi else hi if dhi < dlo else (lo if lo % 2 == 0 else hi)
+    return c | (0x80 if math.copysign(1.0, y) < 0 else 0)
+
+
+def test_e4m3_decode_closed_form():
+    vals = [orc.e4m3_decode(c) for c in range(256)]
+    assert sum(math.isnan(v) for v in vals) == 2                      # S.1111.111 only
+    assert max(v for v in vals if not math.isnan(v)) == 448.0
+    assert orc.e4m3_decode(0x38) == 1.0 and orc.e4m3_decode(0x01) == 2.0 ** -9
+    assert orc.e4m3_decode(0x08) == 2.0 ** -6 and orc.e4m3_decode(0x07) == 7 * 2.0 ** -9
+    exact = _e4m3_values_exact()
+    for c in range(127):
+        assert Fraction(orc.e4m3_decode(c)) == exact[c]
+        assert orc.e4m3_decode(c | 0x80) == -orc.e4m3_decode(c)
+
+
+def test_e4m3_encode_exact_rational_on_values_midpoints_and_neighbours():
+    exact = _e4m3_values_exact()
+    pts = []
+    for i in range(126):
+        mid = (exact[i] + exact[i + 1]) / 2
+        for v in (exact[i], mid):
+            f = float(v)
+            pts += [f, np.nextafter(f, 0.0), np.nextafter(f, np.inf)]
+    pts += [448.0, 464.0, np.nextafter(464.0, 0.0), 465.0, 480.0, 1e4, 3.0e38, 0.0, 2.0 ** -11, 2.0 ** -10]
+    x = np.array(pts + [-p for p in pts], dtype=np.float64)
+    got = orc.e4m3_encode(x)
+    want = np.array([_e4m3_nearest_exact(v) for v in x], dtype=np.uint8)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_e4m3_golden_ties_and_saturation():
+    # midpoints go to the even mantissa; everything at or past 448 stays at 448
+    cases = {1 + 1 / 16: 0x38, 1 + 3 / 16: 0x3A, 2.0 ** -10: 0x00, 3 * 2.0 ** -10: 0x02,
+             464.0: 0x7E, 1e9: 0x7E, -1e9: 0xFE, -0.0: 0x80, -2.0 ** -12: 0x80, 240.0: 0x77}
+    got = orc.e4m3_encode(np.array(list(cases), dtype=np.float64))
+    assert [int(c) for c in got] == list(cases.values())
+
+
+def test_e4m3_encode_matches_torch_float8_in_range():
+    """torch's float8_e4m3fn conversion rounds to nearest even but does not
+    saturate, so the comparison stays below the saturation midpoint 464."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(200000) * np.exp2(rng.uniform(-14, 9, 200000))).astype(np.float32)
+    x = x[np.abs(x) < 464.0]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(orc.e4m3_encode(x), ref)
+
+
+def test_wgrad_fp8_is_scaled_encode_of_the_fp32_gradient():
+    rng = np.random.default_rng(8)
+    dW = (rng.standard_normal((7, 9)) * 1e-3).astype(np.float32)
+    s = 448.0 / float(np.max(np.abs(dW)))
+    codes, amax = orc.wgrad_dge_fp8(dW, s)
+    assert amax == np.max(np.abs(dW))
+    y = dW * np.float32(s)                                   # one fp32 multiply
+    assert [int(c) for c in codes.ravel()] == [_e4m3_nearest_exact(float(v)) for v in y.ravel()]
+    deq = np.array([orc.e4m3_decode(int(c)) for c in codes.ravel()]).reshape(dW.shape) / s
+    # relative spacing of E4M3 is 2^-3, so the rounding error is at most 2^-4 relative
+    # (normals) or 2^-10 / s absolute (subnormals)
+    assert np.all(np.abs(deq - dW) <= np.maximum(np.abs(dW) * 2.0 ** -4, 2.0 ** -10 / s) * (1 + 1e-6))
+    assert codes[np.unravel_index(np.argmax(np.abs(dW)), dW.shape)] & 0x7F == 0x7E
