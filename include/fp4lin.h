@@ -65,6 +65,13 @@ typedef enum fp4_out_type {
   FP4_OUT_RAW_ACC_FP32 = 2 /* the unscaled FP4 accumulator sum_k qA*qW in fp32; no scales, no compensation */
 } fp4_out_type;
 
+/* Element type of the weight gradient written by fp4_linear_wgrad_dge. */
+typedef enum fp4_dw_type {
+  FP4_DW_FP32 = 0,  /* dW in fp32 */
+  FP4_DW_E4M3 = 1   /* E4M3 codes of fl32(dW * scale), one byte each: the FP8 gradient
+                       for communication (page "首个 FP4 ...", mixed-precision passage) */
+} fp4_dw_type;
+
 /* Sticky device flags reported by fp4_device_status. */
 #define FP4_FLAG_TIMEOUT 0x1u  /* an mbarrier wait in a GEMM ran past its limit */
 #define FP4_FLAG_CAPACITY 0x2u /* the CSR staging area was too small */
@@ -292,21 +299,36 @@ fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_bytes, const
  *   W   device BF16 K x ldw, s_w device fp32 N (from fp4_quantize_cols)
  *   M, N, K  M >= 1; N % 8 == 0; K % 8 == 0; all < 2^31
  *   dge_k > 0, dge_clip > 0
- *   dW  device fp32 K x lddw, 16-byte aligned, lddw % 4 == 0; written once per
- *       element while other tiles still read W and s_w, so dW must not alias
- *       A, dY, W or s_w
+ *   dW  device K x lddw, 16-byte aligned, lddw % 4 == 0, of the element type
+ *       dw_type gives; written once per element while other tiles still read
+ *       W and s_w, so dW must not alias A, dY, W or s_w
+ *   dw_type   FP4_DW_FP32, or FP4_DW_E4M3: the page says gradients are
+ *       communicated in FP8 and names neither the variant nor the scaling;
+ *       the reading taken is E4M3 (bias 7, 3 mantissa bits, largest finite
+ *       448) with one per-tensor scale: dW8[r,j] = E4M3(fl32(dW[r,j] * scale)),
+ *       round half to the even mantissa, magnitudes past 448 saturate to 448,
+ *       a value that rounds to zero keeps its sign; dW ~ decode(dW8) / scale
+ *   dw_scale  E4M3 only: device fp32 scalar, the per-tensor scale (read on the
+ *       device, so it may be produced by an earlier kernel); NULL for fp32
+ *   dw_amax   E4M3 only: device fp32 scalar, set to max |dW| over the whole
+ *       gradient (before scaling; zeroed on the stream first, then raised with
+ *       atomics), e.g. to derive the next step's scale 448 / amax; must not
+ *       overlap dW; NULL for fp32
  *   workspace  device, 256-byte aligned, ws_bytes >= fp4_linear_wgrad_dge_workspace(M, N, K),
  *       or NULL.  With it, a last wave of tiles that would leave at least half
  *       of the SM pairs idle is computed as two halves of the token range on
  *       two pairs, combined through the workspace (the result is the same
  *       whichever half finishes first).  Must not be shared by calls that may
  *       run at the same time; owned by the caller.
- * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE (non-NULL and too small),
+ * Errors: INVALID_ARG (also: an unknown dw_type, E4M3 without dw_scale or
+ *         dw_amax, dw_amax inside dW), SHAPE, ALIGNMENT (also: dw_scale or
+ *         dw_amax not 4-byte aligned), WORKSPACE (non-NULL and too small),
  *         DEVICE_UNSUPPORTED, CUDA; device-side TIMEOUT flag as for fp4_linear_fwd.
  */
 fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* dY, int64_t lddy, const void* W,
                                 int64_t ldw, const float* s_w, int64_t M, int64_t N, int64_t K,
-                                float dge_k, float dge_clip, float* dW, int64_t lddw,
+                                float dge_k, float dge_clip, void* dW, int dw_type, int64_t lddw,
+                                const float* dw_scale, float* dw_amax,
                                 void* workspace, size_t ws_bytes, fp4_stream_t stream);
 
 /*

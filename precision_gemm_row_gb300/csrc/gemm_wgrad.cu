@@ -59,15 +59,29 @@ __device__ __forceinline__ float dge_factor(float x, const DgeConst& c) {
   return x < 6.0f ? fu : c.inv_k;
 }
 
-// dW[k, n] = G[k, n] * f'(|fl32(W[k, n] s_W[n])|), fp32.
+// Two E4M3 bytes of fl32 values (lo at the lower address), round to nearest
+// even, magnitudes past 448 saturated to 448.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// dW[k, n] = G[k, n] * f'(|fl32(W[k, n] s_W[n])|): fp32, or (FP8) the E4M3
+// codes of fl32(dW * scale) with max |dW| kept per thread (amax) and folded
+// into *amax_out at the end of the kernel (finish).
+template <bool FP8>
 struct DgeEpilogue {
   const uint16_t* W;
   int64_t ldw;
   const float* s_w;
-  float* dW;
+  void* dW;
   int64_t lddw;
   int rows, cols;   // K, N
   DgeConst dge;
+  const float* scale;   // FP8: device, per-tensor
+  float* amax_out;      // FP8: device, zeroed before the launch
+  mutable float amax;   // FP8: this thread's max |dW| so far
 
   // W rows row0..row0+31 (columns col0..col0+63: one 128-byte line per row)
   // and s_w[col0..col0+63] (two lines) into L2
@@ -98,15 +112,39 @@ struct DgeEpilogue {
     const float f1 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(pr.w[i].x >> 16), pr.sw.y)), dge);
     const float f2 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(pr.w[i].y & 0xFFFFu), pr.sw.z)), dge);
     const float f3 = dge_factor(fabsf(__fmul_rn(bf16_bits_to_float(pr.w[i].y >> 16), pr.sw.w)), dge);
-    *reinterpret_cast<float4*>(dW + int64_t(grow) * lddw + gcol) = make_float4(g.x * f0, g.y * f1, g.z * f2, g.w * f3);
+    const float4 d = make_float4(g.x * f0, g.y * f1, g.z * f2, g.w * f3);
+    if constexpr (FP8) {
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(d.x), fabsf(d.y)), fmaxf(fabsf(d.z), fabsf(d.w))));
+      const float sc = __ldg(scale);
+      const uint32_t q = e4m3x2(__fmul_rn(d.x, sc), __fmul_rn(d.y, sc)) |
+                         (e4m3x2(__fmul_rn(d.z, sc), __fmul_rn(d.w, sc)) << 16);
+      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(dW) + int64_t(grow) * lddw + gcol) = q;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(dW) + int64_t(grow) * lddw + gcol) = d;
+    }
+  }
+
+  // every thread of the block, after the engine: one atomic per warp
+  __device__ __forceinline__ void finish() const {
+    if constexpr (FP8) {
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax));   // amax >= 0: order of bits
+      if ((threadIdx.x & 31) == 0 && m != 0u) atomicMax(reinterpret_cast<unsigned int*>(amax_out), m);
+    }
   }
 };
 
-template <bool PAIR>
+template <bool PAIR, bool FP8>
 __global__ void __launch_bounds__(bwd::kThreads, 1)
     wgrad_dge_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
-                     const bwd::Shape s, const DgeEpilogue e) {
-  bwd::run<false, PAIR>(tmA, tmG, s, e);
+                     const bwd::Shape s, const DgeEpilogue<FP8> e) {
+  if constexpr (FP8) {
+    DgeEpilogue<FP8> el = e;   // a per-thread copy carries the running max
+    el.amax = 0.0f;
+    bwd::run<false, PAIR>(tmA, tmG, s, el);
+    el.finish();
+  } else {
+    bwd::run<false, PAIR>(tmA, tmG, s, e);
+  }
 }
 
 }  // namespace
@@ -114,11 +152,16 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
 
 FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* dY, int64_t lddy, const void* W,
                                         int64_t ldw, const float* s_w, int64_t M, int64_t N, int64_t K, float dge_k,
-                                        float dge_clip, float* dW, int64_t lddw, void* workspace, size_t ws_bytes,
-                                        fp4_stream_t stream) {
+                                        float dge_clip, void* dW, int dw_type, int64_t lddw, const float* dw_scale,
+                                        float* dw_amax, void* workspace, size_t ws_bytes, fp4_stream_t stream) {
   using namespace fp4;
   if (!A || !dY || !W || !s_w || !dW) return FP4_ERR_INVALID_ARG;
   if (!(dge_k > 0.0f) || !(dge_clip > 0.0f) || !isfinite(dge_k)) return FP4_ERR_INVALID_ARG;
+  if (dw_type != FP4_DW_FP32 && dw_type != FP4_DW_E4M3) return FP4_ERR_INVALID_ARG;
+  const bool fp8 = dw_type == FP4_DW_E4M3;
+  if (fp8 && (!dw_scale || !dw_amax)) return FP4_ERR_INVALID_ARG;
+  if (fp8 && ((reinterpret_cast<uintptr_t>(dw_scale) & 3u) || (reinterpret_cast<uintptr_t>(dw_amax) & 3u)))
+    return FP4_ERR_ALIGNMENT;
   if (M < 1 || N < 8 || K < 8 || N % 8 || K % 8 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) ||
       K >= (int64_t(1) << 31))
     return FP4_ERR_SHAPE;
@@ -136,7 +179,13 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   st = encode_tmap_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, uint64_t(N), uint64_t(M), uint64_t(lddy) * 2,
                       bwd::kBox, bwd::kBT, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st != FP4_OK) return st;
-  DgeEpilogue e;
+  if (fp8) {
+    // the running maximum must not land in dW (it is zeroed before the launch)
+    const uintptr_t d0 = reinterpret_cast<uintptr_t>(dW), d1 = d0 + uintptr_t((K - 1) * lddw + N);
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(dw_amax);
+    if (a0 + sizeof(float) > d0 && a0 < d1) return FP4_ERR_INVALID_ARG;
+  }
+  DgeEpilogue<false> e;
   e.W = static_cast<const uint16_t*>(W);
   e.ldw = ldw;
   e.s_w = s_w;
@@ -160,8 +209,29 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   st = bwd::schedule(s, bwd::plan_split(K, N, M, sms), workspace, ws_bytes, cs);
   if (st != FP4_OK) return st;
-  if (bwd::use_pairs(M)) return bwd::launch<false, true>(wgrad_dge_kernel<true>, s, sms, cs, tmA, tmG, s, e);
-  return bwd::launch<false, false>(wgrad_dge_kernel<false>, s, sms, cs, tmA, tmG, s, e);
+  const bool pairs = bwd::use_pairs(M);
+  if (!fp8) {
+    e.scale = nullptr;
+    e.amax_out = nullptr;
+    e.amax = 0.0f;
+    if (pairs) return bwd::launch<false, true>(wgrad_dge_kernel<true, false>, s, sms, cs, tmA, tmG, s, e);
+    return bwd::launch<false, false>(wgrad_dge_kernel<false, false>, s, sms, cs, tmA, tmG, s, e);
+  }
+  DgeEpilogue<true> e8;
+  e8.W = e.W;
+  e8.ldw = e.ldw;
+  e8.s_w = e.s_w;
+  e8.dW = e.dW;
+  e8.lddw = e.lddw;
+  e8.rows = e.rows;
+  e8.cols = e.cols;
+  e8.dge = e.dge;
+  e8.scale = dw_scale;
+  e8.amax_out = dw_amax;
+  e8.amax = 0.0f;
+  if (cudaMemsetAsync(dw_amax, 0, sizeof(float), cs) != cudaSuccess) return launch_status();
+  if (pairs) return bwd::launch<false, true>(wgrad_dge_kernel<true, true>, s, sms, cs, tmA, tmG, s, e8);
+  return bwd::launch<false, false>(wgrad_dge_kernel<false, true>, s, sms, cs, tmA, tmG, s, e8);
 }
 
 FP4_API size_t fp4_linear_wgrad_dge_workspace(int64_t M, int64_t N, int64_t K) {

@@ -65,7 +65,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "fp4_linear_fwd": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp,
                                     _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_sz, _c_vp]),
         "fp4_linear_wgrad_dge": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64,
-                                          _c_i64, _c_f, _c_f, _c_vp, _c_i64, _c_vp, _c_sz, _c_vp]),
+                                          _c_i64, _c_f, _c_f, _c_vp, _c_int, _c_i64, _c_vp, _c_vp, _c_vp, _c_sz,
+                                          _c_vp]),
         "fp4_linear_wgrad_dge_workspace": (_c_sz, [_c_i64, _c_i64, _c_i64]),
         "fp4_linear_dgrad": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64,
                                       _c_vp, _c_sz, _c_vp]),
@@ -343,24 +344,46 @@ def fp4_linear_dgrad_workspace(M: int, N: int, K: int) -> int:
     return int(_lib.fp4_linear_dgrad_workspace(M, N, K))
 
 
+DW_TYPES = {"fp32": 0, "e4m3": 1}
+
+
 def fp4_linear_wgrad_dge(A: torch.Tensor, dY: torch.Tensor, W: torch.Tensor, s_w: torch.Tensor,
                          dge_k: float = 5.0, dge_clip: float = 3.0, dW: Optional[torch.Tensor] = None,
-                         workspace="auto", stream=None) -> torch.Tensor:
-    """dW = (A^T dY) * f'(|W s_W|), fp32 (K x N).  workspace: see _bwd_workspace."""
+                         workspace="auto", stream=None, dw_type: str = "fp32",
+                         dw_scale: Optional[torch.Tensor] = None, dw_amax: Optional[torch.Tensor] = None):
+    """dW = (A^T dY) * f'(|W s_W|) (K x N).  workspace: see _bwd_workspace.
+
+    dw_type "fp32" returns dW in fp32.  dw_type "e4m3" returns (codes, amax):
+    codes K x N uint8 = E4M3(fl32(dW * scale)) with dw_scale a 1-element fp32
+    device tensor, and amax the 1-element fp32 tensor max |dW|."""
+    if dw_type not in DW_TYPES:
+        raise ValueError(f"dw_type must be one of {sorted(DW_TYPES)}")
+    fp8 = dw_type == "e4m3"
     lda = _rowmajor(A, "A", torch.bfloat16)
     M, K = A.shape
     N = dY.shape[1]
     lddy = _mat(dY, "dY", torch.bfloat16, M, N, A.device)
     ldw = _mat(W, "W", torch.bfloat16, K, N, A.device)
     _vec(s_w, "s_w", torch.float32, N, A.device)
+    out_dtype = torch.uint8 if fp8 else torch.float32
     if dW is None:
-        dW = torch.empty((K, N), dtype=torch.float32, device=A.device)
-    lddw = _mat(dW, "dW", torch.float32, K, N, A.device)
+        dW = torch.empty((K, N), dtype=out_dtype, device=A.device)
+    lddw = _mat(dW, "dW", out_dtype, K, N, A.device)
+    if fp8:
+        if dw_scale is None:
+            raise ValueError("dw_type 'e4m3' needs dw_scale (a 1-element fp32 device tensor)")
+        _vec(dw_scale, "dw_scale", torch.float32, 1, A.device)
+        if dw_amax is None:
+            dw_amax = torch.empty(1, dtype=torch.float32, device=A.device)
+        _vec(dw_amax, "dw_amax", torch.float32, 1, A.device)
+    elif dw_scale is not None or dw_amax is not None:
+        raise ValueError("dw_scale / dw_amax apply to dw_type 'e4m3' only")
     ws, ws_bytes = _bwd_workspace(workspace, fp4_linear_wgrad_dge_workspace(M, N, K), A.device)
     _check("fp4_linear_wgrad_dge", _lib.fp4_linear_wgrad_dge(
-        _p(A), lda, _p(dY), lddy, _p(W), ldw, _p(s_w), M, N, K, float(dge_k), float(dge_clip), _p(dW), lddw,
+        _p(A), lda, _p(dY), lddy, _p(W), ldw, _p(s_w), M, N, K, float(dge_k), float(dge_clip), _p(dW),
+        DW_TYPES[dw_type], lddw, _p(dw_scale) if fp8 else None, _p(dw_amax) if fp8 else None,
         _p(ws), ws_bytes, _s(stream)))
-    return dW
+    return (dW, dw_amax) if fp8 else dW
 
 
 def fp4_linear_dgrad(dY: torch.Tensor, W: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16,

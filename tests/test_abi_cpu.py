@@ -120,7 +120,15 @@ def test_host_validation_rejects_bad_arguments_without_launching(lib):
     assert L.fp4_linear_fwd(fake, 32, fake, fake, 32, fake, 4, 8, 64, fake, fake, fake, fake, 8, fake, 0, 8,
                             fake, 16, None) == 4
     # DGE parameters
-    assert L.fp4_linear_wgrad_dge(fake, 64, fake, 8, fake, 8, fake, 4, 8, 64, 0.0, 3.0, fake, 8, None, 0, None) == 1
+    assert L.fp4_linear_wgrad_dge(fake, 64, fake, 8, fake, 8, fake, 4, 8, 64, 0.0, 3.0, fake, 0, 8, None, None, None, 0,
+                                  None) == 1
+    # unknown dW type; E4M3 without its scale or running maximum
+    assert L.fp4_linear_wgrad_dge(fake, 64, fake, 8, fake, 8, fake, 4, 8, 64, 5.0, 3.0, fake, 2, 8, None, None, None, 0,
+                                  None) == 1
+    assert L.fp4_linear_wgrad_dge(fake, 64, fake, 8, fake, 8, fake, 4, 8, 64, 5.0, 3.0, fake, 1, 8, None, fake, None, 0,
+                                  None) == 1
+    assert L.fp4_linear_wgrad_dge(fake, 64, fake, 8, fake, 8, fake, 4, 8, 64, 5.0, 3.0, fake, 1, 8, fake, None, None, 0,
+                                  None) == 1
     # input gradient: raw accumulator is not an output type; ragged N; misaligned leading dimension
     assert L.fp4_linear_dgrad(fake, 64, fake, 64, 4, 64, 16, fake, 2, 16, None, 0, None) == 1
     assert L.fp4_linear_dgrad(None, 64, fake, 64, 4, 64, 16, fake, 0, 16, None, 0, None) == 1

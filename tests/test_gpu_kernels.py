@@ -643,3 +643,78 @@ def test_outlier_pilot_misled_by_its_sample(fp4):
     assert np.array_equal(o["codes"].cpu().numpy(), ref_codes)
     assert np.array_equal(o["scales"].cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
     assert_no_device_flags(fp4)
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) weight gradient
+
+def _small_int_bits(seed, shape, lim):
+    """BF16 patterns of integers in [-lim, lim]: sums of their products are exact in fp32."""
+    rng = np.random.default_rng(seed)
+    return wl.f32_to_bf16_bits(rng.integers(-lim, lim + 1, size=shape).astype(np.float32))
+
+
+@pytest.mark.parametrize("M,K,N", [(300, 136, 264), (2100, 264, 136)])
+@pytest.mark.parametrize("headroom", [1.0, 4.0])
+@pytest.mark.parametrize("workspace", ["auto", None])
+def test_wgrad_fp8_bit_exact_when_the_gradient_is_exact(fp4, M, K, N, headroom, workspace):
+    """With k = 1 the DGE factor is exactly 1, and integer-valued A and dY make
+    every sum exact in fp32, so dW is exact on both sides and the E4M3 codes
+    must match the oracle's bit for bit: round half to even, sign of zero, and
+    (headroom 4: the scale is 4x 448 / amax) saturation at 448.  M = 2100 runs
+    CTA pairs and, with a workspace, the split tail."""
+    A_bits = _small_int_bits(M, (M, K), 3)
+    dY_bits = _small_int_bits(N + 1, (M, N), 2)
+    W_bits = _normal_bits(K + 3, (K, N), 0.02)
+    _, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+    ref32 = orc.wgrad_dge(A_bits, dY_bits, W_bits, s_w, 1.0, 3.0)
+    scale = np.float32(headroom * 448.0 / float(np.max(np.abs(ref32))))
+    ref_codes, ref_amax = orc.wgrad_dge_fp8(ref32, float(scale))
+    codes, amax = fp4.fp4_linear_wgrad_dge(dev_bf16(A_bits), dev_bf16(dY_bits), dev_bf16(W_bits),
+                                           torch.from_numpy(s_w).cuda(), 1.0, 3.0, workspace=workspace,
+                                           dw_type="e4m3", dw_scale=torch.tensor([float(scale)], dtype=torch.float32, device="cuda"))
+    np.testing.assert_array_equal(codes.cpu().numpy(), ref_codes)
+    assert float(amax.item()) == float(ref_amax)
+    if headroom > 1:
+        assert np.count_nonzero((ref_codes & 0x7F) == 0x7E) > 0
+    assert_no_device_flags(fp4)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 8, 8), (1000, 392, 520), (4100, 384, 136)])
+def test_wgrad_fp8_within_one_code_of_the_oracle(fp4, M, K, N):
+    """With the DGE factor (k = 5) the fp32 gradient differs from the oracle's
+    fp64 one in the last bits, so a code may differ by one step where fl32(dW s)
+    lies next to a rounding boundary; every code is within one step of the
+    oracle's, nearly all are equal, and amax agrees to fp32 rounding."""
+    A_bits = _normal_bits(M + 1, (M, K))
+    dY_bits = _normal_bits(N + 2, (M, N), 1e-3)
+    W_bits = _normal_bits(K + 3, (K, N), 0.02)
+    _, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+    ref32 = orc.wgrad_dge(A_bits, dY_bits, W_bits, s_w, 5.0, 3.0)
+    scale = np.float32(448.0 / float(np.max(np.abs(ref32))))
+    ref_codes, ref_amax = orc.wgrad_dge_fp8(ref32, float(scale))
+    codes, amax = fp4.fp4_linear_wgrad_dge(dev_bf16(A_bits), dev_bf16(dY_bits), dev_bf16(W_bits),
+                                           torch.from_numpy(s_w).cuda(), 5.0, 3.0, dw_type="e4m3",
+                                           dw_scale=torch.tensor([float(scale)], dtype=torch.float32, device="cuda"))
+    got = codes.cpu().numpy()
+
+    def signed_step(c):   # E4M3 codes as a monotone signed integer scale
+        c = c.astype(np.int32)
+        return np.where(c & 0x80, -(c & 0x7F), c & 0x7F)
+
+    assert np.max(np.abs(signed_step(got) - signed_step(ref_codes))) <= 1
+    assert np.mean(got == ref_codes) >= 0.99
+    assert abs(float(amax.item()) - float(ref_amax)) <= 1e-5 * float(ref_amax)
+    assert_no_device_flags(fp4)
+
+
+def test_wgrad_fp8_rejects_bad_arguments(fp4):
+    A = dev_bf16(_normal_bits(1, (64, 64)))
+    dY = dev_bf16(_normal_bits(2, (64, 64)))
+    W = dev_bf16(_normal_bits(3, (64, 64)))
+    s_w = torch.ones(64, dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        fp4.fp4_linear_wgrad_dge(A, dY, W, s_w, dw_type="e4m3")                  # no scale
+    with pytest.raises(ValueError):
+        fp4.fp4_linear_wgrad_dge(A, dY, W, s_w, dw_type="e5m2")
+    with pytest.raises(ValueError):
+        fp4.fp4_linear_wgrad_dge(A, dY, W, s_w, dw_scale=torch.ones(1, device="cuda"))   # fp32 with a scale
