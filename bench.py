@@ -6,7 +6,8 @@ for every distinct activation (linears that share an input share this phase)
   quantile threshold + clamp + CSR of dA + row codes of A_clamped (fp4_quantize_rows_outliers)
 and for every linear of the workload
   column quantization of W                               (fp4_quantize_cols)
-  FP4 GEMM + scales + dA*W compensation -> BF16 Y       (fp4_linear_fwd)
+  FP4 GEMM + scales + dA*W compensation -> BF16 Y       (fp4_linear_fwd; fp4_linear_fwd_dense
+                                                          when dA averages >= 28 entries per row)
   BF16 weight-gradient GEMM x DGE factor -> fp32 dW     (fp4_linear_wgrad_dge)
   BF16 input-gradient GEMM dY W^T -> BF16 dX             (fp4_linear_dgrad)
 
@@ -113,7 +114,7 @@ class ActStep:
     and the row codes / scales of A_clamped, all in fp4_quantize_rows_outliers."""
 
     PHASE = "fp4_quantize_rows_outliers"
-    LAUNCHES = 4   # histogram, fused row pass, row scan, CSR gather
+    LAUNCHES = 1   # one cooperative kernel (threshold, clamp, CSR, row codes)
 
     def __init__(self, fp4, A, q, label=""):
         import torch
@@ -148,8 +149,17 @@ class LinStep:
     """One linear: column quantization of W, FP4 GEMM, DGE weight gradient, input gradient."""
 
     PHASES = ("fp4_quantize_cols", "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_linear_dgrad")
-    # fwd: 2 compensation prep kernels (after a memset) and the GEMM
-    LAUNCHES = {"fp4_quantize_cols": 2, "fp4_linear_fwd": 3, "fp4_linear_wgrad_dge": 1, "fp4_linear_dgrad": 1}
+
+    def launches(self) -> int:
+        """Kernels one step of this linear launches: column maxima + codes;
+        the forward's 2 compensation prep kernels and the GEMM (K >= 4096: the
+        wide GEMM and its many-column fallback), or, for a dense dA, the FP4
+        GEMM, the split of dA, W^T and the BF16 product; wgrad; dgrad."""
+        if self.dense:
+            fwd = 4
+        else:
+            fwd = 2 + (2 if self.lin.K >= 4096 else 1)
+        return 2 + fwd + 1 + 1
 
     def __init__(self, fp4, lin, act: ActStep, W, dY):
         import torch
@@ -161,7 +171,10 @@ class LinStep:
         self.s_w = torch.empty(N, dtype=torch.float32, device=dev)
         self.ws_cols = torch.empty(max(fp4.fp4_quantize_cols_workspace(N), 16), dtype=torch.uint8, device=dev)
         self.Y = torch.empty((lin.M, N), dtype=torch.bfloat16, device=dev)
-        self.ws_fwd = torch.empty(fp4.fp4_linear_fwd_workspace(lin.M, N, K), dtype=torch.uint8, device=dev)
+        # a dense dA (a low clamp quantile) is multiplied on the BF16 tensor cores
+        self.dense = fp4.use_dense_compensation(lin.M, K, lin.q)
+        self.ws_fwd = torch.empty((fp4.fp4_linear_fwd_dense_workspace if self.dense else fp4.fp4_linear_fwd_workspace)(
+            lin.M, N, K), dtype=torch.uint8, device=dev)
         self.dW = torch.empty((K, N), dtype=torch.float32, device=dev)
         self.dX = torch.empty((lin.M, K), dtype=torch.bfloat16, device=dev)
         # split-tail workspaces of the backward GEMMs (None when the shapes never split)
@@ -173,8 +186,11 @@ class LinStep:
         fp4, lin, a = self.fp4, self.lin, self.act
         return [
             lambda: fp4.fp4_quantize_cols(self.W, codes_t=self.w_codes, scales=self.s_w, workspace=self.ws_cols),
-            lambda: fp4.fp4_linear_fwd(a.out["codes"], a.out["scales"], self.w_codes, self.s_w, lin.K, csr=a.out,
-                                       W=self.W, out_type="bf16", Y=self.Y, workspace=self.ws_fwd),
+            (lambda: fp4.fp4_linear_fwd_dense(a.out["codes"], a.out["scales"], self.w_codes, self.s_w, lin.K,
+                                              csr=a.out, W=self.W, out_type="bf16", Y=self.Y,
+                                              workspace=self.ws_fwd)) if self.dense else
+            (lambda: fp4.fp4_linear_fwd(a.out["codes"], a.out["scales"], self.w_codes, self.s_w, lin.K, csr=a.out,
+                                        W=self.W, out_type="bf16", Y=self.Y, workspace=self.ws_fwd)),
             lambda: fp4.fp4_linear_wgrad_dge(a.A, self.dY, self.W, self.s_w, DGE_K, DGE_CLIP, dW=self.dW,
                                              workspace=self.ws_wgrad),
             lambda: fp4.fp4_linear_dgrad(self.dY, self.W, dX=self.dX, workspace=self.ws_dgrad),
@@ -268,7 +284,7 @@ class StepPlan:
             self.step(self.side)
 
     def launches(self):
-        return ActStep.LAUNCHES * len(self.acts) + sum(LinStep.LAUNCHES.values()) * len(self.lins)
+        return ActStep.LAUNCHES * len(self.acts) + sum(l.launches() for l in self.lins)
 
 
 def _src_hash(files):
@@ -282,7 +298,7 @@ def _src_hash(files):
 KERNEL_SOURCES = {
     "fp4_linear_wgrad_dge": ["gemm_wgrad.cu", "bwd_gemm.cuh", "common.cuh"],
     "fp4_linear_dgrad": ["gemm_dgrad.cu", "bwd_gemm.cuh", "common.cuh"],
-    "fp4_linear_fwd": ["gemm_fwd.cu", "common.cuh"],
+    "fp4_linear_fwd": ["gemm_fwd.cu", "gemm_fwd_dense.cu", "bwd_gemm.cuh", "common.cuh"],
     "fp4_quantize_cols": ["quantize.cu", "common.cuh"],
     "fp4_quantize_rows_outliers": ["outlier.cu", "common.cuh"],
 }

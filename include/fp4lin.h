@@ -281,6 +281,59 @@ fp4_status fp4_linear_fwd(const uint8_t* a_codes, int64_t lda_codes_bytes, const
                           fp4_stream_t stream);
 
 /*
+ * fp4_linear_fwd_dense_workspace -- bytes of device workspace fp4_linear_fwd_dense
+ * needs: the fp32 FP4 product (4 M N), the dense three-part split of dA
+ * (6 M K), W^T in BF16 (2 N K) and the engine's split-tail area.  0 for
+ * invalid shapes (K % 64 != 0) or an unsupported device.  Host-only.
+ */
+size_t fp4_linear_fwd_dense_workspace(int64_t M, int64_t N, int64_t K);
+
+/*
+ * fp4_linear_fwd_dense -- the same result as fp4_linear_fwd with compensation,
+ * for a dense dA (a low clamp quantile: every tile of dA holds entries).
+ *
+ * Defined by: page "Microsoft Research bringt den ersten FP4-Genauigkeits-
+ * rahmen ..." (topaibox.com), "Peak-Dämpfung und -Kompensation von
+ * Ausreißern" (the clamped A in FP4, the residual dA multiplied in higher
+ * precision and added), with the granularity passage of page "首个 FP4 ..."
+ * (czzqal.com) for the scales:
+ *   Y[i,j] = acc[i,j] / (s_A[i] s_W[j]) + sum_k dA[i,k] W[k,j]
+ * How: the FP4 product goes to the workspace in fp32; dA is written densely as
+ * BF16 parts per entry whose sum is the fp32 entry exactly -- two (A and
+ * -sign(A) t) when the clamp threshold t is given, else three (hi + mid + lo)
+ * -- and multiplied by the BF16 W on the BF16 tensor cores (fp32 accumulation
+ * in 1024-term chunks, about 1e-6 of the sum of |terms| per output); the sum
+ * of the two products is rounded once to the output type.
+ * Choose it over fp4_linear_fwd when dA averages tens of entries per row or
+ * more (its cost does not depend on nnz); fp4_linear_fwd is faster for a few
+ * outlier channels.
+ *
+ *   arguments as for fp4_linear_fwd, except:
+ *   K         64 <= K <= 16384, K % 64 == 0
+ *   dA_row_ptr, dA_col, dA_val, W   required
+ *   dA_t      device fp32 scalar or NULL: the clamp threshold t that produced dA
+ *             (t_out of outlier_clamp_quantile / fp4_quantize_rows_outliers), so
+ *             that every value is A - sign(A) t with A and t BF16 values; then
+ *             the product runs over 2K instead of 3K.  An entry that breaks this
+ *             premise is multiplied as a two-part rounding of its value and
+ *             reported as the device-side INTERNAL flag.  4-byte aligned.
+ *   y_type    FP4_OUT_BF16 or FP4_OUT_FP32
+ *   workspace device, 256-byte aligned, ws_bytes >= fp4_linear_fwd_dense_workspace(M, N, K);
+ *             required; must not be shared by calls that may run at the same time
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, WORKSPACE, DEVICE_UNSUPPORTED, CUDA;
+ *         device-side INTERNAL flag for an entry whose column lies outside [0, K)
+ *         (the entry is skipped) or that breaks the dA_t premise, TIMEOUT as for
+ *         fp4_linear_fwd.
+ */
+fp4_status fp4_linear_fwd_dense(const uint8_t* a_codes, int64_t lda_codes_bytes, const float* s_a,
+                                const uint8_t* w_codes_t, int64_t ldw_codes_bytes, const float* s_w,
+                                int64_t M, int64_t N, int64_t K, const int32_t* dA_row_ptr,
+                                const int32_t* dA_col, const float* dA_val, const float* dA_t,
+                                const void* W, int64_t ldw,
+                                void* Y, int y_type, int64_t ldy, void* workspace, size_t ws_bytes,
+                                fp4_stream_t stream);
+
+/*
  * fp4_linear_wgrad_dge -- BF16 weight-gradient GEMM on tcgen05 (kind::f16)
  * with the differentiable-gradient-estimator (DGE) factor in the epilogue.
  *

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfp4lin.so")
 
-SOURCES = ["api.cu", "quantize.cu", "outlier.cu", "gemm_fwd.cu", "gemm_wgrad.cu", "gemm_dgrad.cu"]
+SOURCES = ["api.cu", "quantize.cu", "outlier.cu", "gemm_fwd.cu", "gemm_fwd_dense.cu", "gemm_wgrad.cu", "gemm_dgrad.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
                      "-I", INCLUDE, "-I", CSRC]

@@ -104,6 +104,8 @@ struct Cfg {
 
 struct Shape {
   int R, C, L;        // output rows, output columns, reduction length
+  int q_wrap;         // > 0: Q's reduction index is taken modulo q_wrap (a multiple of kBT), so
+                      // P's reduction may hold several parts that all meet the same Q; 0: none
   int whole, split;   // tiles computed whole, then `split` tiles computed as two halves
   float* part;        // split > 0: the halves' partial sums (SplitPlan layout)
   uint32_t* cnt;      // split > 0: one arrival counter per tile, warp and CTA, zeroed before launch
@@ -232,7 +234,7 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
           }
 #pragma unroll
           for (int h = 0; h < C::kBCols / kBox; ++h) {
-            const int r = bcol + h * kBox, l = lb * kBT;
+            const int r = bcol + h * kBox, l = p.q_wrap > 0 ? (lb * kBT) % p.q_wrap : lb * kBT;
             tma_load_2d_to<PAIR>(b_dst + h * kBoxBytes, &tmB, fb, KMAJOR ? l : r, KMAJOR ? r : l);
           }
         }

@@ -78,6 +78,7 @@ FP4_API fp4_status fp4_linear_dgrad(const void* dY, int64_t lddy, const void* W,
   s.R = int(M);
   s.C = int(K);
   s.L = int(N);
+  s.q_wrap = 0;
   s.status = status_word();
   s.wait_ns = kWaitLimitNs;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

@@ -204,6 +204,7 @@ FP4_API fp4_status fp4_linear_wgrad_dge(const void* A, int64_t lda, const void* 
   s.R = int(K);
   s.C = int(N);
   s.L = int(M);
+  s.q_wrap = 0;
   s.status = status_word();
   s.wait_ns = kWaitLimitNs;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

@@ -26,7 +26,8 @@ FLAG_TIMEOUT, FLAG_CAPACITY, FLAG_INTERNAL = 0x1, 0x2, 0x4
 EXPORTS = (
     "fp4_status_string", "fp4_abi_version", "fp4_last_cuda_error", "fp4_quantize_rows", "fp4_quantize_cols_workspace",
     "fp4_quantize_cols", "fp4_quantize_cols_noalloc", "outlier_max_nnz", "outlier_clamp_quantile_workspace", "outlier_clamp_quantile",
-    "fp4_quantize_rows_outliers", "fp4_linear_fwd_workspace", "fp4_linear_fwd", "fp4_linear_wgrad_dge", "fp4_linear_wgrad_dge_workspace",
+    "fp4_quantize_rows_outliers", "fp4_linear_fwd_workspace", "fp4_linear_fwd", "fp4_linear_fwd_dense_workspace",
+    "fp4_linear_fwd_dense", "fp4_linear_wgrad_dge", "fp4_linear_wgrad_dge_workspace",
     "fp4_linear_dgrad", "fp4_linear_dgrad_workspace",
     "fp4_device_status", "fp4_selftest_bounded_wait",
 )
@@ -64,6 +65,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "fp4_linear_fwd_workspace": (_c_sz, [_c_i64, _c_i64, _c_i64]),
         "fp4_linear_fwd": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64, _c_i64, _c_vp,
                                     _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_sz, _c_vp]),
+        "fp4_linear_fwd_dense_workspace": (_c_sz, [_c_i64, _c_i64, _c_i64]),
+        "fp4_linear_fwd_dense": (_c_int, [_c_vp, _c_i64, _c_vp, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64, _c_i64,
+                                          _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_i64, _c_vp,
+                                          _c_sz, _c_vp]),
         "fp4_linear_wgrad_dge": (_c_int, [_c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_vp, _c_i64, _c_i64,
                                           _c_i64, _c_f, _c_f, _c_vp, _c_int, _c_i64, _c_vp, _c_vp, _c_vp, _c_sz,
                                           _c_vp]),
@@ -318,6 +323,50 @@ def fp4_linear_fwd(a_codes: torch.Tensor, s_a: Optional[torch.Tensor], w_codes_t
     return Y
 
 
+def fp4_linear_fwd_dense_workspace(M: int, N: int, K: int) -> int:
+    """Bytes of workspace fp4_linear_fwd_dense needs on the current device."""
+    return int(_lib.fp4_linear_fwd_dense_workspace(M, N, K))
+
+
+def fp4_linear_fwd_dense(a_codes: torch.Tensor, s_a: torch.Tensor, w_codes_t: torch.Tensor, s_w: torch.Tensor,
+                         K: int, csr: Dict[str, torch.Tensor], W: torch.Tensor, out_type: str = "bf16",
+                         Y: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """Y = (qA qW^T) / (s_A s_W^T) + dA W with dA multiplied densely on the BF16
+    tensor cores; for a dense dA.  csr may hold "t", the clamp threshold that
+    produced dA (as fp4_quantize_rows_outliers returns it): then each entry is
+    two exact BF16 parts instead of three."""
+    dev = a_codes.device
+    M, N = a_codes.shape[0], w_codes_t.shape[0]
+    lda_c = _mat(a_codes, "a_codes", torch.uint8, M, K // 2, dev)
+    ldw_c = _mat(w_codes_t, "w_codes_t", torch.uint8, N, K // 2, dev)
+    if out_type not in ("bf16", "fp32"):
+        raise ValueError("out_type must be 'bf16' or 'fp32'")
+    yt = _OUT_TYPES[out_type]
+    _vec(s_a, "s_a", torch.float32, M, dev)
+    _vec(s_w, "s_w", torch.float32, N, dev)
+    ydt = torch.bfloat16 if yt == FP4_OUT_BF16 else torch.float32
+    if Y is None:
+        Y = torch.empty((M, N), dtype=ydt, device=dev)
+    ldy = _mat(Y, "Y", ydt, M, N, dev)
+    rp, ci, cv = csr["row_ptr"], csr["col_idx"], csr["vals"]
+    _vec(rp, "row_ptr", torch.int32, M + 1, dev)
+    _vec(ci, "col_idx", torch.int32, 0, dev)
+    _vec(cv, "vals", torch.float32, 0, dev)
+    ldw = _mat(W, "W", torch.bfloat16, K, N, dev)
+    t = csr.get("t")
+    if t is not None:
+        _vec(t, "t", torch.float32, 1, dev)
+    need = fp4_linear_fwd_dense_workspace(M, N, K)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _vec(workspace, "workspace", torch.uint8, need, dev)
+    _check("fp4_linear_fwd_dense", _lib.fp4_linear_fwd_dense(
+        _p(a_codes), lda_c, _p(s_a), _p(w_codes_t), ldw_c, _p(s_w), M, N, K, _p(rp), _p(ci), _p(cv), _p(t), _p(W),
+        ldw, _p(Y), yt, ldy, _p(workspace), workspace.numel(), _s(stream)))
+    return Y
+
+
 def _bwd_workspace(workspace, nbytes: int, device):
     """(pointer, bytes) for the backward GEMMs' split-tail workspace: "auto"
     allocates what the call needs (nothing when it never splits), None runs
@@ -422,15 +471,34 @@ def fp4_selftest_bounded_wait(timeout_us: int, stream=None) -> None:
 
 # ---------------------------------------------------------------- one layer
 
-def linear_forward(A: torch.Tensor, W: torch.Tensor, q: float, out_type: str = "bf16", stream=None):
+# dA averaging at least this many entries per row is multiplied densely
+# (fp4_linear_fwd_dense); the bound is n - ceil(q n), known on the host.
+DENSE_MIN_ROW_ENTRIES = 28
+
+
+def use_dense_compensation(M: int, K: int, q: float) -> bool:
+    """Whether linear_forward multiplies dA densely for this shape and quantile."""
+    return K % 64 == 0 and outlier_max_nnz(M, K, q) >= DENSE_MIN_ROW_ENTRIES * M
+
+
+def linear_forward(A: torch.Tensor, W: torch.Tensor, q: float, out_type: str = "bf16", stream=None,
+                   dense: Optional[bool] = None):
     """The whole forward of the quantized linear layer: quantile threshold,
     clamp + CSR of dA + row quantization of A_clamped (one fused pass), column
-    quantization of W, FP4 GEMM with scales and compensation.  Returns
-    (Y, intermediates)."""
+    quantization of W, FP4 GEMM with scales and compensation.  dense: multiply
+    dA on the BF16 tensor cores as a dense matrix (None: when
+    use_dense_compensation says so).  Returns (Y, intermediates)."""
     o = fp4_quantize_rows_outliers(A, q, stream=stream)
     w_codes_t, s_w = fp4_quantize_cols(W, stream=stream)
-    Y = fp4_linear_fwd(o["codes"], o["scales"], w_codes_t, s_w, A.shape[1], csr=o, W=W, out_type=out_type,
-                       stream=stream)
+    M, K = A.shape
+    if dense is None:
+        dense = use_dense_compensation(M, K, q) and out_type in ("bf16", "fp32")
+    if dense:
+        Y = fp4_linear_fwd_dense(o["codes"], o["scales"], w_codes_t, s_w, K, csr=o, W=W, out_type=out_type,
+                                 stream=stream)
+    else:
+        Y = fp4_linear_fwd(o["codes"], o["scales"], w_codes_t, s_w, K, csr=o, W=W, out_type=out_type,
+                           stream=stream)
     return Y, dict(outlier=o, a_codes=o["codes"], s_a=o["scales"], w_codes_t=w_codes_t, s_w=s_w)
 
 

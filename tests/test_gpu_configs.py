@@ -113,7 +113,8 @@ def test_full_size_linear(fp4, workload, linear):
     y_ref = orc.linear_fwd(ref_a, ref_sa, ref_w, ref_sw, rp_s, ci_s, cv_s, W_bits)
     mag = orc.linear_fwd_magnitude(ref_a, ref_sa, ref_w, ref_sw, rp_s, ci_s, cv_s, W_bits)
     y_gpu = host_bits(step.Y[torch.from_numpy(rows).cuda()])
-    assert_bf16_compensated_close(y_gpu, y_ref, mag)
+    # a dense dA is summed on the tensor cores (the backward engine's bound)
+    assert_bf16_compensated_close(y_gpu, y_ref, mag, **({"bound": TC_SUM_BOUND} if step.dense else {}))
     # DGE weight gradient on sampled feature rows
     dw_ref = orc.wgrad_dge(A_bits, dY_bits, W_bits, ref_sw, 5.0, 3.0, rows=frows)
     dw_gpu = step.dW[torch.from_numpy(frows).cuda()].cpu().numpy()

@@ -718,3 +718,84 @@ def test_wgrad_fp8_rejects_bad_arguments(fp4):
         fp4.fp4_linear_wgrad_dge(A, dY, W, s_w, dw_type="e5m2")
     with pytest.raises(ValueError):
         fp4.fp4_linear_wgrad_dge(A, dY, W, s_w, dw_scale=torch.ones(1, device="cuda"))   # fp32 with a scale
+
+
+# ---------------------------------------------------------------- dense compensation
+
+@pytest.mark.parametrize("M,K,N,q", [(300, 512, 264, 0.97), (2100, 1024, 520, 0.97), (129, 4096, 136, 0.99),
+                                     (64, 64, 8, 0.9)])
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+@pytest.mark.parametrize("with_t", [True, False])
+def test_linear_fwd_dense_compensation(fp4, M, K, N, q, out, with_t):
+    """Heavy-tailed A clamped at a low quantile (dA in every tile), from the
+    oracle's CSR and codes: Y = FP4 product + dA W with dA split into three BF16
+    parts on the tensor cores.  fp32 Y within 1e-5 relative Frobenius of the
+    fp64 oracle; BF16 Y within 1 ulp plus the tensor-core sum bound of the
+    terms' magnitude.  3K >= 2048 (K = 1024, 4096) runs CTA pairs; K = 4096
+    makes the FP4 product the 256 x 480 pair-tile kernel.  With the threshold t
+    each entry is the two BF16 parts A and -sign(A) t (reduction 2K), without
+    it three rounded parts (3K)."""
+    A_bits = _t3_bits(M + K, (M, K))
+    W_bits = _normal_bits(N + 7, (K, N), 0.02)
+    t, _, _ = orc.quantile_threshold(A_bits, q)
+    A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
+    assert rp[-1] >= 8 * M or M * K <= 4096          # dense enough to matter
+    a_codes, s_a = orc.quantize_rows(A_c)
+    w_codes, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+    csr = dict(row_ptr=torch.from_numpy(rp.astype(np.int32)).cuda(),
+               col_idx=torch.from_numpy(np.asarray(ci, np.int32)).cuda(),
+               vals=torch.from_numpy(np.asarray(cv, np.float32)).cuda())
+    if with_t:
+        csr["t"] = torch.tensor([float(t)], dtype=torch.float32, device="cuda")
+    Y = fp4.fp4_linear_fwd_dense(torch.from_numpy(a_codes).cuda(), torch.from_numpy(s_a).cuda(),
+                                 torch.from_numpy(w_codes).cuda(), torch.from_numpy(s_w).cuda(), K, csr=csr,
+                                 W=dev_bf16(W_bits), out_type=out)
+    y_ref = orc.linear_fwd(a_codes, s_a, w_codes, s_w, rp, ci, cv, W_bits)
+    if out == "fp32":
+        err = rel_frobenius(Y.cpu().numpy(), y_ref)
+        assert err <= FROB_TOL, err
+    else:
+        mag = orc.linear_fwd_magnitude(a_codes, s_a, w_codes, s_w, rp, ci, cv, W_bits)
+        assert_bf16_compensated_close(host_bits(Y), y_ref, mag, bound=TC_SUM_BOUND)
+    assert_no_device_flags(fp4)
+
+
+def test_linear_fwd_dense_rejects_bad_arguments(fp4):
+    codes = torch.zeros((64, 48), dtype=torch.uint8, device="cuda")
+    s = torch.ones(64, dtype=torch.float32, device="cuda")
+    csr = dict(row_ptr=torch.zeros(65, dtype=torch.int32, device="cuda"),
+               col_idx=torch.zeros(1, dtype=torch.int32, device="cuda"),
+               vals=torch.zeros(1, dtype=torch.float32, device="cuda"))
+    W = torch.zeros((96, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fp4.FP4Error):             # K % 64 != 0
+        fp4.fp4_linear_fwd_dense(codes, s, torch.zeros((64, 48), dtype=torch.uint8, device="cuda"), s, 96,
+                                 csr=csr, W=W)
+    with pytest.raises(ValueError):
+        fp4.fp4_linear_fwd_dense(codes, s, codes, s, 96, csr=csr, W=W, out_type="raw")
+
+
+def test_linear_fwd_dense_reports_a_wrong_threshold(fp4):
+    """A threshold that did not produce dA breaks the two-part premise: the
+    call still multiplies a two-part rounding of each entry and raises the
+    device-side INTERNAL flag."""
+    M, K, N = 128, 256, 64
+    A_bits = _t3_bits(5, (M, K))
+    W_bits = _normal_bits(6, (K, N), 0.02)
+    t, _, _ = orc.quantile_threshold(A_bits, 0.9)
+    A_c, rp, ci, cv = orc.clamp_and_compensation(A_bits, t)
+    a_codes, s_a = orc.quantize_rows(A_c)
+    w_codes, s_w = orc.quantize_cols(orc.bf16_to_f32(W_bits))
+    wrong = float(np.nextafter(np.float32(t), np.float32(np.inf)))     # not the clamp's threshold
+    csr = dict(row_ptr=torch.from_numpy(rp.astype(np.int32)).cuda(),
+               col_idx=torch.from_numpy(np.asarray(ci, np.int32)).cuda(),
+               vals=torch.from_numpy(np.asarray(cv, np.float32)).cuda(),
+               t=torch.tensor([wrong], dtype=torch.float32, device="cuda"))
+    assert_no_device_flags(fp4)
+    Y = fp4.fp4_linear_fwd_dense(torch.from_numpy(a_codes).cuda(), torch.from_numpy(s_a).cuda(),
+                                 torch.from_numpy(w_codes).cuda(), torch.from_numpy(s_w).cuda(), K, csr=csr,
+                                 W=dev_bf16(W_bits), out_type="fp32")
+    name, flags = fp4.fp4_device_status()
+    assert flags & 0x4, (name, flags)                                  # FP4_FLAG_INTERNAL (then cleared)
+    y_ref = orc.linear_fwd(a_codes, s_a, w_codes, s_w, rp, ci, cv, W_bits)
+    assert rel_frobenius(Y.cpu().numpy(), y_ref) <= 1e-4
+    assert_no_device_flags(fp4)
