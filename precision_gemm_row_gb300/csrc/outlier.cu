@@ -30,7 +30,7 @@ struct Ctrl {
 };
 
 struct WsLayout {
-  size_t hist, hist2, ctrl, fctrl, cta_total, cnt, scol, sval, total;
+  size_t hist, hist2, ctrl, fctrl, cta_total, cnt, rmax, scol, sval, total;
 };
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
@@ -47,6 +47,7 @@ WsLayout ws_layout(int64_t M) {
   L.fctrl = off; off += 256;
   L.cta_total = off; off += round256(size_t(kMaxCtas) * 8);
   L.cnt = off; off += round256(size_t(M) * 4);
+  L.rmax = off; off += round256(size_t(M) * 4);
   L.scol = off; off += round256(size_t(M) * kRowSlots * 4);
   L.sval = off; off += round256(size_t(M) * kRowSlots * 4);
   L.total = off;
@@ -78,20 +79,23 @@ __device__ __forceinline__ uint32_t outlier_mask8(const uint4 v, uint32_t tb) {
 //     unless the sample misleads (then step 4 fills the rest in);
 //  3. main pass over the CTA's rows: a histogram of the magnitudes >= F only
 //     (a chunk whose 8 magnitudes are all below F costs three packed maxima,
-//     no atomics), merged into g_main;                          -- barrier
+//     no atomics), merged into g_main, and each row's largest magnitude;
+//                                                               -- barrier
 //  4. every CTA selects t = the largest bin b with #{|A| >= b} >= n - k + 1
 //     (the k-th smallest); if the bins >= F hold fewer than n - k + 1 values,
 //     a second pass counts the magnitudes < F, and t is selected over all bins;
 //  5. row pass over the CTA's rows in reverse order (the rows read last in
-//     step 3 are still in L2): one warp per row, absmax of the clamped row and
-//     the outlier count, then codes, scale, A_clamped and the row's first
-//     kRowSlots entries (column order) into its slots;          -- barrier
+//     step 3 are still in L2): one warp per row in one streaming sweep -- the
+//     row's largest magnitude was recorded in step 3, so the scale of the
+//     clamped row, min(max |A|, t), comes first -- codes, A_clamped, the
+//     outlier count and the row's first kRowSlots entries (column order) into
+//     its slots;                                                -- barrier
 //  6. row_ptr from the per-CTA totals and a block scan; the slots (or, for a
 //     longer row, A read again) go to their CSR positions.
 constexpr int kRThreads = 512;
 constexpr int kRWarps = kRThreads / 32;
 constexpr int kPilotStride = 64;
-constexpr int kRU = 8;   // 16-byte loads in flight per lane (row pass, two sweeps)
+constexpr int kRU = 8;   // 16-byte chunks a lane per step of the row pass (two steps in flight)
 constexpr int kHU = 16;  // 16-byte loads in flight per lane (histogram passes)
 
 struct FCtrl {
@@ -112,6 +116,7 @@ struct RowCallParams {
   Ctrl* ctrl;              // t_bits and nnz_expect for the caller-visible checks
   int64_t* cta_total;      // one per CTA
   int32_t* row_cnt;
+  uint32_t* rmax;          // per row: the largest magnitude pattern (main histogram pass)
   int32_t* scol;
   float* sval;
   float* t_out;
@@ -160,11 +165,12 @@ __device__ bool grid_sync(FCtrl* c, uint64_t limit_ns) {
 // Counts the magnitude patterns in [lo, hi) of rows r (r_begin <= r < r_end,
 // r - r_begin a multiple of `stride`, one warp per row) into hist (shared).
 __device__ void rows_histogram(const RowCallParams& p, int64_t r_begin, int64_t r_end, int stride, uint32_t lo,
-                               uint32_t hi, uint32_t* hist) {
+                               uint32_t hi, uint32_t* hist, uint32_t* rmax) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunk = p.K >> 3;
   for (int64_t row = r_begin + int64_t(warp) * stride; row < r_end; row += int64_t(kRWarps) * stride) {
     const uint4* src = reinterpret_cast<const uint4*>(p.A + row * p.lda);
+    uint32_t mx = 0;   // the row's largest magnitude pattern (rmax given)
     for (int c00 = 0; c00 < nchunk; c00 += 32 * kHU) {   // every lane takes every step
       uint4 v[kHU];
 #pragma unroll
@@ -176,7 +182,9 @@ __device__ void rows_histogram(const RowCallParams& p, int64_t r_begin, int64_t 
       for (int u = 0; u < kHU; ++u) {
         if (c00 + 32 * u + lane >= nchunk) continue;
         const uint32_t m2 = chunk_maxmag(v[u]);
-        if (max(m2 & 0xFFFFu, m2 >> 16) < lo) continue;   // all 8 below the range: no atomics
+        const uint32_t m1 = max(m2 & 0xFFFFu, m2 >> 16);
+        mx = max(mx, m1);
+        if (m1 < lo) continue;   // all 8 below the range: no atomics
         const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -186,16 +194,20 @@ __device__ void rows_histogram(const RowCallParams& p, int64_t r_begin, int64_t 
         }
       }
     }
+    if (rmax) {
+      mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+      if (lane == 0) rmax[row] = mx;
+    }
   }
 }
 
 // Zeroes hist[lo, hi) (shared), histograms the CTA's rows into it and adds the
 // nonzero bins to g (global).
 __device__ void histogram_phase(const RowCallParams& p, int64_t r0, int64_t r1, int stride, uint32_t lo,
-                                uint32_t hi, uint32_t* hist, uint32_t* g) {
+                                uint32_t hi, uint32_t* hist, uint32_t* g, uint32_t* rmax = nullptr) {
   for (uint32_t b = lo + threadIdx.x; b < hi; b += kRThreads) hist[b] = 0u;
   __syncthreads();
-  rows_histogram(p, r0, r1, stride, lo, hi, hist);
+  rows_histogram(p, r0, r1, stride, lo, hi, hist, rmax);
   __syncthreads();
   for (uint32_t b = lo + threadIdx.x; b < hi; b += kRThreads) {
     const uint32_t c = hist[b];
@@ -325,110 +337,59 @@ __device__ __forceinline__ void chunk_outputs(uint32_t* cdst, uint4* adst, int c
 
 __device__ __noinline__ uint32_t count_outliers(const uint4 v, uint32_t tbits) { return __popc(outlier_mask8(v, tbits)); }
 
-// Scale, row count and slots of one row from its absmax pattern and count
-// (warp-uniform); lane 0 writes them.  Returns the scale.
-__device__ __forceinline__ float row_scale(const RowCallParams& p, int64_t row, uint32_t amax_bits, uint32_t cnt,
-                                           uint32_t tbits) {
+// Loads step s of a row: chunks c = 32 (kRU s + u) + lane (zero past the row).
+__device__ __forceinline__ void load_step(const uint4* src, int s, int nchunk, uint4 (&v)[kRU]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int u = 0; u < kRU; ++u) {
+    const int c = 32 * (kRU * s + u) + lane;
+    v[u] = c < nchunk ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Codes, A_clamped, outlier count and slots of step s's chunks (the scale is
+// known).  Every lane calls.
+__device__ __forceinline__ void row_step(const RowCallParams& p, int64_t row, int s, int nchunk, const uint4 (&v)[kRU],
+                                         uint32_t* cdst, uint4* adst, float sc, uint32_t tbits, uint32_t tb2, float t,
+                                         uint32_t& cnt, uint32_t& pos) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int u = 0; u < kRU; ++u) {
+    const int c = 32 * (kRU * s + u) + lane;
+    const bool has = bf2_gt_mask(chunk_maxmag(v[u]), tb2);   // zero chunks past the row: never
+    if (c < nchunk) chunk_outputs(cdst, adst, c, v[u], sc, tb2, has);
+    if (has) cnt += count_outliers(v[u], tbits);
+    if (pos < uint32_t(kRowSlots) && __any_sync(0xFFFFFFFFu, has)) emit_slots(p, row, c, has, v[u], tbits, t, pos);
+  }
+}
+
+// One row in a single streaming sweep: its largest magnitude is known from the
+// main histogram pass, so the scale comes first, and every chunk is quantized,
+// clamped and searched for outliers as it arrives (two steps of kRU chunks a
+// lane in flight).  Every lane of the warp calls; returns the outlier count.
+__device__ uint32_t row_pass(const RowCallParams& p, int64_t row, int nchunk, uint32_t tbits, float t) {
+  const uint32_t tb2 = tbits | (tbits << 16);
+  const uint4* src = reinterpret_cast<const uint4*>(p.A + row * p.lda);
+  const int nsteps = (nchunk + 32 * kRU - 1) / (32 * kRU);
+  uint4 a[kRU], b[kRU];
+  load_step(src, 0, nchunk, a);
   // max over min(|x|, t) = min(max |x|, t)
-  const float sc = scale_from_absmax(bf16_bits_to_float(min(amax_bits, tbits)));
-  if ((threadIdx.x & 31) == 0) {
-    if (p.scales) p.scales[row] = sc;
-    p.row_cnt[row] = int32_t(cnt);
-  }
-  return sc;
-}
-
-// One row held in registers (CH 16-byte chunks a lane, c = 32 j + lane): one read
-// of A.  Every lane of the warp calls; returns the row's outlier count.
-template <int CH>
-__device__ uint32_t row_pass_regs(const RowCallParams& p, int64_t row, int nchunk, uint32_t tbits, float t) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t tb2 = tbits | (tbits << 16);
-  const uint4* src = reinterpret_cast<const uint4*>(p.A + row * p.lda);
-  uint4 v[CH];
-#pragma unroll
-  for (int j = 0; j < CH; ++j) {
-    const int c = 32 * j + lane;
-    v[j] = c < nchunk ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  uint32_t mx = 0, cnt = 0, ob = 0;   // ob bit j: chunk j holds a value above t
-#pragma unroll
-  for (int j = 0; j < CH; ++j) {
-    const uint32_t m2 = chunk_maxmag(v[j]);   // zero chunks (past the row) add nothing
-    mx = bf2_max(mx, m2);
-    if (bf2_gt_mask(m2, tb2)) {
-      ob |= 1u << j;
-      cnt += count_outliers(v[j], tbits);
-    }
-  }
-  const uint32_t amax_bits = warp_max_bits(mx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
-  const float sc = row_scale(p, row, amax_bits, cnt, tbits);
+  const float sc = scale_from_absmax(bf16_bits_to_float(min(__ldcg(p.rmax + row), tbits)));
+  if ((threadIdx.x & 31) == 0 && p.scales) p.scales[row] = sc;
   uint32_t* cdst = p.codes ? reinterpret_cast<uint32_t*>(p.codes + row * p.ldc) : nullptr;
   uint4* adst = p.A_c ? reinterpret_cast<uint4*>(p.A_c + row * p.ldac) : nullptr;
-  uint32_t pos = 0;
-#pragma unroll
-  for (int j = 0; j < CH; ++j) {
-    const int c = 32 * j + lane;
-    const bool has = (ob >> j) & 1u;
-    if (c < nchunk) chunk_outputs(cdst, adst, c, v[j], sc, tb2, has);
-    if (cnt != 0 && pos < uint32_t(kRowSlots)) {   // warp-uniform
-      if (__any_sync(0xFFFFFFFFu, has)) emit_slots(p, row, c, has, v[j], tbits, t, pos);
+  uint32_t cnt = 0, pos = 0;
+  for (int s = 0; s < nsteps; s += 2) {   // warp-uniform
+    if (s + 1 < nsteps) load_step(src, s + 1, nchunk, b);
+    row_step(p, row, s, nchunk, a, cdst, adst, sc, tbits, tb2, t, cnt, pos);
+    if (s + 1 < nsteps) {
+      if (s + 2 < nsteps) load_step(src, s + 2, nchunk, a);
+      row_step(p, row, s + 1, nchunk, b, cdst, adst, sc, tbits, tb2, t, cnt, pos);
     }
   }
-  return cnt;
-}
-
-// A row too wide for registers: absmax and count in a first sweep over A, then
-// codes, A_clamped and slots in a second (the row is then in L1 / L2).
-__device__ uint32_t row_pass_two_sweeps(const RowCallParams& p, int64_t row, int nchunk, uint32_t tbits, float t) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t tb2 = tbits | (tbits << 16);
-  const uint4* src = reinterpret_cast<const uint4*>(p.A + row * p.lda);
-  uint32_t mx = 0, cnt = 0;
-  uint64_t ob = 0;   // bit g: this lane's chunk 32 g + lane holds a value above t (g < 64: K <= 16384)
-  for (int c00 = 0; c00 < nchunk; c00 += 32 * kRU) {   // every lane takes every step
-    uint4 v[kRU];
-#pragma unroll
-    for (int u = 0; u < kRU; ++u) {
-      const int c = c00 + 32 * u + lane;
-      v[u] = c < nchunk ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < kRU; ++u) {
-      const uint32_t m2 = chunk_maxmag(v[u]);
-      mx = bf2_max(mx, m2);
-      if (bf2_gt_mask(m2, tb2)) {
-        ob |= 1ull << (c00 / 32 + u);
-        cnt += count_outliers(v[u], tbits);
-      }
-    }
-  }
-  const uint32_t amax_bits = warp_max_bits(mx);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
-  const float sc = row_scale(p, row, amax_bits, cnt, tbits);
-  uint32_t* cdst = p.codes ? reinterpret_cast<uint32_t*>(p.codes + row * p.ldc) : nullptr;
-  uint4* adst = p.A_c ? reinterpret_cast<uint4*>(p.A_c + row * p.ldac) : nullptr;
-  uint32_t pos = 0;
-  for (int c00 = 0; c00 < nchunk; c00 += 32 * kRU) {   // every lane takes every step (warp-wide scans)
-    uint4 v[kRU];
-#pragma unroll
-    for (int u = 0; u < kRU; ++u) {
-      const int c = c00 + 32 * u + lane;
-      v[u] = c < nchunk ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < kRU; ++u) {
-      const int c = c00 + 32 * u + lane;
-      const bool has = (ob >> (c00 / 32 + u)) & 1ull;
-      if (c < nchunk) chunk_outputs(cdst, adst, c, v[u], sc, tb2, has);
-      if (cnt != 0 && pos < uint32_t(kRowSlots)) {   // warp-uniform
-        if (__any_sync(0xFFFFFFFFu, has)) emit_slots(p, row, c, has, v[u], tbits, t, pos);
-      }
-    }
-  }
+  if ((threadIdx.x & 31) == 0) p.row_cnt[row] = int32_t(cnt);
   return cnt;
 }
 
@@ -462,7 +423,7 @@ __global__ void __launch_bounds__(kRThreads, 1) rowcall_kernel(const RowCallPara
   int tb = -1;
   uint64_t nnz_expect = 0;
   if (ok) {
-    histogram_phase(p, r0, r1, 1, F, uint32_t(kBins), hist, p.g_main);
+    histogram_phase(p, r0, r1, 1, F, uint32_t(kBins), hist, p.g_main, p.rmax);   // every row: its max too
     ok = grid_sync(p.fctrl, p.wait_ns);
   }
   if (ok) {
@@ -499,16 +460,9 @@ __global__ void __launch_bounds__(kRThreads, 1) rowcall_kernel(const RowCallPara
 
   // ---- 5: row pass, one warp per row, the CTA's rows in reverse order
   const int nchunk = p.K >> 3;
-  const int per_lane = (nchunk + 31) / 32;
   long long cta_cnt = 0;
   for (int64_t i = warp; r1 - 1 - i >= r0; i += kRWarps) {
-    const int64_t row = r1 - 1 - i;
-    uint32_t cnt;
-    if (per_lane <= 4) cnt = row_pass_regs<4>(p, row, nchunk, tbits, t);
-    else if (per_lane <= 8) cnt = row_pass_regs<8>(p, row, nchunk, tbits, t);
-    else if (per_lane <= 16) cnt = row_pass_regs<16>(p, row, nchunk, tbits, t);
-    else if (per_lane <= 20) cnt = row_pass_regs<20>(p, row, nchunk, tbits, t);
-    else cnt = row_pass_two_sweeps(p, row, nchunk, tbits, t);
+    const uint32_t cnt = row_pass(p, r1 - 1 - i, nchunk, tbits, t);
     cta_cnt += cnt;
   }
   // the CTA's total
@@ -684,6 +638,7 @@ fp4_status run_outlier_pipeline(const void* A, int64_t M, int64_t K, int64_t lda
   prm.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
   prm.cta_total = reinterpret_cast<int64_t*>(ws + L.cta_total);
   prm.row_cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
+  prm.rmax = reinterpret_cast<uint32_t*>(ws + L.rmax);
   prm.scol = reinterpret_cast<int32_t*>(ws + L.scol);
   prm.sval = reinterpret_cast<float*>(ws + L.sval);
   prm.t_out = t_out;
