@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(256) col_absmax_kernel(const uint16_t* __restr
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int k = kb + 8 * u;
-        v[u] = k < k1 ? __ldcs(reinterpret_cast<const uint4*>(W + int64_t(k) * ldw) + cchunk)
+        v[u] = k < k1 ? __ldg(reinterpret_cast<const uint4*>(W + int64_t(k) * ldw) + cchunk)
                       : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
@@ -132,7 +132,8 @@ __global__ void __launch_bounds__(256) quantize_cols_tma_kernel(const __grid_con
   __shared__ float s_col[kColTileN];
   __shared__ __align__(8) uint64_t bar;
   const int tid = threadIdx.x;
-  const int j0 = blockIdx.x * kColTileN, k0 = blockIdx.y * kColTileK;
+  // K tiles in reverse: the rows col_absmax_kernel read last are the likeliest to be in L2
+  const int j0 = blockIdx.x * kColTileN, k0 = (int(gridDim.y) - 1 - int(blockIdx.y)) * kColTileK;
   const uint32_t b = smem_u32(&bar);
   if (tid == 0) {
     mbar_init(b, 1);
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(256) quantize_cols_tma_kernel(const __grid_con
     float sc = 1.0f;
     if (j < N) {
       sc = scale_from_absmax(__uint_as_float(colmax[j]));
-      if (blockIdx.y == 0) scales[j] = sc;
+      if (k0 == 0) scales[j] = sc;
     }
     s_col[tid] = sc;
   }
