@@ -16,7 +16,9 @@ inputs resident in HBM and L2 flushed (256 MiB write) before every step.
 `e2e` is the same metric through the C ABI from pinned HOST buffers: the
 host->device copy of A, W, dY and the device->host copy of Y, dW and dX are inside
 the timed region, on their own streams so that they overlap the kernels (the
-phases wait, by events, for their inputs to land).  `--impl reference` times the CPU oracle instead (bounded
+phases wait, by events, for their inputs to land; linear by linear, so one
+linear's outputs go back while the next one's inputs come in).  `e2e.link`
+times the same copies alone.  `--impl reference` times the CPU oracle instead (bounded
 sample, single thread).  Under torchrun each rank runs an independent replica
 on its own GPU (the layer has no data-path exchange on one GPU's batch);
 value = work of all ranks / max-over-ranks time.
@@ -466,13 +468,15 @@ def run_gpu(args):
     bi = sum(h.numel() * 2 for h in uniq_hA.values()) + sum(h[1].numel() * 2 + h[2].numel() * 2 for h in host)
     bo = sum(y.numel() * 2 + d.numel() * 4 + x.numel() * 2 for y, d, x in zip(hY, hdW, hdX))
     e2e_ms = []
-    # Copies overlap the kernels as a user of the layer would run them: host to
-    # device on one stream (activations and weights first, output gradients
-    # last), the phases on the current stream as their inputs land (dgrad
-    # before wgrad), device to host on a third stream as each output is done.
+    # Copies overlap the kernels: host to device on one stream, linear by linear
+    # (its activation if new, W, then dY), the phases on the current stream as
+    # their inputs land (an activation's row call before its first linear,
+    # dgrad before wgrad), device to host on a third stream as each output is
+    # done, so the outputs of one linear go back while the next one's inputs
+    # come in.
     s_c, s_in, s_out = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    acts = list(plan.acts.values())
-    nacts = len(acts)
+    act_index = {id(a): j for j, a in enumerate(plan.acts.values())}
+    nacts = len(act_index)
     idx = {name: i for i, name in enumerate(LinStep.PHASES)}
     for k in range(args.warmup + args.steps):
         flush.fill_(float(k))
@@ -490,14 +494,15 @@ def run_gpu(args):
                 l.W.copy_(host[i][1], non_blocking=True)
                 ev_w.append(torch.cuda.Event())
                 ev_w[-1].record(s_in)
-            for i, l in enumerate(plan.lins):
                 l.dY.copy_(host[i][2], non_blocking=True)
                 ev_g.append(torch.cuda.Event())
                 ev_g[-1].record(s_in)
-        for j, a in enumerate(acts):
-            s_c.wait_event(ev_a[id(a)])
-            plan.graphs[j].replay()
+        done_acts = set()
         for i, l in enumerate(plan.lins):
+            if id(l.act) not in done_acts:
+                s_c.wait_event(ev_a[id(l.act)])
+                plan.graphs[act_index[id(l.act)]].replay()
+                done_acts.add(id(l.act))
             base = nacts + len(LinStep.PHASES) * i
             s_c.wait_event(ev_w[i])
             plan.graphs[base + idx["fp4_quantize_cols"]].replay()
@@ -525,6 +530,41 @@ def run_gpu(args):
         if k >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
     e2e_ms_mean = sum(e2e_ms) / len(e2e_ms)
+
+    # ---- the same copies alone, on the same streams, with no kernels: the
+    # link's rate for these bytes, which bounds e2e from below
+    def copies_only(h2d: bool, d2h: bool) -> float:
+        ts = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_c)
+            s_in.wait_event(e0)
+            s_out.wait_event(e0)
+            if h2d:
+                with torch.cuda.stream(s_in):
+                    seen = set()
+                    for i, l in enumerate(plan.lins):
+                        if id(l.act) not in seen:
+                            l.act.A.copy_(host[i][0], non_blocking=True)
+                            seen.add(id(l.act))
+                        l.W.copy_(host[i][1], non_blocking=True)
+                        l.dY.copy_(host[i][2], non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s_out):
+                    for i, l in enumerate(plan.lins):
+                        hY[i].copy_(l.Y, non_blocking=True)
+                        hdX[i].copy_(l.dX, non_blocking=True)
+                        hdW[i].copy_(l.dW, non_blocking=True)
+            s_c.wait_stream(s_in)
+            s_c.wait_stream(s_out)
+            e1.record(s_c)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    t_in, t_out, t_both = copies_only(True, False), copies_only(False, True), copies_only(True, True)
+    link = {"h2d_gbs": round(bi / t_in / 1e6, 1), "d2h_gbs": round(bo / t_out / 1e6, 1),
+            "copies_only_ms": round(t_both, 3), "e2e_over_copies_only": round(e2e_ms_mean / t_both, 3)}
 
     # ---- max over ranks
     ms_max, e2e_max = max_over_ranks([ms_per_step, e2e_ms_mean], "cuda")
@@ -590,7 +630,7 @@ def run_gpu(args):
         "kernels": kernels, "phases_one_after_another_ms": round(seq_ms, 5), "nnz": nnz,
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-                "ms_per_step": round(e2e_max, 5)},
+                "ms_per_step": round(e2e_max, 5), "link": link},
         "gpu_launches": args.steps * plan.launches(),
         "clocks": clocks.summary(),
     }
@@ -641,6 +681,19 @@ print(json.dumps(dict(steps=steps, flops=flops)))
 ORACLE_SAMPLE = 256     # tokens x output columns of every linear's sub-problem
 
 
+FULL_PROBLEM_MAX = 1024   # a workload whose linears all have M, N <= this is timed in full
+
+
+def effective_sample(workload: str, sample: int) -> int:
+    """The sub-problem size: the whole problem when it is small (every token and
+    output column), else `sample`."""
+    from precision_gemm_row_gb300 import workloads as wl
+    lins = wl.WORKLOADS[workload].linears
+    if all(l.M <= FULL_PROBLEM_MAX and l.N <= FULL_PROBLEM_MAX for l in lins):
+        return max(max(l.M, l.N) for l in lins)
+    return sample
+
+
 def _oracle_steps(workload: str, sample: int, nsteps: int):
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
@@ -651,7 +704,14 @@ def _oracle_steps(workload: str, sample: int, nsteps: int):
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def _sample_text(sample: int) -> str:
+def _sample_text(sample: int, workload: str) -> str:
+    from precision_gemm_row_gb300 import workloads as wl
+    lins = wl.WORKLOADS[workload].linears
+    if all(l.M <= sample and l.N <= sample for l in lins):
+        return ("the whole problem: every linear of the workload on all its tokens and output columns (quantile + "
+                "clamp + CSR + row codes, column codes, FP4 GEMM + epilogue, DGE weight gradient, input gradient), "
+                "all measured; value = 6 M K N summed over the linears / measured time; one thread "
+                "(OPENBLAS/OMP threads = 1)")
     return (f"every linear of the workload on its first {sample} tokens x first {sample} output columns (the whole "
             f"reduction length K): quantile + clamp + CSR + row codes of that activation slice, column codes of that "
             f"weight slice, FP4 GEMM + epilogue, DGE weight gradient and input gradient, all measured (nothing "
@@ -663,10 +723,11 @@ def cpu_baseline(workload: str, sample: int = ORACLE_SAMPLE, nsteps: int = 2):
     """The oracle, as it stands, timed in a fresh single-thread interpreter on a
     bounded sub-problem of every linear of the workload (see _sample_text)."""
     t0 = time.time()
+    sample = effective_sample(workload, sample)
     d = _oracle_steps(workload, sample, nsteps)
     step_s = statistics.median(d["steps"])
     return {"value": round(d["flops"] / step_s / 1e12, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": _sample_text(sample), "sample_flops_per_step": d["flops"], "step_s": round(step_s, 6),
+            "sample": _sample_text(sample, workload), "sample_flops_per_step": d["flops"], "step_s": round(step_s, 6),
             "steps": nsteps, "wall_s": round(time.time() - t0, 1)}
 
 
@@ -679,10 +740,11 @@ def run_reference(args):
         return None
     from precision_gemm_row_gb300 import workloads as wl
     t0 = time.time()
-    d = _oracle_steps(args.workload, args.cpu_sample, args.warmup + args.steps)
+    sample = effective_sample(args.workload, args.cpu_sample)
+    d = _oracle_steps(args.workload, sample, args.warmup + args.steps)
     step_s = statistics.median(d["steps"][args.warmup:])
     v = round(d["flops"] / step_s / 1e12, 8)
-    cb = {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": _sample_text(args.cpu_sample),
+    cb = {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": _sample_text(sample, args.workload),
           "sample_flops_per_step": d["flops"], "step_s": round(step_s, 6), "steps": args.steps,
           "wall_s": round(time.time() - t0, 1)}
     return {"impl": "reference", "metric": "FP4 linear fwd+bwd TFLOPS on 1 GB300, % of dense FP4 peak; quantize GB/s "

@@ -78,7 +78,8 @@ def test_bench_linear_selection():
 
 def test_reference_arm_line_on_the_small_workload():
     """bench.py --impl reference times the oracle on the host; its JSON line
-    carries the contract's keys (checked on the 256 x 512 x 512 workload)."""
+    carries the contract's keys (checked on the 256 x 512 x 512 workload, which
+    it times in full)."""
     import bench
     args = types.SimpleNamespace(workload="c1_single_linear_256x512x512", steps=1, warmup=3, cpu_sample=16,
                                  fuse_shared_input=False, linear=[])
@@ -95,7 +96,9 @@ def test_reference_arm_line_on_the_small_workload():
     cb = line["cpu_baseline"]
     assert line["ms_per_step"] == pytest.approx(cb["step_s"] * 1e3, abs=1e-3)
     assert line["value"] == pytest.approx(cb["sample_flops_per_step"] / cb["step_s"] / 1e12, rel=2e-3)
-    assert cb["sample_flops_per_step"] == 6 * 16 * 512 * 16
+    # the small workload is timed in full (every token and output column), whatever the sample
+    assert cb["sample_flops_per_step"] == 6 * 256 * 512 * 512
+    assert cb["sample"].startswith("the whole problem")
     assert line["config"]["workload"] == "c1_single_linear_256x512x512"
     assert line["config"]["linears"] == [["linear", 256, 512, 512, 0.99]]
 
