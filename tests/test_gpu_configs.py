@@ -10,7 +10,8 @@ Student-t stress case), run through the same launches bench.py times
 * the whole M x N raw FP4 accumulator against torch._int_mm (cuBLASLt int8) on
   the x2 integer codes; raw accumulators bit-exact and BF16 Y (1 ulp + fp32 sum
   bound) against the oracle, from the oracle's own codes, on sampled rows;
-* DGE weight gradient within 1e-5 relative Frobenius on sampled feature rows;
+* DGE weight gradient within 1e-5 relative Frobenius on sampled feature rows, and its E4M3
+  form within one code of the oracle's encoding there;
 * BF16 input gradient dY W^T within 1 ulp + the tensor-core sum bound on sampled rows.
 """
 import types
@@ -119,6 +120,23 @@ def test_full_size_linear(fp4, workload, linear):
     dw_ref = orc.wgrad_dge(A_bits, dY_bits, W_bits, ref_sw, 5.0, 3.0, rows=frows)
     dw_gpu = step.dW[torch.from_numpy(frows).cuda()].cpu().numpy()
     assert rel_frobenius(dw_gpu, dw_ref) <= FROB_TOL
+    # the FP8 (E4M3) weight gradient of the same launch shape, with a scale set
+    # from the oracle's sampled gradient: codes within one step of the oracle's
+    # encoding of its own gradient, almost all equal; the returned max |dW|
+    # covers the sampled rows and agrees with the fp32 gradient's
+    scale = np.float32(448.0 / float(np.max(np.abs(dw_ref))))
+    codes8, amax = fp4.fp4_linear_wgrad_dge(act.A, step.dY, step.W, step.s_w, 5.0, 3.0, dw_type="e4m3",
+                                            dw_scale=torch.tensor([float(scale)], dtype=torch.float32,
+                                                                  device="cuda"))
+    ref8, _ = orc.wgrad_dge_fp8(dw_ref, float(scale))
+    got8 = codes8[torch.from_numpy(frows).cuda()].cpu().numpy().astype(np.int32)
+    step_of = lambda c: np.where(c & 0x80, -(c & 0x7F), c & 0x7F)
+    assert np.max(np.abs(step_of(got8) - step_of(ref8.astype(np.int32)))) <= 1
+    assert np.mean(got8 == ref8) >= 0.99
+    amax = float(amax.item())
+    assert amax >= float(np.max(np.abs(dw_ref))) * (1 - 1e-5)
+    assert amax == float(step.dW.abs().max().item())
+    del codes8
     # input gradient on sampled token rows
     dx_ref = orc.linear_dgrad(dY_bits, W_bits, rows=rows)
     dx_mag = orc.linear_dgrad(dY_bits & np.uint16(0x7FFF), W_bits & np.uint16(0x7FFF), rows=rows)
