@@ -517,7 +517,33 @@ __global__ void __launch_bounds__(kRThreads, 1) rowcall_kernel(const RowCallPara
       if (w < warp) before += (long long)red64[w];
       tile_total += (long long)red64[w];
     }
-    if (row < r1) p.row_ptr[row + 1] = int32_t(base + carry + before + x);
+    if (row < r1) {
+      const long long end = base + carry + before + x;
+      p.row_ptr[row + 1] = int32_t(end);
+      // a row whose entries all fit in its slots is copied to its CSR position
+      // here, by its own thread (longer rows are read again from A below)
+      if (p.cap > 0 && c > 0 && c <= kRowSlots && end <= p.cap) {
+        const long long dst = end - c;
+        for (int e0 = 0; e0 < int(c); e0 += 8) {
+          int32_t ci[8];
+          float cv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (e0 + u < int(c)) {
+              ci[u] = __ldcg(p.scol + row * kRowSlots + e0 + u);
+              cv[u] = __ldcg(p.sval + row * kRowSlots + e0 + u);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (e0 + u < int(c)) {
+              p.col_idx[dst + e0 + u] = ci[u];
+              p.vals[dst + e0 + u] = cv[u];
+            }
+          }
+        }
+      }
+    }
     carry += tile_total;
   }
   if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
@@ -528,51 +554,52 @@ __global__ void __launch_bounds__(kRThreads, 1) rowcall_kernel(const RowCallPara
   }
   __syncthreads();   // this CTA's row_ptr entries are visible to all its threads
   if (p.cap == 0) return;
-  // gather: the row's slots to its CSR position, or the row read again from A
-  for (int64_t row = r0 + warp; row < r1; row += kRWarps) {
-    const int32_t nr = __ldcg(p.row_cnt + row);
-    const int64_t dst = p.row_ptr[row];
-    if (nr == 0 || dst + nr > p.cap) continue;   // beyond the capacity: flagged above
-    if (nr <= kRowSlots) {
-      if (lane < nr) {
-        p.col_idx[dst + lane] = __ldcg(p.scol + row * kRowSlots + lane);
-        p.vals[dst + lane] = __ldcg(p.sval + row * kRowSlots + lane);
-      }
-      continue;
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(p.A + row * p.lda);
-    int64_t b = dst;
-    constexpr int kDepth = 4;   // 32-chunk groups loaded before any is scanned
-    for (int c00 = 0; c00 < nchunk; c00 += 32 * kDepth) {   // every lane takes every step
-      uint4 vv[kDepth];
+  // rows with more entries than slots: read again from A, one warp per row (a
+  // warp finds them 32 rows at a time)
+  for (int64_t g0 = r0 + 32 * int64_t(warp); g0 < r1; g0 += 32 * int64_t(kRWarps)) {
+    const int32_t myc = g0 + lane < r1 ? __ldcg(p.row_cnt + g0 + lane) : 0;
+    uint32_t longrows = __ballot_sync(0xFFFFFFFFu, myc > kRowSlots);
+    while (longrows) {   // warp-uniform
+      const int l = __ffs(longrows) - 1;
+      longrows &= longrows - 1;
+      const int64_t row = g0 + l;
+      const int32_t nr = __shfl_sync(0xFFFFFFFFu, myc, l);
+      const int64_t dst = p.row_ptr[row];
+      if (dst + nr > p.cap) continue;   // beyond the capacity: flagged above
+      const uint4* src = reinterpret_cast<const uint4*>(p.A + row * p.lda);
+      int64_t b = dst;
+      constexpr int kDepth = 4;   // 32-chunk groups loaded before any is scanned
+      for (int c00 = 0; c00 < nchunk; c00 += 32 * kDepth) {   // every lane takes every step
+        uint4 vv[kDepth];
 #pragma unroll
-      for (int u = 0; u < kDepth; ++u) {
-        const int ci = c00 + 32 * u + lane;
-        vv[u] = ci < nchunk ? __ldg(src + ci) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int u = 0; u < kDepth; ++u) {
-        const int ci = c00 + 32 * u + lane;
-        const uint4 v = vv[u];
-        uint32_t m = ci < nchunk ? outlier_mask8(v, tbits) : 0u;
-        const uint32_t nm = __popc(m);
-        uint32_t incl = nm;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += y;
+        for (int u = 0; u < kDepth; ++u) {
+          const int ci = c00 + 32 * u + lane;
+          vv[u] = ci < nchunk ? __ldg(src + ci) : make_uint4(0u, 0u, 0u, 0u);
         }
-        int64_t ps = b + (incl - nm);
-        while (m) {
-          const int e = __ffs(m) - 1;
-          m &= m - 1;
-          const uint32_t word = e < 4 ? (e < 2 ? v.x : v.y) : (e < 6 ? v.z : v.w);
-          const float x = bf16_bits_to_float((word >> (16 * (e & 1))) & 0xFFFFu);
-          p.col_idx[ps] = ci * 8 + e;
-          p.vals[ps] = __fsub_rn(x, copysignf(t, x));
-          ++ps;
+#pragma unroll
+        for (int u = 0; u < kDepth; ++u) {
+          const int ci = c00 + 32 * u + lane;
+          const uint4 v = vv[u];
+          uint32_t m = ci < nchunk ? outlier_mask8(v, tbits) : 0u;
+          const uint32_t nm = __popc(m);
+          uint32_t incl = nm;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          int64_t ps = b + (incl - nm);
+          while (m) {
+            const int e = __ffs(m) - 1;
+            m &= m - 1;
+            const uint32_t word = e < 4 ? (e < 2 ? v.x : v.y) : (e < 6 ? v.z : v.w);
+            const float x = bf16_bits_to_float((word >> (16 * (e & 1))) & 0xFFFFu);
+            p.col_idx[ps] = ci * 8 + e;
+            p.vals[ps] = __fsub_rn(x, copysignf(t, x));
+            ++ps;
+          }
+          b += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
-        b += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
     }
   }
