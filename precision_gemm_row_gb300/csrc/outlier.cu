@@ -72,11 +72,13 @@ __device__ __forceinline__ uint32_t outlier_mask8(const uint4 v, uint32_t tb) {
 // codes / scales and A_clamped in ONE cooperative kernel (one CTA of 512
 // threads per SM, all resident; grid barriers are bounded waits).
 //
-//  1. pilot: every 64th row of each CTA's row block in a full 32768-bin
-//     histogram, merged into g_pilot;                          -- barrier
-//  2. every CTA derives the same floor F from the pilot: the sample's
-//     magnitude with 4x the requested exceedance (plus 16) above it, so t >= F
-//     unless the sample misleads (then step 4 fills the rest in);
+//  1. pilot: every 64th row of each CTA's row block in a coarse 512-bin
+//     histogram (exponent and the first mantissa bit), merged into g_pilot;
+//                                                               -- barrier
+//  2. every CTA derives the same floor F from the pilot: the lower edge of the
+//     coarse bin holding the sample's magnitude with 4x the requested
+//     exceedance (plus 16) above it, so t >= F unless the sample misleads
+//     (then step 4 fills the rest in);
 //  3. main pass over the CTA's rows: a histogram of the magnitudes >= F only
 //     (a chunk whose 8 magnitudes are all below F costs three packed maxima,
 //     no atomics), merged into g_main, and each row's largest magnitude;
@@ -95,6 +97,8 @@ __device__ __forceinline__ uint32_t outlier_mask8(const uint4 v, uint32_t tb) {
 constexpr int kRThreads = 512;
 constexpr int kRWarps = kRThreads / 32;
 constexpr int kPilotStride = 64;
+constexpr int kCoarseShift = 6;                      // pilot bins: magnitude pattern >> 6 (exponent + 1 mantissa bit)
+constexpr int kCoarseBins = kBins >> kCoarseShift;  // 512
 constexpr int kRU = 8;   // 16-byte chunks a lane per step of the row pass (two steps in flight)
 constexpr int kHU = 16;  // 16-byte loads in flight per lane (histogram passes)
 
@@ -199,6 +203,92 @@ __device__ void rows_histogram(const RowCallParams& p, int64_t r_begin, int64_t 
       if (lane == 0) rmax[row] = mx;
     }
   }
+}
+
+// Pilot: coarse histogram (kCoarseBins bins of the magnitude pattern >>
+// kCoarseShift) of every kPilotStride-th row of [r0, r1), one warp per row,
+// each warp counting into its own kCoarseBins words of `hist` (shared), then
+// merged into g (global).
+__device__ void pilot_phase(const RowCallParams& p, int64_t r0, int64_t r1, uint32_t* hist, uint32_t* g) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int b = threadIdx.x; b < kRWarps * kCoarseBins; b += kRThreads) hist[b] = 0u;
+  __syncthreads();
+  uint32_t* mine = hist + warp * kCoarseBins;
+  const int nchunk = p.K >> 3;
+  for (int64_t row = r0 + int64_t(warp) * kPilotStride; row < r1; row += int64_t(kRWarps) * kPilotStride) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.A + row * p.lda);
+    for (int c00 = 0; c00 < nchunk; c00 += 32 * kRU) {   // every lane takes every step
+      uint4 v[kRU];
+#pragma unroll
+      for (int u = 0; u < kRU; ++u) {
+        const int c = c00 + 32 * u + lane;
+        v[u] = c < nchunk ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kRU; ++u) {
+        if (c00 + 32 * u + lane >= nchunk) continue;
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          atomicAdd(mine + ((w[i] & 0x7FFFu) >> kCoarseShift), 1u);
+          atomicAdd(mine + (((w[i] >> 16) & 0x7FFFu) >> kCoarseShift), 1u);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < kCoarseBins; b += kRThreads) {
+    uint32_t c = 0;
+    for (int w = 0; w < kRWarps; ++w) c += hist[w * kCoarseBins + b];
+    if (c) atomicAdd(g + b, c);
+  }
+}
+
+// Over the kCoarseBins bins of g (global, complete): the lower edge (a
+// magnitude pattern) of the largest coarse bin B with #{coarse bins >= B} >=
+// target, or 0 when there is none.  Computed by warp 0, returned to all
+// threads of the CTA.
+__device__ uint32_t coarse_floor(const uint32_t* g, uint64_t target) {
+  __shared__ uint32_t s_floor;
+  constexpr int kPer = kCoarseBins / 32;   // 16 bins a lane
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    uint32_t c[kPer];
+    unsigned long long sum = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      c[i] = __ldcg(g + lane * kPer + i);
+      sum += c[i];
+    }
+    // suffix over the lanes above: the bins of lanes lane+1 .. 31
+    unsigned long long incl = sum;   // sum of lanes lane .. 31
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    const unsigned long long above = incl - sum;
+    uint32_t f = 0u;
+    bool found = false;
+    if (above < target && incl >= target) {   // the crossing is in this lane's bins
+      unsigned long long run = above;
+      for (int i = kPer - 1; i >= 0; --i) {
+        run += c[i];
+        if (run >= target) {
+          f = uint32_t(lane * kPer + i) << kCoarseShift;
+          found = true;
+          break;
+        }
+      }
+    }
+    const uint32_t who = __ballot_sync(0xFFFFFFFFu, found);
+    f = who ? __shfl_sync(0xFFFFFFFFu, f, __ffs(who) - 1) : 0u;
+    if (lane == 0) s_floor = f;
+  }
+  __syncthreads();
+  const uint32_t r = s_floor;
+  __syncthreads();
+  return r;
 }
 
 // Zeroes hist[lo, hi) (shared), histograms the CTA's rows into it and adds the
@@ -407,16 +497,12 @@ __global__ void __launch_bounds__(kRThreads, 1) rowcall_kernel(const RowCallPara
   uint32_t F = 0;
   const bool use_pilot = e_rank * 4 <= uint64_t(n);   // q > 0.75: the threshold sits in the tail
   if (use_pilot) {
-    histogram_phase(p, r0, r1, kPilotStride, 0u, uint32_t(kBins), hist, p.g_pilot);
+    pilot_phase(p, r0, r1, hist, p.g_pilot);
     ok = grid_sync(p.fctrl, p.wait_ns);
     if (ok) {
       const uint64_t n_pilot = uint64_t(p.n_pilot);
-      uint64_t dummy = 0;
       const double want = 4.0 * double(e_rank) * double(n_pilot) / double(n) + 16.0;
-      if (n_pilot >= 4096 && want < double(n_pilot)) {
-        const int f = suffix_select(p.g_pilot, 0u, uint64_t(want), hist, &dummy, &dummy);
-        F = f < 0 ? 0u : uint32_t(f);
-      }
+      if (n_pilot >= 4096 && want < double(n_pilot)) F = coarse_floor(p.g_pilot, uint64_t(want));
     }
   }
   // ---- 3-4: histogram of the magnitudes >= F, then t
