@@ -5,13 +5,14 @@
 // is nonzero only where clamping happened.
 //
 // One cooperative kernel does it all (rowcall_kernel, below; HBM-bound): a
-// pilot histogram of every 64th row gives a floor under the threshold, a full
-// pass histograms only the magnitudes above the floor (a second pass fills in
-// the rest when the pilot misleads), every CTA selects the exact k-th order
-// statistic t, a row pass writes the row codes / scales, A_clamped on request
-// and each row's first kRowSlots entries (column, A - sign(A) t) into per-row
-// slots, and row_ptr and the CSR follow from per-CTA totals.  Its three or four
-// grid barriers are bounded waits.
+// coarse pilot histogram of every 64th row gives a floor under the threshold,
+// a full pass histograms only the magnitudes above the floor and records each
+// row's largest magnitude (a second pass fills in the rest when the pilot
+// misleads), every CTA selects the exact k-th order statistic t, a streaming
+// row pass writes the row codes / scales, A_clamped on request and each row's
+// first kRowSlots entries (column, A - sign(A) t) into per-row slots, and
+// row_ptr and the CSR follow from per-CTA totals.  Its three or four grid
+// barriers are bounded waits.
 #include <cmath>
 
 #include "common.cuh"
