@@ -473,17 +473,15 @@ def run_gpu(args):
     # their inputs land (an activation's row call before its first linear,
     # dgrad before wgrad), device to host on a third stream as each output is
     # done, so the outputs of one linear go back while the next one's inputs
-    # come in.
-    s_c, s_in, s_out = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    act_index = {id(a): j for j, a in enumerate(plan.acts.values())}
-    nacts = len(act_index)
-    idx = {name: i for i, name in enumerate(LinStep.PHASES)}
-    for k in range(args.warmup + args.steps):
-        flush.fill_(float(k))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s_c)
-        s_in.wait_event(e0)
-        s_out.wait_event(e0)
+    # come in.  Like the device step, the whole of it is one CUDA graph.
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def e2e_ops():
+        main = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(main)
+        s_in.wait_event(fork)
+        s_out.wait_event(fork)
         ev_a, ev_w, ev_g = {}, [], []
         with torch.cuda.stream(s_in):
             for i, l in enumerate(plan.lins):
@@ -500,22 +498,22 @@ def run_gpu(args):
         done_acts = set()
         for i, l in enumerate(plan.lins):
             if id(l.act) not in done_acts:
-                s_c.wait_event(ev_a[id(l.act)])
-                plan.graphs[act_index[id(l.act)]].replay()
+                main.wait_event(ev_a[id(l.act)])
+                l.act.fn()()
                 done_acts.add(id(l.act))
-            base = nacts + len(LinStep.PHASES) * i
-            s_c.wait_event(ev_w[i])
-            plan.graphs[base + idx["fp4_quantize_cols"]].replay()
-            plan.graphs[base + idx["fp4_linear_fwd"]].replay()
+            fns = dict(zip(LinStep.PHASES, l.fns()))
+            main.wait_event(ev_w[i])
+            fns["fp4_quantize_cols"]()
+            fns["fp4_linear_fwd"]()
             ev_y = torch.cuda.Event()
-            ev_y.record(s_c)
-            s_c.wait_event(ev_g[i])
-            plan.graphs[base + idx["fp4_linear_dgrad"]].replay()
+            ev_y.record(main)
+            main.wait_event(ev_g[i])
+            fns["fp4_linear_dgrad"]()
             ev_x = torch.cuda.Event()
-            ev_x.record(s_c)
-            plan.graphs[base + idx["fp4_linear_wgrad_dge"]].replay()
+            ev_x.record(main)
+            fns["fp4_linear_wgrad_dge"]()
             ev_w2 = torch.cuda.Event()
-            ev_w2.record(s_c)
+            ev_w2.record(main)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_y)
                 hY[i].copy_(l.Y, non_blocking=True)
@@ -523,8 +521,22 @@ def run_gpu(args):
                 hdX[i].copy_(l.dX, non_blocking=True)
                 s_out.wait_event(ev_w2)
                 hdW[i].copy_(l.dW, non_blocking=True)
-        s_c.wait_stream(s_out)
-        s_c.wait_stream(s_in)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
+
+    for _ in range(2):
+        e2e_ops()
+    torch.cuda.synchronize()
+    e2e_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(e2e_graph):
+        e2e_ops()
+    s_c = torch.cuda.current_stream()
+    e2e_ms = []
+    for k in range(args.warmup + args.steps):
+        flush.fill_(float(k))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_c)
+        e2e_graph.replay()
         e1.record(s_c)
         e1.synchronize()
         if k >= args.warmup:
