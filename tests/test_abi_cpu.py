@@ -162,3 +162,21 @@ def test_binding_argument_counts_match_header():
         argtypes = getattr(fp4lin._lib, name).argtypes
         assert argtypes is not None, name
         assert len(argtypes) == n, (name, len(argtypes), n)
+
+
+def test_dense_compensation_is_chosen_from_the_entry_bound(lib):
+    """linear_forward multiplies dA densely when the host bound n - ceil(q n)
+    averages at least DENSE_MIN_ROW_ENTRIES entries per row (and K % 64 == 0):
+    the Student-t stress case at q = 0.97 / 0.99 (153 / 51 per row), not the
+    13B layer at q = 0.999 (5 / 14 per row)."""
+    from precision_gemm_row_gb300 import fp4lin
+    assert fp4lin.outlier_max_nnz(16384, 5120, 0.97) == 16384 * 5120 - math.ceil(0.97 * 16384 * 5120)
+    assert fp4lin.use_dense_compensation(16384, 5120, 0.97)
+    assert fp4lin.use_dense_compensation(16384, 5120, 0.99)
+    assert not fp4lin.use_dense_compensation(16384, 5120, 0.999)
+    assert not fp4lin.use_dense_compensation(16384, 13824, 0.999)
+    assert not fp4lin.use_dense_compensation(16384, 5120 + 32, 0.9)      # K % 64 != 0
+    # the boundary: exactly DENSE_MIN_ROW_ENTRIES entries per row on average
+    M, K = 1000, 6400
+    q_at = 1.0 - fp4lin.DENSE_MIN_ROW_ENTRIES / K
+    assert fp4lin.outlier_max_nnz(M, K, q_at) >= fp4lin.DENSE_MIN_ROW_ENTRIES * M - 1
