@@ -13,7 +13,10 @@ weight gradient, input gradient); the non-GEMM parts (RMSNorm, rotary
 embedding, attention softmax, SiLU, residuals) are plain BF16 torch ops, which
 the pages leave in higher precision.  The loss is a stand-in (a squared error
 against a seeded target) and the update plain SGD on fp32 master weights; no
-dataset, no claim about accuracy.
+dataset, no claim about accuracy.  With fp8_grads the weight gradients leave
+the GEMM as E4M3 codes with a per-tensor scale set from the previous step's
+max |dW| (the page's FP8 gradient communication; the first step, with no
+history, uses fp32), and the update uses their dequantized values.
 
 Every linear runs on the CUDA library: without it (or without a GPU) the
 calls fail loudly, there is no fallback.
@@ -45,6 +48,7 @@ class BlockConfig:
     dge_clip: float = 3.0
     lr: float = 0.1
     loss_scale: float = 1.0    # static loss scale (the gradients are unscaled before the update)
+    fp8_grads: bool = False    # weight gradients as E4M3 codes (delayed per-tensor scale), as communicated
     seed: int = 0
 
 
@@ -53,12 +57,12 @@ class _FP4Linear(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, A: torch.Tensor, W_master: torch.Tensor, cfg: BlockConfig, name: str,
-                record: Optional[Dict[str, dict]]):
+                record: Optional[Dict[str, dict]], amax: Optional[Dict[str, torch.Tensor]] = None):
         A = A.contiguous()
         W = W_master.to(torch.bfloat16)
         Y, inter = fp4lin.linear_forward(A, W, cfg.q)
         ctx.save_for_backward(A, W, inter["s_w"])
-        ctx.cfg, ctx.name, ctx.record = cfg, name, record
+        ctx.cfg, ctx.name, ctx.record, ctx.amax = cfg, name, record, amax
         if record is not None:
             record[name] = dict(A=A, W=W, s_w=inter["s_w"], nnz=int(inter["outlier"]["nnz"].item()))
         return Y
@@ -66,11 +70,24 @@ class _FP4Linear(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dY: torch.Tensor):
         A, W, s_w = ctx.saved_tensors
+        cfg = ctx.cfg
         dY = dY.to(torch.bfloat16).contiguous()
-        dX, dW = fp4lin.linear_backward(A, W, dY, s_w, ctx.cfg.dge_k, ctx.cfg.dge_clip)
+        dX = fp4lin.fp4_linear_dgrad(dY, W)
+        prev = ctx.amax.get(ctx.name) if (cfg.fp8_grads and ctx.amax is not None) else None
+        if prev is None:
+            dW = fp4lin.fp4_linear_wgrad_dge(A, dY, W, s_w, cfg.dge_k, cfg.dge_clip)
+            if cfg.fp8_grads and ctx.amax is not None:
+                ctx.amax[ctx.name] = dW.abs().amax().reshape(1)
+        else:
+            # delayed scaling: the previous step's max |dW| sets this step's scale
+            scale = (448.0 / torch.clamp(prev, min=1e-30)).to(torch.float32)
+            codes, amax = fp4lin.fp4_linear_wgrad_dge(A, dY, W, s_w, cfg.dge_k, cfg.dge_clip, dw_type="e4m3",
+                                                     dw_scale=scale)
+            ctx.amax[ctx.name] = amax
+            dW = codes.view(torch.float8_e4m3fn).to(torch.float32) / scale
         if ctx.record is not None:
             ctx.record[ctx.name].update(dY=dY, dW=dW)
-        return dX, dW, None, None, None
+        return dX, dW, None, None, None, None
 
 
 def _rms_norm(x: torch.Tensor, eps: float = 1e-6) -> torch.Tensor:
@@ -109,9 +126,10 @@ class LlamaBlock:
         tokens = torch.randint(0, cfg.vocab, (cfg.batch, cfg.seq), generator=g)
         self.tokens = tokens.to(device)
         self.target = (torch.randn((cfg.batch * cfg.seq, cfg.hidden), generator=g)).to(device, torch.bfloat16)
+        self.amax: Dict[str, torch.Tensor] = {}   # per linear: last step's max |dW| (FP8 gradients)
 
     def _lin(self, x: torch.Tensor, name: str, record) -> torch.Tensor:
-        return _FP4Linear.apply(x, self.W[name], self.cfg, name, record)
+        return _FP4Linear.apply(x, self.W[name], self.cfg, name, record, self.amax)
 
     def forward(self, record: Optional[Dict[str, dict]] = None) -> torch.Tensor:
         c = self.cfg
