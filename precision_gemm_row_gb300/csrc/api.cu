@@ -130,7 +130,7 @@ FP4_API const char* fp4_status_string(fp4_status s) {
   return "FP4_ERR_UNKNOWN";
 }
 
-FP4_API int fp4_abi_version(void) { return 1; }
+FP4_API int fp4_abi_version(void) { return 2; }   // 2: fp4_linear_wgrad_dge takes dw_type, dw_scale, dw_amax
 
 FP4_API const char* fp4_last_cuda_error(void) { return fp4::last_cuda_error(); }
 

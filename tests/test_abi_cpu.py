@@ -53,7 +53,7 @@ def test_status_strings(lib):
     assert lib.fp4_status_string(0) == b"FP4_OK"
     assert lib.fp4_status_string(6) == b"FP4_ERR_TIMEOUT"
     assert lib.fp4_status_string(123) == b"FP4_ERR_UNKNOWN"
-    assert lib.fp4_abi_version() == 1
+    assert lib.fp4_abi_version() == 2
 
 
 def test_outlier_max_nnz_is_n_minus_rank(lib):
