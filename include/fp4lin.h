@@ -302,7 +302,7 @@ size_t fp4_linear_fwd_dense_workspace(int64_t M, int64_t N, int64_t K);
  * BF16 parts per entry whose sum is the fp32 entry exactly -- two (A and
  * -sign(A) t) when the clamp threshold t is given, else three (hi + mid + lo)
  * -- and multiplied by the BF16 W on the BF16 tensor cores (fp32 accumulation
- * in 1024-term chunks, about 1e-6 of the sum of |terms| per output); the sum
+ * in 2048-term chunks, about 2e-6 of the sum of |terms| per output); the sum
  * of the two products is rounded once to the output type.
  * Choose it over fp4_linear_fwd when dA averages tens of entries per row or
  * more (its cost does not depend on nnz); fp4_linear_fwd is faster for a few
@@ -401,7 +401,7 @@ size_t fp4_linear_wgrad_dge_workspace(int64_t M, int64_t N, int64_t K);
  * This is the chain rule of Y = A W, the plainest reading that closes the
  * linear's backward: the same BF16 engine as fp4_linear_wgrad_dge, with the
  * BF16 W the caller passes (the unquantized weight, as the compensation uses).
- * The reduction over N runs in 1024-element chunks summed in fp32 registers.
+ * The reduction over N runs in 2048-element chunks summed in fp32 registers.
  *
  *   dY  device BF16 M x lddy (tokens x out), 16-byte aligned, lddy % 8 == 0
  *   W   device BF16 K x ldw (in x out), 16-byte aligned, ldw % 8 == 0

@@ -17,7 +17,9 @@
 // error), which would exceed 1e-5 at 16k.  The reduction range of every tile is
 // therefore split into chunks of kChunkStages x 64; each chunk is accumulated in
 // one of two TMEM buffers and the epilogue warps add it into fp32 registers
-// (round to nearest), so the error stays at the chunk level.  While the
+// (round to nearest), so the error stays at the chunk level (chunks of 2048
+// products: about 2e-6 of the sum, against 1e-6 for 1024 and 4.4e-6 for 4096,
+// measured on the 13B shapes, where 2048 was 1-5% faster than 1024).  While the
 // epilogue drains one buffer the MMA warp fills the other.
 //
 // Roles (18 warps): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
@@ -69,7 +71,7 @@ constexpr int kMmaT = 16;     // reduction elements per MMA (BF16 K = 16)
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + 32 * kEpiWarps;   // 576 (18 warps: up to 5 per scheduler, so 96 registers)
 constexpr int kNAcc = 2;
-constexpr int kChunkStages = 16;                 // 1024 reduction elements per TMEM accumulation chunk
+constexpr int kChunkStages = 32;                 // 2048 reduction elements per TMEM accumulation chunk
 constexpr int kEpiCols = kBN / (kEpiWarps / 4);  // columns per epilogue warp (64)
 constexpr int kBlk = 32;                         // epilogue block: 32 rows x 32 columns per warp,
 constexpr int kHalf = 16;                        // staged 16 rows at a time

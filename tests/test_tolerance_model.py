@@ -3,7 +3,7 @@
 The input gradient dX = dY W^T is a BF16 product summed on the tensor core.  Its
 parity tests allow 1 BF16 ulp plus TC_SUM_BOUND x sum |terms| per output
 (tests/gpu_common.py).  The bound follows from an accumulation model:
-  * the reduction is split into chunks of 1024 terms (64 MMA steps of 16),
+  * the reduction is split into chunks of 2048 terms (128 MMA steps of 16),
     each accumulated in fp32 in tensor memory;
   * every MMA step forms its 16-term sum and adds it to the fp32 accumulator,
     and both the step's sum and the add may truncate (round toward zero):
@@ -11,8 +11,8 @@ parity tests allow 1 BF16 ulp plus TC_SUM_BOUND x sum |terms| per output
     chunk's sum of |terms|;
   * the chunk sums are added in fp32 registers with round to nearest (2^-24
     of at most the whole sum of |terms| per add).
-So |error| <= (2 * 64 * 2^-23 + n_chunks * 2^-24) sum |terms|, which for the
-longest reduction here (16384 terms, 16 chunks) is 129 * 2^-23 < 2^-15.
+So |error| <= (2 * 128 * 2^-23 + n_chunks * 2^-24) sum |terms|, which for the
+longest reduction here (16384 terms, 8 chunks) is 260 * 2^-23 < 2^-14.
 
 The tests below run that model in numpy (exact products in fp64, truncating
 fp32 adds) on data shaped like the 13B layer's input gradient and on
@@ -25,7 +25,7 @@ import pytest
 from precision_gemm_row_gb300 import workloads as wl
 from tests.gpu_common import TC_SUM_BOUND
 
-CHUNK, STEP = 1024, 16
+CHUNK, STEP = 2048, 16
 
 
 def _rz_f32(x: np.ndarray) -> np.ndarray:
@@ -38,7 +38,7 @@ def _rz_f32(x: np.ndarray) -> np.ndarray:
 
 def _tensor_core_sum_model(terms: np.ndarray) -> np.ndarray:
     """Row sums of `terms` (rows x L, exact fp64 products) as the model above
-    forms them: truncating fp32 accumulation of 16-term steps per 1024-term
+    forms them: truncating fp32 accumulation of 16-term steps per 2048-term
     chunk, chunks added in fp32 with round to nearest."""
     rows, L = terms.shape
     total = np.zeros(rows, np.float32)
