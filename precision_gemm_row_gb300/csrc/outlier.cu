@@ -641,15 +641,17 @@ __global__ void __launch_bounds__(kRThreads, 1) rowcall_kernel(const RowCallPara
   }
   __syncthreads();   // this CTA's row_ptr entries are visible to all its threads
   if (p.cap == 0) return;
-  // rows with more entries than slots: read again from A, one warp per row (a
-  // warp finds them 32 rows at a time)
-  for (int64_t g0 = r0 + 32 * int64_t(warp); g0 < r1; g0 += 32 * int64_t(kRWarps)) {
-    const int32_t myc = g0 + lane < r1 ? __ldcg(p.row_cnt + g0 + lane) : 0;
+  // rows with more entries than slots: read again from A, one warp per row;
+  // warp w takes rows r0 + w + kRWarps t, finding the long ones among 32
+  // values of t at a time (so all warps share the work when every row is long)
+  for (int64_t first = r0 + warp; first < r1; first += 32 * int64_t(kRWarps)) {
+    const int64_t myrow = first + int64_t(kRWarps) * lane;
+    const int32_t myc = myrow < r1 ? __ldcg(p.row_cnt + myrow) : 0;
     uint32_t longrows = __ballot_sync(0xFFFFFFFFu, myc > kRowSlots);
     while (longrows) {   // warp-uniform
       const int l = __ffs(longrows) - 1;
       longrows &= longrows - 1;
-      const int64_t row = g0 + l;
+      const int64_t row = first + int64_t(kRWarps) * l;
       const int32_t nr = __shfl_sync(0xFFFFFFFFu, myc, l);
       const int64_t dst = p.row_ptr[row];
       if (dst + nr > p.cap) continue;   // beyond the capacity: flagged above
