@@ -15,7 +15,8 @@
 // Accumulation precision: the tensor core's fp32 accumulation drifts by about
 // 1e-9 x (number of accumulated products) relative (a biased, truncation-like
 // error), which would exceed 1e-5 at 16k.  The reduction range of every tile is
-// therefore split into chunks of kChunkStages x 64; each chunk is accumulated in
+// therefore split into chunks of 32 x 64 (16 x 64 where a split tail's halves
+// come out more even that way); each chunk is accumulated in
 // one of two TMEM buffers and the epilogue warps add it into fp32 registers
 // (round to nearest), so the error stays at the chunk level (chunks of 2048
 // products: about 2e-6 of the sum, against 1e-6 for 1024 and 4.4e-6 for 4096,
@@ -71,7 +72,8 @@ constexpr int kMmaT = 16;     // reduction elements per MMA (BF16 K = 16)
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + 32 * kEpiWarps;   // 576 (18 warps: up to 5 per scheduler, so 96 registers)
 constexpr int kNAcc = 2;
-constexpr int kChunkStages = 32;                 // 2048 reduction elements per TMEM accumulation chunk
+constexpr int kChunkLong = 32;    // stages (of 64) per TMEM accumulation chunk: 2048 reduction elements,
+constexpr int kChunkShort = 16;   // or 1024 when a split tail would halve an odd number of long chunks
 constexpr int kEpiCols = kBN / (kEpiWarps / 4);  // columns per epilogue warp (64)
 constexpr int kBlk = 32;                         // epilogue block: 32 rows x 32 columns per warp,
 constexpr int kHalf = 16;                        // staged 16 rows at a time
@@ -106,6 +108,7 @@ struct Cfg {
 
 struct Shape {
   int R, C, L;        // output rows, output columns, reduction length
+  int chunk;          // stages per accumulation chunk (kChunkLong or kChunkShort; plan_split picks it)
   int q_wrap;         // > 0: Q's reduction index is taken modulo q_wrap (a multiple of kBT), so
                       // P's reduction may hold several parts that all meet the same Q; 0: none
   int whole, split;   // tiles computed whole, then `split` tiles computed as two halves
@@ -199,7 +202,8 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
   const int num_r = (p.R + kTileR - 1) / kTileR;
   const int num_n = (p.C + kBN - 1) / kBN;
   const int lblocks = (p.L + kBT - 1) / kBT;
-  const int nchunks = (lblocks + kChunkStages - 1) / kChunkStages;
+  const int chunk_stages = p.chunk;
+  const int nchunks = (lblocks + chunk_stages - 1) / chunk_stages;
   const int pair_id = int(blockIdx.x) / C::kCtas, npairs = int(gridDim.x) / C::kCtas;
 
   if (warp == 0) {
@@ -214,8 +218,8 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
       tile_coords(w.tile, num_r, num_n, rb, nb);
       const int arow = rb * kTileR + int(rank) * kBM;          // this CTA's 128 rows of P
       const int bcol = nb * kBN + int(rank) * C::kBCols;       // this CTA's rows of Q
-      const int lb_end = w.c1 * kChunkStages < lblocks ? w.c1 * kChunkStages : lblocks;
-      for (int lb = w.c0 * kChunkStages; lb < lb_end; ++lb) {
+      const int lb_end = w.c1 * chunk_stages < lblocks ? w.c1 * chunk_stages : lblocks;
+      for (int lb = w.c0 * chunk_stages; lb < lb_end; ++lb) {
         if (!mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_ns)) {
           ok = false;
           break;
@@ -267,8 +271,8 @@ __device__ __forceinline__ void run(const CUtensorMap& tmA, const CUtensorMap& t
     Work w;
     for (int k = 0; ok && work_item(k, pair_id, npairs, nchunks, p, w); ++k) {
       for (int ch = w.c0; ch < w.c1 && ok; ++ch) {
-        const int lb0 = ch * kChunkStages;
-        const int lb1 = lb0 + kChunkStages < lblocks ? lb0 + kChunkStages : lblocks;
+        const int lb0 = ch * chunk_stages;
+        const int lb1 = lb0 + chunk_stages < lblocks ? lb0 + chunk_stages : lblocks;
         if (!mbar_wait_warp(acce0 + 8 * acc, acc_phase ^ 1u, p.wait_ns)) {
           ok = false;
           break;
@@ -454,17 +458,36 @@ inline bool use_pairs(int64_t red) { return red >= 2048; }
 // with `sms` SMs: [counters, 256-byte aligned][partial sums].
 struct SplitPlan {
   int64_t tiles, units, whole, split;
+  int chunk;   // stages per accumulation chunk when the split tail runs
   size_t cnt_bytes, part_bytes, total;
 };
+
+// Stages of the longer half when a tile of `stages` stages is split at the
+// middle chunk boundary (chunks of `chunk` stages; as work_item splits them).
+inline int64_t split_half_stages(int64_t stages, int chunk) {
+  const int64_t nchunks = (stages + chunk - 1) / chunk;
+  const int64_t h0 = (nchunks / 2) * chunk < stages ? (nchunks / 2) * chunk : stages;
+  return h0 > stages - h0 ? h0 : stages - h0;
+}
 
 inline SplitPlan plan_split(int64_t rows, int64_t cols, int64_t red, int sms) {
   const int ctas = use_pairs(red) ? 2 : 1;
   SplitPlan sp{};
   sp.tiles = ((rows + kBM * ctas - 1) / (kBM * ctas)) * ((cols + kBN - 1) / kBN);
   sp.units = sms / ctas;
-  const int64_t nchunks = ((red + kBT - 1) / kBT + kChunkStages - 1) / kChunkStages;
+  const int64_t stages = (red + kBT - 1) / kBT;
   const int64_t rem = sp.tiles % sp.units;
-  sp.split = (nchunks >= 2 && rem > 0 && 2 * rem <= sp.units) ? rem : 0;
+  const bool tail = rem > 0 && 2 * rem <= sp.units;
+  // long chunks, unless the split tail's halves would come out more even with
+  // short ones (the tail's time is its longer half); the choice depends on the
+  // shape only, so a call with and without a workspace sums the same chunks
+  const int64_t nlong = (stages + kChunkLong - 1) / kChunkLong, nshort = (stages + kChunkShort - 1) / kChunkShort;
+  sp.chunk = kChunkLong;
+  if (tail && nshort >= 2 &&
+      (nlong < 2 || split_half_stages(stages, kChunkShort) < split_half_stages(stages, kChunkLong)))
+    sp.chunk = kChunkShort;
+  const int64_t nchunks = (stages + sp.chunk - 1) / sp.chunk;
+  sp.split = (tail && nchunks >= 2) ? rem : 0;
   sp.whole = sp.tiles - sp.split;
   sp.cnt_bytes = (size_t(sp.split) * ctas * kEpiWarps * 4 + 255) / 256 * 256;
   sp.part_bytes = size_t(2 * sp.split) * ctas * kEpiWarps * kEpiCols * 32 * 4;
@@ -472,13 +495,12 @@ inline SplitPlan plan_split(int64_t rows, int64_t cols, int64_t red, int sms) {
   return sp;
 }
 
-// Checks the caller's workspace against the plan and fills the schedule of
-// `s`: the split tail when the workspace is given, else every tile whole.
 inline fp4_status schedule(Shape& s, const SplitPlan& sp, void* workspace, size_t ws_bytes, cudaStream_t cs) {
   s.whole = int(sp.tiles);
   s.split = 0;
   s.part = nullptr;
   s.cnt = nullptr;
+  s.chunk = sp.chunk;   // a function of the shape alone, with or without the split
   if (workspace == nullptr || sp.split == 0) return FP4_OK;
   if (ws_bytes < sp.total) return FP4_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FP4_ERR_ALIGNMENT;

@@ -240,8 +240,9 @@ def test_wgrad_dge(fp4, M, K, N, k, clip, workspace):
     """A single token (M = 1) and the smallest K, N; M >= 2048 tokens runs the GEMM
     as CTA pairs (256-row dW tiles; K = 200, 520 and 384 leave partial pair
     tiles, N = 264 / 136 partial column tiles).  With a
-    workspace, these few-tile shapes with 2 or more 2048-token chunks (M = 2304
-    and up) compute every tile as two halves of the token range."""
+    workspace, these few-tile shapes with 2 or more 1024-token chunks (M = 1500
+    and up) compute every tile as two halves of the token range (in 2048- or
+    1024-token chunks, whichever halves it more evenly)."""
     A_bits = _normal_bits(M + 1, (M, K))
     dY_bits = _normal_bits(N + 2, (M, N), 1e-3)
     W_bits = _normal_bits(K + 3, (K, N), 0.02)
@@ -271,9 +272,10 @@ def test_dgrad(fp4, M, N, K, out, workspace):
     """N >= 2048 (a long reduction) runs CTA pairs (256-row tiles); M = 200, 1000,
     300, 2304, 513 leave partial row tiles, K = 136, 392, 264, 520, 8 partial
     column tiles, N = 264, 72, 1096, 2056, 4104 a partial last stage of 64.
-    With a workspace, shapes with 2 or more 2048-element chunks (N = 2056 and
-    up) split their few tiles into two halves of the N range (N = 4104 gives
-    halves of 1 and 2 chunks)."""
+    With a workspace, shapes with 2 or more 1024-element chunks (N = 1096 and
+    up) split their few tiles into two halves of the N range (N = 2056 in
+    1024-element chunks, halves of 1 and 2; N = 4104 in 2048-element chunks,
+    halves of 1 and 2)."""
     dY_bits = _normal_bits(M + 7, (M, N), 1e-3)
     W_bits = _normal_bits(K + 11, (K, N), 0.02)
     dX = fp4.fp4_linear_dgrad(dev_bf16(dY_bits), dev_bf16(W_bits),
